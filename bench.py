@@ -1,0 +1,339 @@
+"""Benchmark of the routed-expert VQ2 MoE layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole layer (router logits, top-k, permutation,
+expert FFN, combine) over one batch of synthetic tokens, for each layer of
+the workload.  Default workload: decode batch 1 (hidden 4096, intermediate
+2048, 256 experts, top-8, all experts resident, 4 independent layers).  The
+value is MoE-layer tokens per second (tokens x layers / time).  Inputs
+already sit in HBM when the timed region starts; the e2e figure adds the
+pinned-host -> device copy of each step's tokens and the device -> host copy
+of the layer outputs.  The roofline entry covers the expert-FFN call
+(moe_vq2_expert_ffn: its schedule, FC1 and FC2 kernels), with the code +
+scale bytes of each distinct expert touched as algorithmic bytes.
+--impl reference times the CPU oracle on the same workload and metric.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU (the layer has no exchange step); the slowest rank's time counts.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth as ms  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and achieved HBM GB/s of VQ2 code reads vs ~8 TB/s (1 GB300)"
+UNIT = "layer-tokens/s"
+VQ2_EXPERT_BYTES = 6_684_672     # codes + scales, gate + up + down, H=4096 I=2048
+FP4_EXPERT_BYTES = 13_369_344
+L2_BYTES = 129 * 2 ** 20
+
+WORKLOADS = {
+    "decode_b1": dict(T=1, layers=4, zipf=None, fp4_top=0, pool=64,
+                      desc="decode batch 1: H4096 I2048 E256 top-8 softmax, all 256 experts resident, "
+                           "4 layers with independent seeded weights"),
+    "decode_b32_zipf": dict(T=32, layers=1, zipf=1.1, fp4_top=0, pool=8,
+                            desc="decode batch 32, Zipf(1.1) router bias, H4096 I2048 E256 top-8"),
+    "mixed_fp4_b8": dict(T=8, layers=1, zipf=1.1, fp4_top=52, pool=8,
+                         desc="decode batch 8, 52 most routed experts FP4 (MXFP4), 204 VQ2, Zipf(1.1)"),
+    "prefill_4096": dict(T=4096, layers=1, zipf=1.1, fp4_top=0, pool=1,
+                         desc="prefill chunk 4096 tokens, Zipf(1.1), H4096 I2048 E256 top-8"),
+}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def make_layers(wl):
+    return [ms.Layer(ms.spec_decode(L, zipf_s=wl["zipf"], fp4_top=wl["fp4_top"])) for L in range(wl["layers"])]
+
+
+def token_pool(wl, L):
+    return ms.tokens(wl["T"] * wl["pool"], 4096, seed=1000 + L).reshape(wl["pool"], wl["T"], 4096)
+
+
+# --------------------------------------------------------------- CPU oracle arm
+
+def oracle_time(wl, layers, budget_s: float, max_steps: int):
+    """Times the CPU oracle over whole steps (every layer, one batch each)
+    until the budget is spent.  Weights are drawn before the clock starts."""
+    import oracle
+    O = oracle.default
+    cores = O.set_threads(os.cpu_count() or 1)
+    pools = [token_pool(wl, L) for L in range(len(layers))]
+    T = wl["T"]
+    if T > 64:  # prefill: a bounded token sample of the chunk
+        sample = np.arange(0, T, T // 16)[:16]
+    else:
+        sample = None
+    # draw the experts each step needs before timing
+    for s in range(max_steps):
+        for L, layer in enumerate(layers):
+            x = pools[L][s % wl["pool"]]
+            lg = O.router_logits(x, layer.w_router, layer.bias)
+            ids, _ = O.route_topk(lg, layer.spec.k, 1)
+            sel = ids if sample is None else ids[sample]
+            for e in np.unique(sel):
+                layer.expert(int(e))
+    done, t0, tok = 0, time.perf_counter(), 0
+    while done < max_steps:
+        for L, layer in enumerate(layers):
+            x = pools[L][done % wl["pool"]]
+            r = O.moe_layer(layer, x, tokens=sample)
+            tok += len(r["tokens"])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    what = f"{done} step(s) x {len(layers)} layer(s) x {T if sample is None else len(sample)} token(s)"
+    if sample is not None:
+        what += f" (token sample of the {T}-token chunk; routing of all {T} tokens included)"
+    return tok / el, cores, what, done, el
+
+
+# --------------------------------------------------------------- GPU arm
+
+def run_gpu(args, wl, world, rank, local):
+    import torch
+    import bit_vq_routed_gb300 as bv
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    layers = make_layers(wl)
+    T, nL = wl["T"], len(layers)
+    devs, keeps = [], []
+    for layer in layers:
+        s = layer.spec
+        dev, keep = bv.upload_layer(s.H, s.I, s.E, s.k, T, layer.codebook, layer.w_router, layer.bias,
+                                    lambda e, L=layer: (lambda ex: (ex.fmt, ex.codes, ex.scales))(
+                                        L.expert(e, cache=False)))
+        devs.append(dev)
+        keeps.append(keep)
+    pools = [torch.from_numpy(token_pool(wl, L)).view(torch.bfloat16).cuda() for L in range(nL)]
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step(s, evs=None):
+        for L, dev in enumerate(devs):
+            x = pools[L][s % wl["pool"]]
+            dev.route(x)
+            if evs is not None:
+                evs[L][0].record(stream)
+            dev.experts(x, bv.MOE_PER_PAIR)
+            if evs is not None:
+                evs[L][1].record(stream)
+            bv.moe_combine(dev.ypair[:T * dev.k], dev.pair_to_sorted[:T * dev.k], dev.weights[:T],
+                           dev.pair_status[:T * dev.k], dev.k, dev.out[:T])
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ffn_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nL)]
+              for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for s in range(args.steps):
+        step(args.warmup + s, ffn_ev[s])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_total = start.elapsed_time(end)
+    ffn_ms = [ffn_ev[s][L][0].elapsed_time(ffn_ev[s][L][1]) for s in range(args.steps) for L in range(nL)]
+    # distinct experts touched per FFN launch (read back after timing)
+    code_bytes = []
+    for s in range(args.steps):
+        for L, dev in enumerate(devs):
+            dev.route(pools[L][(args.warmup + s) % wl["pool"]])
+            ids = np.unique(dev.ids[:T].cpu().numpy())
+            fmts = layers[L].formats[ids]
+            code_bytes.append(int((fmts == ms.FMT_VQ2).sum()) * VQ2_EXPERT_BYTES
+                              + int((fmts == ms.FMT_FP4).sum()) * FP4_EXPERT_BYTES)
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+
+    # end to end through the public API: pinned host tokens in, outputs out
+    host_in = [torch.from_numpy(token_pool(wl, L)).view(torch.bfloat16).pin_memory() for L in range(nL)]
+    host_out = torch.empty(nL, T, 4096, dtype=torch.float32).pin_memory()
+    dev_in = [torch.empty(T, 4096, dtype=torch.bfloat16, device="cuda") for _ in range(nL)]
+    e2e_steps = args.steps
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(e2e_steps):
+        for L, dev in enumerate(devs):
+            dev_in[L].copy_(host_in[L][s % wl["pool"]], non_blocking=True)
+            out = dev.forward(dev_in[L])
+            host_out[L].copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+        torch.distributed.destroy_process_group()
+    return dict(ms_total=ms_total, ffn_ms=ffn_ms, code_bytes=code_bytes, clocks=clk, e2e_ms=e2e_ms,
+                e2e_steps=e2e_steps, launches_per_layer=7)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode_b1", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing (profiling runs)")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+    wl = dict(WORKLOADS[args.workload])
+    if args.layers:
+        wl["layers"] = args.layers
+    config = {"workload": wl["desc"], "name": args.workload, "tokens_per_step": wl["T"],
+              "layers_per_step": wl["layers"],
+              "l2": f"inputs larger than L2: each step touches its layers' routed experts "
+                    f"(>= {wl['layers'] * 8 * VQ2_EXPERT_BYTES / 1e6:.0f} MB vs 129 MB L2), tokens rotate "
+                    f"over a pool of {wl['pool']} batches per layer"}
+    T, nL = wl["T"], wl["layers"]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        layers = make_layers(wl)
+        max_steps = args.warmup + args.steps
+        tps, cores, what, done, el = oracle_time(wl, layers, budget_s=max(5.0, args.cpu_budget), max_steps=max_steps)
+        line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": args.gpus,
+                "steps": done, "warmup": 0, "ms_per_step": 1000 * el / max(done, 1),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded; random weights, no trained checkpoint)", "config": config,
+                "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what},
+                "e2e": {"value": tps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    r = run_gpu(args, wl, world, rank, local)
+    if rank != 0:
+        return
+    hbm, bf16, peak_src = measured_peaks()
+    ms_step = r["ms_total"] / args.steps
+    value = T * nL * world / (ms_step / 1000.0)
+    ffn_avg_ms = float(np.mean(r["ffn_ms"]))
+    bytes_avg = float(np.mean(r["code_bytes"]))
+    achieved = bytes_avg / (ffn_avg_ms / 1000.0) / 1e9
+    e2e_value = T * nL * world / (r["e2e_ms"] / r["e2e_steps"] / 1000.0)
+    if args.no_cpu:
+        tps, cores, what = None, None, "skipped (--no-cpu)"
+    else:
+        layers = make_layers(wl)
+        tps, cores, what, done, el = oracle_time(wl, layers, budget_s=args.cpu_budget, max_steps=4)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16*f16->f32 (bf16 activations)",
+        "data": "synthetic (seeded; random weights, no trained checkpoint)", "config": config,
+        "roofline": {"bound": "hbm", "kernel": "moe_vq2_expert_ffn (schedule + FC1 + FC2 launches)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)", "traffic": None,
+                     "algorithmic_bytes_per_launch": bytes_avg, "avg_launch_ms": ffn_avg_ms},
+        "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * 4096 * 2 * nL,
+                "d2h_bytes_per_step": T * 4096 * 4 * nL},
+        "gpu_launches": r["launches_per_layer"] * nL * args.steps,
+        "clocks": r["clocks"],
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

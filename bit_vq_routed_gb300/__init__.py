@@ -1,0 +1,223 @@
+"""Python binding of libmoe_vq2.so, the GB300 (sm_103a) routed-expert VQ2 MoE
+layer library.  Argument marshalling only: every step of the layer runs in
+the library's CUDA kernels; PyTorch provides device memory and streams.
+
+The functions carry the names of the C ABI in ``include/moe_vq2.h`` and take
+CUDA tensors (any dtype of the right element size: bf16 activations as
+``torch.bfloat16``, fp16 codebook/scales as ``torch.float16``, codes and
+ue8m0 scales as ``torch.uint8``).  A non-zero status raises ``MoeError``
+with the library's message.  There is no CPU or PyTorch fallback: if the
+shared library cannot be built or loaded, the import of the functions fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_CUDA = -3
+MOE_ERR_NO_MEM = -4
+MOE_ERR_WORKSPACE = -5
+MOE_ERR_TIMEOUT = -6
+MOE_ERR_MISMATCH = -7
+
+MOE_FMT_VQ2 = 0
+MOE_FMT_FP4 = 1
+MOE_FUSED_SCATTER = 0
+MOE_PER_PAIR = 1
+
+LIB_PATH = _build.LIB
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"status {status}: {msg}")
+        self.status = status
+
+
+class _ExpertDesc(ctypes.Structure):
+    _fields_ = [("format", ctypes.c_int), ("codes", ctypes.c_void_p * 3), ("scales", ctypes.c_void_p * 3)]
+
+
+_lib = None
+
+EXPORTED = [
+    "moe_version", "moe_last_error", "moe_vq2_pack", "moe_fp4_pack", "moe_slot_table_create",
+    "moe_slot_table_set", "moe_slot_table_evict", "moe_slot_table_destroy", "moe_router_logits",
+    "moe_route_topk", "moe_permute_workspace_size", "moe_permute",
+    "moe_vq2_expert_ffn_workspace_size", "moe_vq2_expert_ffn", "moe_combine",
+]
+
+
+def load(path: Optional[str] = None, build_if_stale: bool = True):
+    """Loads (building it first if it is missing or older than its sources)
+    the shared library and declares the C signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if path is None and build_if_stale and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with bit_vq_routed_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "moe_version": ([], I),
+        "moe_last_error": ([], ctypes.c_char_p),
+        "moe_vq2_pack": ([P, P, I, I, P, P, P], I),
+        "moe_fp4_pack": ([P, P, I, I, P, P, P], I),
+        "moe_slot_table_create": ([I, I, I, P, ctypes.POINTER(P)], I),
+        "moe_slot_table_set": ([P, I, ctypes.POINTER(_ExpertDesc), P], I),
+        "moe_slot_table_evict": ([P, I, P], I),
+        "moe_slot_table_destroy": ([P], I),
+        "moe_router_logits": ([P, P, P, P, I, I, I, P], I),
+        "moe_route_topk": ([P, I, I, I, I, P, P, P], I),
+        "moe_permute_workspace_size": ([I, I, I], Z),
+        "moe_permute": ([P, I, I, I, P, P, P, P, Z, P], I),
+        "moe_vq2_expert_ffn_workspace_size": ([I, I, I, I], Z),
+        "moe_vq2_expert_ffn": ([P, P, P, P, P, I, I, I, P, P, P, Z, P], I),
+        "moe_combine": ([P, P, P, P, I, I, I, P, P, P], I),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        raise MoeError(status, load().moe_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ------------------------------------------------------------------ formats
+
+def moe_vq2_pack(codes, scales, packed_codes, packed_scales, stream=None):
+    rows, G = codes.shape
+    _check(load().moe_vq2_pack(_ptr(codes), _ptr(scales), rows, 4 * G, _ptr(packed_codes),
+                               _ptr(packed_scales), _stream(stream)))
+
+
+def moe_fp4_pack(codes, scales, packed_codes, packed_scales, stream=None):
+    rows, nb = codes.shape
+    _check(load().moe_fp4_pack(_ptr(codes), _ptr(scales), rows, 2 * nb, _ptr(packed_codes),
+                               _ptr(packed_scales), _stream(stream)))
+
+
+class SlotTable:
+    """moe_slot_table_create / _set / _evict / _destroy.  Keeps references to
+    the tensors of every set entry so they outlive the table's use of them."""
+
+    def __init__(self, num_experts: int, H: int, I: int, codebook: torch.Tensor):
+        self.lib = load()
+        self.codebook = codebook
+        self.E, self.H, self.I = num_experts, H, I
+        h = ctypes.c_void_p()
+        _check(self.lib.moe_slot_table_create(num_experts, H, I, _ptr(codebook), ctypes.byref(h)))
+        self.handle = h
+        self._keep = {}
+
+    def set(self, expert_id: int, fmt: int, codes: Sequence[torch.Tensor], scales: Sequence[torch.Tensor],
+            stream=None):
+        d = _ExpertDesc()
+        d.format = fmt
+        for m in range(3):
+            d.codes[m] = _ptr(codes[m])
+            d.scales[m] = _ptr(scales[m])
+        _check(self.lib.moe_slot_table_set(self.handle, expert_id, ctypes.byref(d), _stream(stream)))
+        self._keep[expert_id] = (list(codes), list(scales))
+
+    def evict(self, expert_id: int, stream=None):
+        _check(self.lib.moe_slot_table_evict(self.handle, expert_id, _stream(stream)))
+
+    def destroy(self):
+        if self.handle is not None:
+            _check(self.lib.moe_slot_table_destroy(self.handle))
+            self.handle = None
+            self._keep.clear()
+
+    def __del__(self):
+        try:
+            if self.handle is not None and torch.cuda.is_initialized():
+                torch.cuda.synchronize()
+                self.destroy()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------------ hot path
+
+def moe_router_logits(x, w_router, bias, logits, stream=None):
+    T, H = x.shape
+    E = w_router.shape[0]
+    _check(load().moe_router_logits(_ptr(x), _ptr(w_router), _ptr(bias), _ptr(logits), T, H, E,
+                                    _stream(stream)))
+
+
+def moe_route_topk(logits, k: int, renormalize: int, ids, weights, stream=None):
+    T, E = logits.shape
+    _check(load().moe_route_topk(_ptr(logits), T, E, k, renormalize, _ptr(ids), _ptr(weights),
+                                 _stream(stream)))
+
+
+def moe_permute_workspace_size(T: int, k: int, E: int) -> int:
+    return load().moe_permute_workspace_size(T, k, E)
+
+
+def moe_permute(ids, E: int, expert_offsets, sorted_pair, pair_to_sorted, ws=None, stream=None):
+    T, k = ids.shape
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().moe_permute(_ptr(ids), T, k, E, _ptr(expert_offsets), _ptr(sorted_pair),
+                              _ptr(pair_to_sorted), _ptr(ws), nbytes, _stream(stream)))
+
+
+def moe_vq2_expert_ffn_workspace_size(T: int, k: int, E: int, I: int) -> int:
+    return load().moe_vq2_expert_ffn_workspace_size(T, k, E, I)
+
+
+def moe_vq2_expert_ffn(table: SlotTable, x, expert_offsets, sorted_pair, weights, k: int, mode: int,
+                       out, pair_status, ws, stream=None):
+    T = x.shape[0]
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().moe_vq2_expert_ffn(table.handle, _ptr(x), _ptr(expert_offsets), _ptr(sorted_pair),
+                                     _ptr(weights), T, k, mode, _ptr(out), _ptr(pair_status), _ptr(ws),
+                                     nbytes, _stream(stream)))
+
+
+def moe_combine(ypair, pair_to_sorted, weights, pair_status, k: int, out_f32=None, out_bf16=None,
+                stream=None):
+    T = weights.shape[0]
+    H = ypair.shape[1]
+    _check(load().moe_combine(_ptr(ypair), _ptr(pair_to_sorted), _ptr(weights), _ptr(pair_status), T, k,
+                              H, _ptr(out_f32), _ptr(out_bf16), _stream(stream)))
+
+
+from .layer import MoELayer, upload_layer  # noqa: E402  (the layer helper uses the functions above)

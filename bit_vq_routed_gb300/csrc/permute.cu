@@ -1,0 +1,98 @@
+// Token -> expert permutation: histogram, exclusive scan, stable scatter.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int PT = 1024;  // threads of the single CTA
+
+// One CTA.  Shared memory: cursor[E] then wcnt[32][E] (per-warp counts of a
+// 1024-pair chunk).  Pairs are scattered chunk by chunk in increasing p;
+// inside a chunk a pair's rank among the pairs of its expert is the count
+// in lower warps plus the count in lower lanes of its own warp, so equal
+// ids keep their pair order (a stable counting sort).
+__global__ void __launch_bounds__(PT) permute_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                                     int32_t* __restrict__ offsets,
+                                                     int32_t* __restrict__ sorted_pair,
+                                                     int32_t* __restrict__ pair_to_sorted) {
+    extern __shared__ int32_t sm[];
+    int32_t* cursor = sm;
+    int32_t* wcnt = sm + E;
+    __shared__ int32_t warp_tot[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+    for (int i = tid; i < E * 33; i += PT) sm[i] = 0;
+    __syncthreads();
+    for (int p = tid; p < P; p += PT) atomicAdd(&cursor[ids[p]], 1);
+    __syncthreads();
+    // exclusive scan of cursor[0..E): thread e owns one entry (E <= 1024)
+    int v = tid < E ? cursor[tid] : 0;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int wv = warp_tot[lane];
+        int wi = wv;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += o;
+        }
+        warp_tot[lane] = wi - wv;
+    }
+    __syncthreads();
+    int excl = incl - v + warp_tot[warp];
+    if (tid < E) {
+        offsets[tid] = excl;
+        cursor[tid] = excl;
+    }
+    if (tid == 0) offsets[E] = P;
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = 0; base < P; base += PT) {
+        const int p = base + tid;
+        const bool valid = p < P;
+        const int e = valid ? ids[p] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & lt);
+        const bool leader = (__ffs(peers) - 1) == lane;
+        if (valid && leader) wcnt[warp * E + e] = __popc(peers);
+        __syncthreads();
+        if (valid) {
+            int pre = 0;
+            for (int w2 = 0; w2 < warp; ++w2) pre += wcnt[w2 * E + e];
+            const int pos = cursor[e] + pre + rank;
+            sorted_pair[pos] = p;
+            pair_to_sorted[p] = pos;
+        }
+        __syncthreads();
+        if (valid && leader) {
+            atomicAdd(&cursor[e], __popc(peers));
+            wcnt[warp * E + e] = 0;
+        }
+        __syncthreads();
+    }
+    pdl_launch_dependents();
+}
+
+}  // namespace
+
+moe_status launch_permute(const int32_t* ids, int P, int E, int32_t* offsets, int32_t* sorted_pair,
+                          int32_t* pair_to_sorted, cudaStream_t s) {
+    size_t smem = sizeof(int32_t) * (size_t)E * 33;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return cuda_status(e, "moe_permute: shared memory attribute");
+    }
+    permute_kernel<<<1, PT, smem, s>>>(ids, P, E, offsets, sorted_pair, pair_to_sorted);
+    MOE_LAUNCH_CHECK("moe_permute: launch");
+    return MOE_OK;
+}
+
+}  // namespace moe

@@ -1,0 +1,125 @@
+"""One routed-expert MoE layer on the device: the buffers it needs and the
+sequence of library calls of one forward pass.
+
+    logits = router(x)                  moe_router_logits
+    ids, w = top-k softmax(logits)      moe_route_topk
+    permutation by expert               moe_permute
+    y per (token, expert) pair          moe_vq2_expert_ffn (per-pair mode)
+    out = sum_j w * y                   moe_combine
+
+All five run as library kernels on one stream, with no host synchronisation,
+so a forward pass can be captured in a CUDA graph.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import (MOE_FMT_FP4, MOE_FMT_VQ2, MOE_FUSED_SCATTER, MOE_PER_PAIR, SlotTable, moe_combine,
+               moe_fp4_pack, moe_permute, moe_route_topk, moe_router_logits, moe_vq2_expert_ffn,
+               moe_vq2_expert_ffn_workspace_size)
+
+
+def _dev(a, dtype=None, device="cuda"):
+    if isinstance(a, torch.Tensor):
+        return a.to(device=device)
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(device=device)
+
+
+def upload_expert(fmt: int, codes: Sequence, scales: Sequence, stream=None, device="cuda"):
+    """Copies one expert's logical (row-major) codes and scales to the device
+    and packs them (moe_vq2_pack / moe_fp4_pack).  Returns (packed codes,
+    packed scales), three tensors each: gate, up, down."""
+    from . import moe_vq2_pack
+    pc, ps = [], []
+    for m in range(3):
+        c = _dev(codes[m], torch.uint8, device)
+        if fmt == MOE_FMT_VQ2:
+            s = _dev(scales[m], torch.float16, device)
+            c2, s2 = torch.empty_like(c), torch.empty_like(s)
+            moe_vq2_pack(c, s, c2, s2, stream)
+        else:
+            s = _dev(scales[m], torch.uint8, device)
+            c2, s2 = torch.empty_like(c), torch.empty_like(s)
+            moe_fp4_pack(c, s, c2, s2, stream)
+        pc.append(c2)
+        ps.append(s2)
+    return pc, ps
+
+
+class MoELayer:
+    def __init__(self, H: int, I: int, E: int, k: int, T_max: int, codebook, w_router, bias=None,
+                 renormalize: int = 1, device="cuda"):
+        self.H, self.I, self.E, self.k, self.T_max = H, I, E, k, T_max
+        self.renormalize = renormalize
+        self.codebook = _dev(codebook, torch.float16, device).contiguous()
+        self.w_router = _dev(w_router, torch.bfloat16, device).contiguous()
+        self.bias = None if bias is None else _dev(bias, torch.float32, device).contiguous()
+        self.table = SlotTable(E, H, I, self.codebook)
+        P = T_max * k
+        f32, i32 = torch.float32, torch.int32
+        self.logits = torch.empty(T_max, E, dtype=f32, device=device)
+        self.ids = torch.empty(T_max, k, dtype=i32, device=device)
+        self.weights = torch.empty(T_max, k, dtype=f32, device=device)
+        self.offsets = torch.empty(E + 1, dtype=i32, device=device)
+        self.sorted_pair = torch.empty(P, dtype=i32, device=device)
+        self.pair_to_sorted = torch.empty(P, dtype=i32, device=device)
+        self.pair_status = torch.empty(P, dtype=torch.uint8, device=device)
+        self.ypair = torch.empty(P, H, dtype=f32, device=device)
+        self.out = torch.empty(T_max, H, dtype=f32, device=device)
+        self.ws = torch.empty(moe_vq2_expert_ffn_workspace_size(T_max, k, E, I), dtype=torch.uint8,
+                              device=device)
+
+    def set_expert(self, e: int, fmt: int, packed_codes, packed_scales, stream=None):
+        self.table.set(e, fmt, packed_codes, packed_scales, stream)
+
+    def evict(self, e: int, stream=None):
+        self.table.evict(e, stream)
+
+    def route(self, x, stream=None):
+        T = x.shape[0]
+        moe_router_logits(x, self.w_router, self.bias, self.logits[:T], stream)
+        moe_route_topk(self.logits[:T], self.k, self.renormalize, self.ids[:T], self.weights[:T], stream)
+        moe_permute(self.ids[:T], self.E, self.offsets, self.sorted_pair[:T * self.k],
+                    self.pair_to_sorted[:T * self.k], None, stream)
+
+    def experts(self, x, mode=MOE_PER_PAIR, out=None, stream=None):
+        T = x.shape[0]
+        P = T * self.k
+        dst = self.ypair[:P] if mode == MOE_PER_PAIR else out
+        moe_vq2_expert_ffn(self.table, x, self.offsets, self.sorted_pair[:P], self.weights[:T], self.k, mode,
+                           dst, self.pair_status[:P], self.ws, stream)
+
+    def forward(self, x, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """x: bf16 [T, H] on the device -> fp32 [T, H] (a view of self.out
+        unless out is given)."""
+        T = x.shape[0]
+        if T > self.T_max:
+            raise ValueError(f"T={T} above T_max={self.T_max}")
+        o = self.out[:T] if out is None else out
+        self.route(x, stream)
+        self.experts(x, MOE_PER_PAIR, None, stream)
+        moe_combine(self.ypair[:T * self.k], self.pair_to_sorted[:T * self.k], self.weights[:T],
+                    self.pair_status[:T * self.k], self.k, o, None, stream)
+        return o
+
+
+def upload_layer(H, I, E, k, T_max, codebook, w_router, bias, experts, renormalize=1, resident=None,
+                 stream=None, device="cuda"):
+    """Builds a MoELayer and makes resident the experts in ``resident`` (all
+    when None).  ``experts(e)`` returns (fmt, codes[3], scales[3]) in the
+    logical layout.  Returns (layer, packed buffers by expert id)."""
+    layer = MoELayer(H, I, E, k, T_max, codebook, w_router, bias, renormalize, device)
+    keep = {}
+    ids = range(E) if resident is None else resident
+    for e in ids:
+        fmt, codes, scales = experts(int(e))
+        pc, ps = upload_expert(fmt, codes, scales, stream, device)
+        layer.set_expert(int(e), fmt, pc, ps, stream)
+        keep[int(e)] = (pc, ps)
+    return layer, keep

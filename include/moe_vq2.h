@@ -1,0 +1,208 @@
+/*
+ * moe_vq2.h -- C ABI of the routed-expert VQ2 MoE layer on one GB300 (sm_103a).
+ *
+ * The layer, as the pages state the problem:
+ *   - each token's router picks its top-k experts (vLLM-Moet page, "What we
+ *     changed": "7 launches from router to FC1" at decode; the router's
+ *     top-k, "2-bit experts on vLLM v0.24.0");
+ *   - each chosen expert's FC1 (gate, up), silu(gate)*up and FC2 run from
+ *     weights stored as 2-bit vector codes, about 2.1 bits per weight
+ *     (Tandem-vLLM page, "How it works"), with a sign-symmetric codebook
+ *     (vLLM-Moet page, "2-bit experts on vLLM v0.24.0"); the most routed
+ *     experts may stay in FP4 (Tandem-vLLM page, "Quality": FP4_TOP);
+ *   - a GPU cache holds the resident experts; the others are computed
+ *     elsewhere and nothing is skipped or substituted (Tandem-vLLM page,
+ *     "How it works"; vLLM-Moet page: "the GPU as an expert cache ... a miss
+ *     is fetched and the step's graph replayed, bit-identical");
+ *   - the experts' outputs are combined by router weight.
+ *
+ * Conventions (every entry point):
+ *   - Returns a moe_status.  MOE_OK is 0; negative values are errors, and
+ *     moe_last_error() then returns a message (thread-local, valid until the
+ *     next call on the same thread).
+ *   - All array arguments are DEVICE pointers owned by the caller unless a
+ *     comment says otherwise; the library never frees them.  Pointers must
+ *     be 16-byte aligned.
+ *   - Arguments are checked on the host before anything is enqueued; a
+ *     failed check enqueues nothing.  Calls only enqueue work on the given
+ *     stream: they never synchronise the host with the device.
+ *   - Activations: bf16 (uint16_t bit patterns).  Codebook and VQ2 scales:
+ *     fp16 (uint16_t bit patterns).  FP4 scales: ue8m0 bytes.
+ *   - Shapes: T tokens, H hidden, I expert intermediate, E experts, k top-k,
+ *     P = T*k (token, slot) pairs, pair p = t*k + j.
+ */
+#ifndef MOE_VQ2_H
+#define MOE_VQ2_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int moe_status;
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG -1 /* null / negative / out-of-range argument        */
+#define MOE_ERR_UNSUPPORTED -2 /* shape or alignment this build does not handle  */
+#define MOE_ERR_CUDA -3        /* a CUDA runtime call or launch failed          */
+#define MOE_ERR_NO_MEM -4      /* a library allocation failed                   */
+#define MOE_ERR_WORKSPACE -5   /* workspace missing or smaller than required    */
+#define MOE_ERR_TIMEOUT -6     /* reserved: a bounded device wait gave up        */
+#define MOE_ERR_MISMATCH -7    /* moe_selftest: a result differs from its check  */
+
+#define MOE_FMT_VQ2 0 /* 2-bit vector codes + fp16 row scales per 128 inputs */
+#define MOE_FMT_FP4 1 /* MXFP4: e2m1 elements + ue8m0 scale per 32 inputs     */
+
+#define MOE_FUSED_SCATTER 0 /* out[t] += w[t,j] * y  (fp32 atomics, caller zeroes out) */
+#define MOE_PER_PAIR 1      /* ypair[sorted position] = y (deterministic)               */
+
+int moe_version(void);
+const char* moe_last_error(void);
+
+/* ---------------------------------------------------------------------- */
+/* Weight formats and packing                                              */
+/* ---------------------------------------------------------------------- */
+/*
+ * Logical VQ2 matrix W [rows, K] (the expert code of the Tandem-vLLM page,
+ * "How it works", with the sign-symmetric codebook of the vLLM-Moet page):
+ *   codes  uint8 [rows, K/4]: code c of row r, group q covers inputs 4q..4q+3;
+ *          bit 7 = sign (1 = negative), bits 0-6 = codebook index;
+ *   scales fp16  [rows, K/128]: one scale per row per 128 inputs;
+ *   codebook fp16 [128, 4], one per layer;
+ *   W[r][4q+i] = (c >> 7 ? -1 : 1) * codebook[c & 127][i] * scales[r][4q/128].
+ *
+ * Packed VQ2 (what the slot table points at), same byte counts:
+ *   codes: tiles of 16 rows x 32 groups (128 inputs), 512 bytes each, tile
+ *          (rt, kb) at byte (rt*(K/128) + kb)*512; inside a tile byte
+ *          16*g + 2*i + h holds the code of row 16*rt + i + 8*h, group
+ *          32*kb + g (g < 32, i < 8, h < 2);
+ *   scales: 16 fp16 per tile, at element (rt*(K/128) + kb)*16 + (r - 16*rt).
+ *
+ * Logical FP4 matrix [rows, K] (MXFP4, OCP MX v1.0):
+ *   codes  uint8 [rows, K/2]: byte b of row r holds elements 2b (low nibble)
+ *          and 2b+1 (high nibble), each e2m1;
+ *   scales uint8 [rows, K/32]: ue8m0 exponent E, scale 2^(E-127); E = 255
+ *          (NaN) is not allowed.
+ * Packed FP4: tiles of 16 rows x 64 elements, 512 bytes each, tile (rt, kt)
+ *   at byte (rt*(K/64) + kt)*512; inside a tile the 16 bytes at 16*(4*i + j)
+ *   hold, for s = 0..3, the four bytes [row i: b, row i: b+4, row i+8: b,
+ *   row i+8: b+4] with b = 32*kt + 8*s + j (rows relative to 16*rt);
+ *   scales: 16 bytes per (rt, 32-element block kb), at (rt*(K/32) + kb)*16
+ *   + (r - 16*rt).
+ *
+ * Requirements: rows % 16 == 0; K % 128 == 0 (VQ2) or K % 64 == 0 (FP4).
+ * The pack calls read the logical arrays and write the packed ones; source
+ * and destination must not overlap.  Sizes are unchanged by packing.
+ */
+moe_status moe_vq2_pack(const uint8_t* codes, const uint16_t* scales, int rows, int K,
+                        uint8_t* packed_codes, uint16_t* packed_scales, cudaStream_t stream);
+moe_status moe_fp4_pack(const uint8_t* codes, const uint8_t* scales, int rows, int K,
+                        uint8_t* packed_codes, uint8_t* packed_scales, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Expert-slot table (the GPU expert cache of the Tandem-vLLM page, "How it */
+/* works": "a GPU cache holds the most-used ones")                           */
+/* ---------------------------------------------------------------------- */
+typedef struct moe_slot_table moe_slot_table;
+
+typedef struct moe_expert_desc {
+    int format;                /* MOE_FMT_VQ2 or MOE_FMT_FP4                       */
+    const void* codes[3];      /* packed codes of gate [I,H], up [I,H], down [H,I] */
+    const void* scales[3];     /* packed scales of the same three matrices         */
+} moe_expert_desc;
+
+/* Creates a table of num_experts entries, all non-resident, for one layer
+ * with hidden H and intermediate I.  codebook: device fp16 [128*4], the
+ * layer's codebook; it must outlive the table.  Allocates a small device
+ * descriptor array (the only memory the table owns).  H % 256 == 0 and
+ * I % 128 == 0. */
+moe_status moe_slot_table_create(int num_experts, int H, int I, const uint16_t* codebook,
+                                 moe_slot_table** out);
+/* Makes expert_id resident with the given packed buffers (not copied: they
+ * must stay valid while the entry is set).  Setting an id again replaces it.
+ * Enqueued on stream: work launched later on the same stream sees it. */
+moe_status moe_slot_table_set(moe_slot_table* t, int expert_id, const moe_expert_desc* d,
+                              cudaStream_t stream);
+/* Marks expert_id non-resident (enqueued on stream). */
+moe_status moe_slot_table_evict(moe_slot_table* t, int expert_id, cudaStream_t stream);
+/* Frees the descriptor array; the caller must have synchronised the streams
+ * that used the table. */
+moe_status moe_slot_table_destroy(moe_slot_table* t);
+
+/* ---------------------------------------------------------------------- */
+/* Hot path                                                                */
+/* ---------------------------------------------------------------------- */
+
+/* Router logits (the router of the vLLM-Moet page, "What we changed", MoE
+ * at decode): logits[t,e] = sum_h x[t,h]*w_router[e,h] + bias[e], fp32.
+ * x bf16 [T,H], w_router bf16 [E,H] row-major, bias fp32 [E] or NULL,
+ * logits fp32 [T,E].  The sum runs in one fixed order so that repeated
+ * runs and the CPU reference give identical bits: lane l = (h/8) mod 32
+ * adds its exact products in increasing h, then the 32 lane sums combine
+ * by a butterfly (xor 16, 8, 4, 2, 1), then the bias is added.
+ * Requires H % 256 == 0, T >= 0, E >= 1. */
+moe_status moe_router_logits(const uint16_t* x, const uint16_t* w_router, const float* bias,
+                             float* logits, int T, int H, int E, cudaStream_t stream);
+
+/* Top-k routing + softmax weights: for each token the k largest logits,
+ * ordered by (logit descending, expert id ascending) -- equal logits go to
+ * the lower id.  renormalize = 1: weights = softmax over the k selected
+ * logits; 0: the softmax over all E logits read at the k selected.
+ * logits fp32 [T,E] -> ids int32 [T,k], weights fp32 [T,k].
+ * Requires 1 <= k <= min(E, 32), E <= 1024. */
+moe_status moe_route_topk(const float* logits, int T, int E, int k, int renormalize,
+                          int32_t* ids, float* weights, cudaStream_t stream);
+
+/* Token -> expert permutation (no padding rows; the vLLM-Moet page, "What
+ * we changed", names padding every expert to 128 rows as the cost to
+ * avoid): a stable counting sort of the pairs p by ids[p].
+ * expert_offsets int32 [E+1] (offsets[e] = pairs routed to experts below e),
+ * sorted_pair int32 [P] (pair at each sorted position), pair_to_sorted
+ * int32 [P] (inverse).  Requires every id in [0, E), E <= 1024, P <= 2^24.
+ * ws: device workspace of moe_permute_workspace_size() bytes (may be NULL
+ * when that size is 0). */
+size_t moe_permute_workspace_size(int T, int k, int E);
+moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_offsets,
+                       int32_t* sorted_pair, int32_t* pair_to_sorted, void* ws, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/* Expert FFN over the resident experts (Tandem-vLLM page, "How it works";
+ * vLLM-Moet page, "Qwen3.8": silu*up fused into the MoE GEMV): for every
+ * pair p routed to a resident expert e,
+ *     g = Wg_e x_t,  u = Wu_e x_t,  a = silu(g) * u,  y = Wd_e a,
+ * with the weights decoded from the slot table's packed codes.
+ * mode MOE_FUSED_SCATTER: out_or_ypair is fp32 [T,H] and receives
+ *     w[p] * y by fp32 atomic adds (the caller zeroes it first; the order of
+ *     the adds, and so the low bits, may differ between runs);
+ * mode MOE_PER_PAIR: out_or_ypair is fp32 [P,H]; row s receives y of the
+ *     pair at sorted position s (run-to-run deterministic).
+ * pair_status uint8 [P]: 1 if pair p was computed, 0 if its expert is not
+ * resident (such pairs are skipped, never substituted; their rows of ypair
+ * are left untouched).  expert_offsets/sorted_pair come from moe_permute
+ * over the same ids; weights fp32 [T,k] from moe_route_topk.
+ * ws: moe_vq2_expert_ffn_workspace_size(T, k, E, I) bytes of device memory
+ * (scratch: the schedule and the fp32 intermediate a [P, I]).
+ * Requires H % 256 == 0, I % 128 == 0, x 16-byte aligned. */
+size_t moe_vq2_expert_ffn_workspace_size(int T, int k, int E, int I);
+moe_status moe_vq2_expert_ffn(const moe_slot_table* table, const uint16_t* x,
+                              const int32_t* expert_offsets, const int32_t* sorted_pair,
+                              const float* weights, int T, int k, int mode, float* out_or_ypair,
+                              uint8_t* pair_status, void* ws, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/* Deterministic combine: out[t] = sum over j = 0..k-1 (in that order) of
+ * pair_status[t*k+j] * weights[t,j] * ypair[pair_to_sorted[t*k+j]].
+ * ypair fp32 [P,H] (per-pair mode of moe_vq2_expert_ffn); out_f32 fp32
+ * [T,H] and/or out_bf16 bf16 [T,H] (round to nearest even of the fp32
+ * result); either may be NULL but not both (T = 0 is a no-op that reads
+ * no pointer). */
+moe_status moe_combine(const float* ypair, const int32_t* pair_to_sorted, const float* weights,
+                       const uint8_t* pair_status, int T, int k, int H, float* out_f32,
+                       uint16_t* out_bf16, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_VQ2_H */

@@ -1,0 +1,158 @@
+"""GPU parity of the CUDA path against the CPU oracle on small layers: the
+tiny workload, ragged per-expert token counts, degenerate shapes, residency,
+determinism and the sign-symmetry invariant.  Every call goes through the
+C ABI (ctypes)."""
+import numpy as np
+import pytest
+
+import moe_synth as ms
+import oracle
+from gpu_common import (assert_close, assert_routing_exact, device_layer, run, torch_cuda,
+                        MAX_REL_RMS, MEAN_REL)
+
+pytestmark = pytest.mark.gpu
+O = oracle.default
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return torch_cuda()
+
+
+def _check_layer(spec, T, seed=0, resident=None):
+    layer = ms.Layer(spec)
+    x = ms.tokens(T, spec.H, seed=seed)
+    res_ids = None if resident is None else np.nonzero(resident)[0]
+    dev, keep = device_layer(layer, T, res_ids)
+    g = run(dev, x)
+    r = O.moe_layer(layer, x, resident=resident)
+    assert_routing_exact(g, r)
+    res = np.ones(spec.E, bool) if resident is None else resident
+    assert np.array_equal(g["status"], res[r["ids"]].ravel().astype(np.uint8))
+    assert_close(g["out"], r["partial"], f"T={T} E={spec.E} k={spec.k}")
+    return layer, x, dev, keep, g, r
+
+
+def test_tiny_layer_full_parity(torch):
+    _check_layer(ms.spec_tiny(0), 4)
+
+
+def test_tiny_layer_fp4_experts(torch):
+    spec = ms.spec_tiny(1)
+    spec.fp4_top = 3
+    _check_layer(spec, 4, seed=1)
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (37, 4, 2), (5, 16, 3), (64, 8, 8), (3, 1, 1), (17, 32, 1)])
+def test_ragged_and_degenerate_shapes(torch, T, E, k):
+    spec = ms.LayerSpec(H=256, I=128, E=E, k=k, seed=T + 10 * E + k)
+    _check_layer(spec, T, seed=T)
+
+
+def test_wider_hidden_mixed_formats(torch):
+    spec = ms.LayerSpec(H=1024, I=384, E=12, k=4, seed=21, zipf_s=1.1, fp4_top=4)
+    _check_layer(spec, 24, seed=3)
+
+
+def test_renormalize_off(torch):
+    spec = ms.LayerSpec(H=256, I=128, E=16, k=4, seed=5, renormalize=0)
+    _check_layer(spec, 9, seed=5)
+
+
+def test_non_resident_experts_are_reported_not_substituted(torch):
+    spec = ms.LayerSpec(H=512, I=256, E=16, k=4, seed=7, zipf_s=1.1, fp4_top=3)
+    res = np.zeros(16, bool)
+    res[[0, 3, 4, 9, 10, 15]] = True
+    layer, x, dev, keep, g, r = _check_layer(spec, 12, seed=7, resident=res)
+    # rows of ypair for skipped pairs are left untouched
+    P = 12 * 4
+    dev.ypair[:P].fill_(float("nan"))
+    g2 = run(dev, x)
+    skipped = g2["status"] == 0
+    assert skipped.any() and (~skipped).any()
+    assert np.isnan(g2["ypair"][g2["pair_to_sorted"][skipped]]).all()
+    assert not np.isnan(g2["ypair"][g2["pair_to_sorted"][~skipped]]).any()
+    # GPU partial + oracle remainder = oracle whole layer
+    assert_close(g2["out"] + r["remainder"], r["out"], "partial + remainder")
+
+
+def test_per_pair_is_deterministic_and_slot_reload_bit_identical(torch):
+    spec = ms.LayerSpec(H=512, I=256, E=8, k=2, seed=8)
+    layer = ms.Layer(spec)
+    x = ms.tokens(16, 512, seed=8)
+    dev, keep = device_layer(layer, 16)
+    a = run(dev, x)
+    b = run(dev, x)
+    assert np.array_equal(a["out"].view(np.uint32), b["out"].view(np.uint32))
+    # evict and re-set every expert from freshly packed buffers: same bits
+    import bit_vq_routed_gb300 as bv
+    for e in range(8):
+        dev.evict(e)
+    for e in range(8):
+        ex = layer.expert(e)
+        pc, ps = bv.layer.upload_expert(ex.fmt, ex.codes, ex.scales)
+        dev.set_expert(e, ex.fmt, pc, ps)
+        keep[e] = (pc, ps)
+    c = run(dev, x)
+    assert np.array_equal(a["ypair"].view(np.uint32), c["ypair"].view(np.uint32))
+
+
+def test_fused_scatter_matches_per_pair(torch):
+    import bit_vq_routed_gb300 as bv
+    spec = ms.LayerSpec(H=512, I=256, E=8, k=3, seed=9)
+    layer = ms.Layer(spec)
+    x = ms.tokens(20, 512, seed=9)
+    dev, keep = device_layer(layer, 20)
+    g = run(dev, x)
+    xt = torch.from_numpy(x).view(torch.bfloat16).cuda()
+    out = torch.zeros(20, 512, dtype=torch.float32, device="cuda")
+    dev.route(xt)
+    dev.experts(xt, bv.MOE_FUSED_SCATTER, out)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert np.abs(o - g["out"]).max() <= 1e-5 * np.abs(g["out"]).max()
+
+
+@pytest.mark.parametrize("m", [1, 2])
+def test_sign_flip_negates_expert_output_bit_exactly(torch, m):
+    # sign-symmetric codebook: flipping every sign bit of the up (m=1) or
+    # down (m=2) codes of every expert negates each per-pair y exactly
+    import bit_vq_routed_gb300 as bv
+    spec = ms.LayerSpec(H=512, I=256, E=4, k=2, seed=12)
+    layer = ms.Layer(spec)
+    x = ms.tokens(6, 512, seed=12)
+    dev, keep = device_layer(layer, 6)
+    a = run(dev, x)
+    for e in range(4):
+        ex = layer.expert(e)
+        codes = list(ex.codes)
+        codes[m] = codes[m] ^ 0x80
+        pc, ps = bv.layer.upload_expert(ex.fmt, codes, ex.scales)
+        dev.set_expert(e, ex.fmt, pc, ps)
+        keep[e] = (pc, ps)
+    b = run(dev, x)
+    assert np.array_equal(b["ypair"], -a["ypair"])
+
+
+def test_empty_batch_is_a_no_op(torch):
+    spec = ms.spec_tiny(0)
+    layer = ms.Layer(spec)
+    dev, keep = device_layer(layer, 4)
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    out = dev.forward(x)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 256)
+
+
+def test_workspace_too_small_is_rejected(torch):
+    import bit_vq_routed_gb300 as bv
+    spec = ms.spec_tiny(0)
+    layer = ms.Layer(spec)
+    dev, keep = device_layer(layer, 4)
+    x = torch.from_numpy(ms.tokens(4, 256, 0)).view(torch.bfloat16).cuda()
+    dev.route(x)
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(bv.MoeError) as ei:
+        bv.moe_vq2_expert_ffn(dev.table, x, dev.offsets, dev.sorted_pair[:8], dev.weights[:4], 2,
+                              bv.MOE_PER_PAIR, dev.ypair[:8], dev.pair_status[:8], small)
+    assert ei.value.status == bv.MOE_ERR_WORKSPACE

@@ -1,0 +1,104 @@
+"""GPU parity at the full workload sizes (hidden 4096, intermediate 2048,
+256 experts, top-8), in the launch configuration the benchmark times:
+  - decode batch 1, 4 layers, all experts resident;
+  - decode batch 32 with Zipf(1.1) routing bias;
+  - mixed FP4 (52 most routed) / VQ2 decode batch 8, all resident and with
+    only the 96 most routed resident (GPU partial + oracle remainder = whole);
+  - prefill chunk of 4096 tokens: routing bit-exact for every token, layer
+    output on a sample of tokens the oracle computes one by one.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import moe_synth as ms
+import oracle
+from gpu_common import assert_close, assert_routing_exact, device_layer, run, torch_cuda
+
+pytestmark = pytest.mark.gpu
+O = oracle.default
+
+
+@pytest.fixture(scope="module")
+def torch():
+    t = torch_cuda()
+    O.set_threads(os.cpu_count() or 1)
+    return t
+
+
+def _sub(r, tokens, k):
+    return {key: r[key] for key in ("logits", "ids", "weights")}
+
+
+def test_decode_batch1_four_layers(torch):
+    for L in range(4):
+        layer = ms.Layer(ms.spec_decode(L))
+        dev, keep = device_layer(layer, 1)
+        for stream in range(2):
+            x = ms.tokens(1, 4096, seed=100 + L, stream=stream)
+            g = run(dev, x)
+            r = O.moe_layer(layer, x)
+            assert_routing_exact(g, r)
+            assert (g["status"] == 1).all()
+            assert_close(g["out"], r["out"], f"layer {L} token {stream}")
+        del dev, keep
+        torch.cuda.empty_cache()
+
+
+def test_decode_batch32_zipf(torch):
+    layer = ms.Layer(ms.spec_decode(0, zipf_s=1.1))
+    dev, keep = device_layer(layer, 32)
+    x = ms.tokens(32, 4096, seed=200)
+    g = run(dev, x)
+    r = O.moe_layer(layer, x)
+    assert_routing_exact(g, r)
+    counts = np.diff(g["offsets"])
+    assert counts.max() >= 8 and (counts == 1).any()  # uneven per-expert token counts
+    assert_close(g["out"], r["out"], "decode b32")
+
+
+def test_mixed_fp4_vq2_batch8_and_partial_residency(torch):
+    layer = ms.Layer(ms.spec_decode(0, zipf_s=1.1, fp4_top=52))
+    x = ms.tokens(8, 4096, seed=300)
+    dev, keep = device_layer(layer, 8)
+    g = run(dev, x)
+    r = O.moe_layer(layer, x)
+    assert_routing_exact(g, r)
+    assert (layer.formats[np.unique(r["ids"])] == ms.FMT_FP4).any()
+    assert_close(g["out"], r["out"], "mixed all resident")
+    del dev, keep
+    # second run: only the 96 most routed experts in the slot table
+    res = np.zeros(256, bool)
+    res[ms.most_popular(layer, 96)] = True
+    dev, keep = device_layer(layer, 8, np.nonzero(res)[0])
+    g2 = run(dev, x)
+    r2 = O.moe_layer(layer, x, resident=res)
+    assert_routing_exact(g2, r2)
+    assert np.array_equal(g2["status"], res[r2["ids"]].ravel().astype(np.uint8))
+    assert (g2["status"] == 0).any()
+    assert_close(g2["out"], r2["partial"], "resident partial")
+    assert_close(g2["out"] + r2["remainder"], r2["out"], "partial + remainder")
+
+
+def test_prefill_4096_routing_exact_and_sampled_outputs(torch):
+    layer = ms.Layer(ms.spec_decode(0, zipf_s=1.1))
+    T = 4096
+    x = ms.tokens(T, 4096, seed=400)
+    dev, keep = device_layer(layer, T)
+    g = run(dev, x)
+    logits = O.router_logits(x, layer.w_router, layer.bias)
+    ids, w = O.route_topk(logits, 8, 1)
+    off, sp, p2s = O.permute(ids, 256)
+    assert np.array_equal(g["logits"].view(np.uint32), logits.view(np.uint32))
+    assert np.array_equal(g["ids"], ids)
+    assert np.abs(g["weights"] - w).max() <= 1e-6
+    assert np.array_equal(g["offsets"], off) and np.array_equal(g["sorted_pair"], sp)
+    counts = np.diff(off)
+    assert counts.max() > 1000  # hot experts get prefill-sized batches
+    # sample: 12 spread tokens + every token of the coldest non-empty expert
+    cold = int(np.argmin(np.where(counts > 0, counts, 1 << 30)))
+    cold_tokens = sp[off[cold]:off[cold + 1]] // 8
+    sample = np.unique(np.concatenate([np.linspace(0, T - 1, 12).astype(int), cold_tokens]))
+    r = O.moe_layer(layer, x, tokens=sample)
+    assert_close(g["out"][sample], r["out"], "prefill sample")
