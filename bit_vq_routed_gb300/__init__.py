@@ -52,7 +52,7 @@ EXPORTED = [
     "moe_version", "moe_last_error", "moe_vq2_pack", "moe_fp4_pack", "moe_slot_table_create",
     "moe_slot_table_set", "moe_slot_table_evict", "moe_slot_table_destroy", "moe_router_logits",
     "moe_route_topk", "moe_permute_workspace_size", "moe_permute",
-    "moe_vq2_expert_ffn_workspace_size", "moe_vq2_expert_ffn", "moe_combine",
+    "moe_vq2_expert_ffn_workspace_size", "moe_vq2_expert_ffn", "moe_vq2_expert_ffn_noalloc", "moe_combine",
 ]
 
 
@@ -84,6 +84,7 @@ def load(path: Optional[str] = None, build_if_stale: bool = True):
         "moe_permute": ([P, I, I, I, P, P, P, P, Z, P], I),
         "moe_vq2_expert_ffn_workspace_size": ([I, I, I, I], Z),
         "moe_vq2_expert_ffn": ([P, P, P, P, P, I, I, I, P, P, P, Z, P], I),
+        "moe_vq2_expert_ffn_noalloc": ([P, P, P, P, P, I, I, I, P, P, P], I),
         "moe_combine": ([P, P, P, P, I, I, I, P, P, P], I),
     }
     for name, (args, res) in sig.items():
@@ -210,6 +211,21 @@ def moe_vq2_expert_ffn(table: SlotTable, x, expert_offsets, sorted_pair, weights
     _check(load().moe_vq2_expert_ffn(table.handle, _ptr(x), _ptr(expert_offsets), _ptr(sorted_pair),
                                      _ptr(weights), T, k, mode, _ptr(out), _ptr(pair_status), _ptr(ws),
                                      nbytes, _stream(stream)))
+
+
+MOE_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def moe_vq2_expert_ffn_noalloc(table: SlotTable, x, expert_offsets, sorted_pair, weights, k: int, mode: int,
+                               out, pair_status, stream=None):
+    """moe_vq2_expert_ffn without a workspace argument, for callers that cannot
+    allocate device memory: the library's fixed MOE_NOALLOC_SCRATCH_BYTES
+    device array serves as scratch (shared by every call on a device, so
+    calls must not overlap on the GPU)."""
+    T = x.shape[0]
+    _check(load().moe_vq2_expert_ffn_noalloc(table.handle, _ptr(x), _ptr(expert_offsets), _ptr(sorted_pair),
+                                             _ptr(weights), T, k, mode, _ptr(out), _ptr(pair_status),
+                                             _stream(stream)))
 
 
 def moe_combine(ypair, pair_to_sorted, weights, pair_status, k: int, out_f32=None, out_bf16=None,

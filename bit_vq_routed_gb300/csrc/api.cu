@@ -31,10 +31,6 @@ int num_sms() {
 
 }  // namespace moe
 
-struct moe_slot_table {
-    moe::SlotTableHost h;
-};
-
 using namespace moe;
 
 extern "C" {

@@ -132,3 +132,8 @@ moe_status launch_combine(const float* ypair, const int32_t* p2s, const float* w
                           int T, int k, int H, float* out32, uint16_t* out16, cudaStream_t s);
 
 }  // namespace moe
+
+// The opaque handle of include/moe_vq2.h.
+struct moe_slot_table {
+    moe::SlotTableHost h;
+};

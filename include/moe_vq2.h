@@ -192,6 +192,40 @@ moe_status moe_vq2_expert_ffn(const moe_slot_table* table, const uint16_t* x,
                               uint8_t* pair_status, void* ws, size_t ws_bytes,
                               cudaStream_t stream);
 
+/* Scratch-free variant of moe_vq2_expert_ffn (the pages have no counterpart:
+ * this entry point exists for library users, not for the method).
+ *
+ * Some callers cannot call cudaMalloc (or any allocator) at the point where
+ * they run the layer: a host that owns every byte of device memory through
+ * its own fixed arena or pool and forbids library allocations, a real-time
+ * or serving loop that must not pay allocation latency or risk an
+ * out-of-memory in the middle of a step, or code running where allocation is
+ * not allowed.  This call takes no workspace: it computes exactly what
+ * moe_vq2_expert_ffn computes (same arguments and outputs) using a scratch
+ * area of MOE_NOALLOC_SCRATCH_BYTES that is a static device array of the
+ * library, reserved on every GPU that loads the library and held until the
+ * process exits.  It never calls cudaMalloc, cudaFree or an allocating
+ * library routine.
+ *
+ * Limits and rules:
+ *   - the call fails with MOE_ERR_UNSUPPORTED, and enqueues nothing, when
+ *     moe_vq2_expert_ffn_workspace_size(T, k, E, I) exceeds
+ *     MOE_NOALLOC_SCRATCH_BYTES (64 MiB: at H = 4096, I = 2048 this covers
+ *     decode batches of up to 32 tokens at top-8, and more);
+ *   - the first call on each device looks up the device address of the
+ *     static array (cudaGetSymbolAddress, with that device current); make
+ *     that first call before any stream capture on the device;
+ *   - every call on a device shares the one array, which keeps the contents
+ *     of the last call (no part of it needs to start at zero: each call
+ *     writes what it reads).  Calls whose work overlaps on the GPU (on
+ *     different streams, or from different host threads without ordering)
+ *     race on it: order them on one stream or with events. */
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+moe_status moe_vq2_expert_ffn_noalloc(const moe_slot_table* table, const uint16_t* x,
+                                      const int32_t* expert_offsets, const int32_t* sorted_pair,
+                                      const float* weights, int T, int k, int mode, float* out_or_ypair,
+                                      uint8_t* pair_status, cudaStream_t stream);
+
 /* Deterministic combine: out[t] = sum over j = 0..k-1 (in that order) of
  * pair_status[t*k+j] * weights[t,j] * ypair[pair_to_sorted[t*k+j]].
  * ypair fp32 [P,H] (per-pair mode of moe_vq2_expert_ffn); out_f32 fp32
