@@ -193,48 +193,102 @@ def run_gpu(args, wl, world, rank, local):
         keeps.append(keep)
     pools = [torch.from_numpy(token_pool(wl, L)).view(torch.bfloat16).cuda() for L in range(nL)]
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
+    G = wl["pool"]
 
     def step(s, evs=None):
         for L, dev in enumerate(devs):
-            x = pools[L][s % wl["pool"]]
+            x = pools[L][s % G]
             dev.route(x)
             if evs is not None:
-                evs[L][0].record(stream)
+                evs[L][0].record()
             dev.experts(x, bv.MOE_PER_PAIR)
             if evs is not None:
-                evs[L][1].record(stream)
+                evs[L][1].record()
             bv.moe_combine(dev.ypair[:T * dev.k], dev.pair_to_sorted[:T * dev.k], dev.weights[:T],
                            dev.pair_status[:T * dev.k], dev.k, dev.out[:T])
 
+    def new_events():
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nL)]
+
+    step(0)  # first eager step: the library sets its kernel attributes outside any capture
+    torch.cuda.synchronize()
+    if args.graph:
+        # Per token batch s of the pool: CUDA graphs of the step's pieces
+        # [route 0] [ffn 0] [combine 0 + route 1] [ffn 1] ... [combine last];
+        # the expert-FFN graphs are bracketed by events recorded on the
+        # stream between replays (event records cannot sit inside a capture).
+        def piece(fn):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            return g
+
+        def route_fn(L, s):
+            return lambda: devs[L].route(pools[L][s])
+
+        def ffn_fn(L, s):
+            return lambda: devs[L].experts(pools[L][s], bv.MOE_PER_PAIR)
+
+        def comb(L):
+            d = devs[L]
+            bv.moe_combine(d.ypair[:T * d.k], d.pair_to_sorted[:T * d.k], d.weights[:T],
+                           d.pair_status[:T * d.k], d.k, d.out[:T])
+
+        graphs = []
+        for s in range(G):
+            seq = [("g", piece(route_fn(0, s)))]
+            for L in range(nL):
+                seq.append(("ffn", L, piece(ffn_fn(L, s))))
+                if L + 1 < nL:
+                    seq.append(("g", piece(lambda L=L, s=s: (comb(L), devs[L + 1].route(pools[L + 1][s])))))
+                else:
+                    seq.append(("g", piece(lambda L=L: comb(L))))
+            graphs.append(seq)
+
+        def run(s, evs=None):
+            for item in graphs[s % G]:
+                if item[0] == "g":
+                    item[1].replay()
+                else:
+                    L, g = item[1], item[2]
+                    if evs is not None:
+                        evs[L][0].record()
+                    g.replay()
+                    if evs is not None:
+                        evs[L][1].record()
+    else:
+        run = step
+    stream = torch.cuda.current_stream()
     for s in range(args.warmup):
-        step(s)
+        run(s)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    ffn_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nL)]
-              for _ in range(args.steps)]
+    step_ev = [new_events() for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     start.record(stream)
     for s in range(args.steps):
-        step(args.warmup + s, ffn_ev[s])
+        run(args.warmup + s, step_ev[s])
     end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     ms_total = start.elapsed_time(end)
-    ffn_ms = [ffn_ev[s][L][0].elapsed_time(ffn_ev[s][L][1]) for s in range(args.steps) for L in range(nL)]
+    timed_slots = [(args.warmup + s) % G for s in range(args.steps)]
+    ffn_ms = [step_ev[s][L][0].elapsed_time(step_ev[s][L][1]) for s in range(args.steps) for L in range(nL)]
     # distinct experts touched per FFN launch (read back after timing)
     code_bytes = []
-    for s in range(args.steps):
+    per_slot = {}
+    for sl in sorted(set(timed_slots)):
         for L, dev in enumerate(devs):
-            dev.route(pools[L][(args.warmup + s) % wl["pool"]])
+            dev.route(pools[L][sl])
             ids = np.unique(dev.ids[:T].cpu().numpy())
             fmts = layers[L].formats[ids]
-            code_bytes.append(int((fmts == ms.FMT_VQ2).sum()) * VQ2_EXPERT_BYTES
-                              + int((fmts == ms.FMT_FP4).sum()) * FP4_EXPERT_BYTES)
+            per_slot[(sl, L)] = (int((fmts == ms.FMT_VQ2).sum()) * VQ2_EXPERT_BYTES
+                                 + int((fmts == ms.FMT_FP4).sum()) * FP4_EXPERT_BYTES)
+    code_bytes = [per_slot[(sl, L)] for sl in timed_slots for L in range(nL)]
     if world > 1:
         t = torch.tensor([ms_total], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -243,15 +297,20 @@ def run_gpu(args, wl, world, rank, local):
     # end to end through the public API: pinned host tokens in, outputs out
     host_in = [torch.from_numpy(token_pool(wl, L)).view(torch.bfloat16).pin_memory() for L in range(nL)]
     host_out = torch.empty(nL, T, 4096, dtype=torch.float32).pin_memory()
-    dev_in = [torch.empty(T, 4096, dtype=torch.bfloat16, device="cuda") for _ in range(nL)]
+    if args.graph:
+        fwd = [bv.GraphedForward(dev, T) for dev in devs]
     e2e_steps = args.steps
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for s in range(e2e_steps):
         for L, dev in enumerate(devs):
-            dev_in[L].copy_(host_in[L][s % wl["pool"]], non_blocking=True)
-            out = dev.forward(dev_in[L])
+            if args.graph:
+                fwd[L].x.copy_(host_in[L][s % G], non_blocking=True)
+                out = fwd[L].replay()
+            else:
+                xin = host_in[L][s % G].cuda(non_blocking=True)
+                out = dev.forward(xin)
             host_out[L].copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -262,7 +321,7 @@ def run_gpu(args, wl, world, rank, local):
         e2e_ms = float(t.item())
         torch.distributed.destroy_process_group()
     return dict(ms_total=ms_total, ffn_ms=ffn_ms, code_bytes=code_bytes, clocks=clk, e2e_ms=e2e_ms,
-                e2e_steps=e2e_steps, launches_per_layer=7)
+                e2e_steps=e2e_steps, launches_per_layer=10)
 
 
 def main():
@@ -275,6 +334,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--eager", dest="graph", action="store_false",
+                    help="launch every call from Python instead of replaying one CUDA graph per step")
     args = ap.parse_args()
     world, rank, local = dist_env()
     wl = dict(WORKLOADS[args.workload])
@@ -330,6 +391,8 @@ def main():
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * 4096 * 2 * nL,
                 "d2h_bytes_per_step": T * 4096 * 4 * nL},
         "gpu_launches": r["launches_per_layer"] * nL * args.steps,
+        "launch": ("CUDA graphs: per layer [route] [expert FFN] [combine], replayed; events between "
+                   "replays time the expert-FFN call") if args.graph else "eager",
         "clocks": r["clocks"],
     }
     print(json.dumps(line))

@@ -82,7 +82,7 @@ def load(path: Optional[str] = None, build_if_stale: bool = True):
         "moe_route_topk": ([P, I, I, I, I, P, P, P], I),
         "moe_permute_workspace_size": ([I, I, I], Z),
         "moe_permute": ([P, I, I, I, P, P, P, P, Z, P], I),
-        "moe_vq2_expert_ffn_workspace_size": ([I, I, I, I], Z),
+        "moe_vq2_expert_ffn_workspace_size": ([I, I, I, I, I], Z),
         "moe_vq2_expert_ffn": ([P, P, P, P, P, I, I, I, P, P, P, Z, P], I),
         "moe_vq2_expert_ffn_noalloc": ([P, P, P, P, P, I, I, I, P, P, P], I),
         "moe_combine": ([P, P, P, P, I, I, I, P, P, P], I),
@@ -200,8 +200,8 @@ def moe_permute(ids, E: int, expert_offsets, sorted_pair, pair_to_sorted, ws=Non
                               _ptr(pair_to_sorted), _ptr(ws), nbytes, _stream(stream)))
 
 
-def moe_vq2_expert_ffn_workspace_size(T: int, k: int, E: int, I: int) -> int:
-    return load().moe_vq2_expert_ffn_workspace_size(T, k, E, I)
+def moe_vq2_expert_ffn_workspace_size(T: int, k: int, E: int, H: int, I: int) -> int:
+    return load().moe_vq2_expert_ffn_workspace_size(T, k, E, H, I)
 
 
 def moe_vq2_expert_ffn(table: SlotTable, x, expert_offsets, sorted_pair, weights, k: int, mode: int,
@@ -236,4 +236,4 @@ def moe_combine(ypair, pair_to_sorted, weights, pair_status, k: int, out_f32=Non
                               H, _ptr(out_f32), _ptr(out_bf16), _stream(stream)))
 
 
-from .layer import MoELayer, upload_layer  # noqa: E402  (the layer helper uses the functions above)
+from .layer import GraphedForward, MoELayer, upload_layer  # noqa: E402  (the layer helper uses the functions above)

@@ -178,9 +178,9 @@ moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_
     return launch_permute(ids, (int)P, E, expert_offsets, sorted_pair, pair_to_sorted, stream);
 }
 
-size_t moe_vq2_expert_ffn_workspace_size(int T, int k, int E, int I) {
-    if (T < 0 || k < 1 || E < 1 || I < 1) return 0;
-    return ffn_workspace_size(T, k, E, I);
+size_t moe_vq2_expert_ffn_workspace_size(int T, int k, int E, int H, int I) {
+    if (T < 0 || k < 1 || E < 1 || H < 1 || I < 1) return 0;
+    return ffn_workspace_size(T, k, E, H, I);
 }
 
 moe_status moe_vq2_expert_ffn(const moe_slot_table* table, const uint16_t* x,
@@ -197,7 +197,7 @@ moe_status moe_vq2_expert_ffn(const moe_slot_table* table, const uint16_t* x,
                   "moe_vq2_expert_ffn: null pointer");
     MOE_CHECK_SUPPORTED(aligned16(x) && aligned16(out_or_ypair) && aligned16(ws),
                         "moe_vq2_expert_ffn: x, out and ws must be 16-byte aligned");
-    size_t need = ffn_workspace_size(T, k, table->h.E, table->h.I);
+    size_t need = ffn_workspace_size(T, k, table->h.E, table->h.H, table->h.I);
     if (!ws || ws_bytes < need) {
         set_error("moe_vq2_expert_ffn: workspace %zu bytes, need %zu", ws_bytes, need);
         return MOE_ERR_WORKSPACE;

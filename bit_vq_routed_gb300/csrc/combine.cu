@@ -6,6 +6,9 @@
 namespace moe {
 namespace {
 
+// out[t, h..h+3] = sum_j status * w * ypair[pair_to_sorted[t*k+j], h..h+3] in
+// increasing j.  Lanes j < k fetch pair j's (row, weight) once and broadcast
+// them, so each thread issues its k row loads back to back.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ypair,
                                                       const int32_t* __restrict__ p2s,
                                                       const float* __restrict__ w,
@@ -13,27 +16,38 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       float* __restrict__ out32,
                                                       uint16_t* __restrict__ out16) {
     pdl_wait();
-    const int t = blockIdx.y;
+    const int t = blockIdx.y, lane = threadIdx.x & 31;
     const int h = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
-    if (h >= H) return;
+    int row = -1;
+    float wj = 0.0f;
+    if (lane < k) {
+        const int p = t * k + lane;
+        if (st[p]) {
+            row = p2s[p];
+            wj = w[p];
+        }
+    }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
-        const int p = t * k + j;
-        if (!st[p]) continue;
-        const float wj = w[p];
-        const float4 y = *reinterpret_cast<const float4*>(ypair + (size_t)p2s[p] * H + h);
-        acc.x = __fadd_rn(acc.x, __fmul_rn(wj, y.x));
-        acc.y = __fadd_rn(acc.y, __fmul_rn(wj, y.y));
-        acc.z = __fadd_rn(acc.z, __fmul_rn(wj, y.z));
-        acc.w = __fadd_rn(acc.w, __fmul_rn(wj, y.w));
+        const int r = __shfl_sync(0xffffffffu, row, j);
+        const float wv = __shfl_sync(0xffffffffu, wj, j);
+        if (r >= 0 && h < H) {
+            const float4 y = *reinterpret_cast<const float4*>(ypair + (size_t)r * H + h);
+            acc.x = __fadd_rn(acc.x, __fmul_rn(wv, y.x));
+            acc.y = __fadd_rn(acc.y, __fmul_rn(wv, y.y));
+            acc.z = __fadd_rn(acc.z, __fmul_rn(wv, y.z));
+            acc.w = __fadd_rn(acc.w, __fmul_rn(wv, y.w));
+        }
     }
-    if (out32) *reinterpret_cast<float4*>(out32 + (size_t)t * H + h) = acc;
-    if (out16) {
-        uint16_t* o = out16 + (size_t)t * H + h;
-        o[0] = __bfloat16_as_ushort(__float2bfloat16_rn(acc.x));
-        o[1] = __bfloat16_as_ushort(__float2bfloat16_rn(acc.y));
-        o[2] = __bfloat16_as_ushort(__float2bfloat16_rn(acc.z));
-        o[3] = __bfloat16_as_ushort(__float2bfloat16_rn(acc.w));
+    if (h < H) {
+        if (out32) *reinterpret_cast<float4*>(out32 + (size_t)t * H + h) = acc;
+        if (out16) {
+            const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.x)) |
+                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.y)) << 16);
+            const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.z)) |
+                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.w)) << 16);
+            *reinterpret_cast<uint2*>(out16 + (size_t)t * H + h) = make_uint2(lo, hi);
+        }
     }
     pdl_launch_dependents();
 }
@@ -47,7 +61,8 @@ moe_status launch_combine(const float* ypair, const int32_t* p2s, const float* w
         return MOE_ERR_UNSUPPORTED;
     }
     dim3 grid((unsigned)((H / 4 + 255) / 256), (unsigned)T);
-    combine_kernel<<<grid, 256, 0, s>>>(ypair, p2s, w, st, T, k, H, out32, out16);
+    cudaError_t e = launch_pdl(combine_kernel, grid, dim3(256), 0, s, ypair, p2s, w, st, T, k, H, out32, out16);
+    if (e != cudaSuccess) return cuda_status(e, "moe_combine: launch");
     MOE_LAUNCH_CHECK("moe_combine: launch");
     return MOE_OK;
 }

@@ -12,67 +12,29 @@
 // 128-input block in fp32 after the block's 8 MMAs.  FP4 (e2m1) bytes are
 // converted to f16x2 with cvt and scaled per 32-input block.
 // Code tiles stream into shared memory through a per-warp cp.async ring.
-#include "common.cuh"
+#include "ffn_common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int NT = 8;            // tokens per chunk: one n8 MMA tile
 constexpr int WARPS = 4;         // warps per CTA, one 16-row tile each
 constexpr int ROWS = 16 * WARPS;  // rows per work unit
 constexpr int STAGES = 8;        // cp.async ring depth per warp
 constexpr int STAGE_BYTES = 1024;  // two 512-byte tiles (gate + up) per step
 constexpr int CB_COPIES = 16;
 
-struct Chunk {
-    int32_t expert, start, count, fmt;
-};
-
-struct WsLayout {
-    size_t chunks_off, a_off, total;
-    int max_chunks;
-};
-
-__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-__host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int I) {
-    WsLayout L;
-    long long P = (long long)T * k;
-    L.max_chunks = (int)(P / NT + E);
-    L.chunks_off = 256;
-    L.a_off = align_up(L.chunks_off + sizeof(Chunk) * (size_t)L.max_chunks, 256);
-    L.total = L.a_off + sizeof(float) * (size_t)P * I;
-    return L;
-}
-
 // ---------------------------------------------------------------- schedule
-// One CTA of 1024 threads: expert e -> ceil(m_e / NT) chunks if resident;
-// pair_status of every pair from the residency of its expert.
-__global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restrict__ desc, int E,
-                                                        const int32_t* __restrict__ offsets,
-                                                        const int32_t* __restrict__ sorted_pair, int P,
-                                                        uint8_t* __restrict__ status, int* __restrict__ header,
-                                                        Chunk* __restrict__ chunks) {
-    __shared__ int warp_tot[32];
-    __shared__ int s_off[1025];
-    __shared__ uint8_t s_res[1024];
-    __shared__ uint8_t s_fmt[1024];
-    pdl_wait();
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i <= E; i += 1024) s_off[i] = offsets[i];
-    if (tid < E) {
-        s_res[tid] = (uint8_t)(desc[tid].resident != 0);
-        s_fmt[tid] = (uint8_t)desc[tid].format;
-    }
-    __syncthreads();
-    int m = tid < E ? s_off[tid + 1] - s_off[tid] : 0;
-    int n = (tid < E && s_res[tid] && m > 0) ? (m + NT - 1) / NT : 0;
-    int incl = n;
+// Exclusive scan over the 1024 threads of the block; returns the block total
+// through *total.
+__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         int o = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += o;
     }
+    __syncthreads();
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
@@ -83,17 +45,82 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
             if (lane >= off) wi += o;
         }
         warp_tot[lane] = wi - wv;
-        if (lane == 31) header[0] = wi;
+        if (lane == 31) warp_tot[32] = wi;
     }
     __syncthreads();
-    int base = incl - n + warp_tot[warp];
+    *total = warp_tot[32];
+    return incl - v + warp_tot[warp];
+}
+
+// One CTA of 1024 threads.  Expert e with m_e pairs, if resident:
+//   VQ2 with m_e == 1 (and use_lut) -> one activation-table pair;
+//   otherwise -> ceil(m_e / NT) tensor-core chunks.
+// Table pairs are listed sorted by (token, expert) and grouped by token, so
+// the experts of one token share each activation table.  pair_status of every
+// pair from the residency of its expert; the header's error word is cleared.
+__global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restrict__ desc, int E,
+                                                        const int32_t* __restrict__ offsets,
+                                                        const int32_t* __restrict__ sorted_pair, int P, int k,
+                                                        uint8_t* __restrict__ status, int* __restrict__ header,
+                                                        Chunk* __restrict__ chunks, int32_t* __restrict__ lut_s,
+                                                        int32_t* __restrict__ lut_e, int32_t* __restrict__ lut_grp,
+                                                        int32_t* __restrict__ grp_start, int use_lut) {
+    __shared__ int warp_tot[33];
+    __shared__ int s_off[1025];
+    __shared__ int s_tok[1024];  // token of each table pair, by expert (INT_MAX otherwise)
+    __shared__ int s_sorted_tok[1024];
+    __shared__ uint8_t s_res[1024];
+    __shared__ uint8_t s_fmt[1024];
+    pdl_wait();
+    const int tid = threadIdx.x;
+    for (int i = tid; i <= E; i += 1024) s_off[i] = offsets[i];
+    if (tid < E) {
+        s_res[tid] = (uint8_t)(desc[tid].resident != 0);
+        s_fmt[tid] = (uint8_t)desc[tid].format;
+    }
+    __syncthreads();
+    const int m = tid < E ? s_off[tid + 1] - s_off[tid] : 0;
+    const bool res = tid < E && s_res[tid] && m > 0;
+    const bool lut = res && use_lut && m == 1 && s_fmt[tid] == MOE_FMT_VQ2;
+    const int n = (res && !lut) ? (m + NT - 1) / NT : 0;
+    const int tok = lut ? sorted_pair[s_off[tid]] / k : 0x7fffffff;
+    s_tok[tid] = tok;
+    int n_chunks, n_lut;
+    const int cbase = block_exclusive_scan(n, warp_tot, &n_chunks);
     for (int c = 0; c < n; ++c) {
         Chunk ch;
         ch.expert = tid;
         ch.start = s_off[tid] + c * NT;
         ch.count = min(NT, m - c * NT);
         ch.fmt = s_fmt[tid];
-        chunks[base + c] = ch;
+        chunks[cbase + c] = ch;
+    }
+    block_exclusive_scan(lut ? 1 : 0, warp_tot, &n_lut);  // (its barriers also publish s_tok)
+    if (lut) {
+        // rank by (token, expert id): a stable sort of the table pairs by token
+        int rank = 0;
+        for (int e2 = 0; e2 < E; ++e2) {
+            const int t2 = s_tok[e2];
+            rank += (t2 < tok) || (t2 == tok && e2 < tid);
+        }
+        lut_s[rank] = s_off[tid];
+        lut_e[rank] = tid;
+        s_sorted_tok[rank] = tok;
+    }
+    __syncthreads();
+    const bool first = tid < n_lut && (tid == 0 || s_sorted_tok[tid] != s_sorted_tok[tid - 1]);
+    int n_groups;
+    const int gid = block_exclusive_scan(first ? 1 : 0, warp_tot, &n_groups) + (first ? 1 : 0) - 1;
+    if (tid < n_lut) {
+        lut_grp[tid] = gid;
+        if (first) grp_start[gid] = tid;
+    }
+    if (tid == 0) {
+        grp_start[n_groups] = n_lut;
+        header[HDR_NCHUNKS] = n_chunks;
+        header[HDR_NLUT] = n_lut;
+        header[HDR_ERR] = 0;
+        header[HDR_NGROUPS] = n_groups;
     }
     for (int s = tid; s < P; s += 1024) {
         int lo = 0, hi = E;  // find e with off[e] <= s < off[e+1]
@@ -145,16 +172,17 @@ __global__ void __launch_bounds__(32 * WARPS, 1) ffn_mma_kernel(
     const int i = lane >> 2, j = lane & 3;
     uint8_t* ring = xt + NT * (2 * K + 32) + warp * STAGES * STAGE_BYTES;
 
+    pdl_wait();
+    const int n_chunks = header[HDR_NCHUNKS];
+    const int row_groups = R / ROWS;
+    const long n_items = (long)n_chunks * row_groups;
+    if (blockIdx.x >= n_items) return;  // no tensor-core work for this CTA
     for (int idx = threadIdx.x; idx < 256 * CB_COPIES; idx += blockDim.x) {
         int c = idx / CB_COPIES;
         const uint2 e = reinterpret_cast<const uint2*>(codebook)[c & 127];
         uint32_t flip = (c & 0x80) ? 0x80008000u : 0u;
         cbt[idx] = make_uint2(e.x ^ flip, e.y ^ flip);
     }
-    pdl_wait();
-    const int n_chunks = header[0];
-    const int row_groups = R / ROWS;
-    const long n_items = (long)n_chunks * row_groups;
 
     for (long item = blockIdx.x; item < n_items; item += gridDim.x) {
         const Chunk ch = chunks[item / row_groups];
@@ -318,7 +346,7 @@ size_t mma_smem_bytes(int K) { return 256 * CB_COPIES * 8 + (size_t)NT * (2 * K 
 
 }  // namespace
 
-size_t ffn_workspace_size(int T, int k, int E, int I) { return ws_layout(T, k, E, I).total; }
+size_t ffn_workspace_size(int T, int k, int E, int H, int I) { return ws_layout(T, k, E, H, I).total; }
 
 moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const int32_t* offsets,
                              const int32_t* sorted_pair, const float* weights, int T, int k, int mode,
@@ -326,12 +354,25 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     (void)ws_bytes;
     const int E = t->E, H = t->H, I = t->I;
     const int P = T * k;
-    const WsLayout L = ws_layout(T, k, E, I);
-    int* header = reinterpret_cast<int*>(ws);
-    Chunk* chunks = reinterpret_cast<Chunk*>(static_cast<char*>(ws) + L.chunks_off);
-    float* abuf = reinterpret_cast<float*>(static_cast<char*>(ws) + L.a_off);
+    if (k > 32) {  // the experts of one token are handled as one group of at most 32
+        set_error("moe_vq2_expert_ffn: k=%d above 32", k);
+        return MOE_ERR_UNSUPPORTED;
+    }
+    const WsLayout L = ws_layout(T, k, E, H, I);
+    char* w = static_cast<char*>(ws);
+    int* header = reinterpret_cast<int*>(w);
+    Chunk* chunks = reinterpret_cast<Chunk*>(w + L.chunks_off);
+    int32_t* lut_s = reinterpret_cast<int32_t*>(w + L.lut_s_off);
+    int32_t* lut_e = reinterpret_cast<int32_t*>(w + L.lut_e_off);
+    int32_t* lut_grp = reinterpret_cast<int32_t*>(w + L.lut_grp_off);
+    int32_t* grp_start = reinterpret_cast<int32_t*>(w + L.grp_start_off);
+    float* abuf = reinterpret_cast<float*>(w + L.a_off);
+    const int use_lut = 1;
+    cudaError_t e;
 
-    schedule_kernel<<<1, 1024, 0, s>>>(t->d_desc, E, offsets, sorted_pair, P, status, header, chunks);
+    e = launch_pdl(schedule_kernel, dim3(1), dim3(1024), 0, s, (const SlotDesc*)t->d_desc, E, offsets, sorted_pair, P,
+                   k, status, header, chunks, lut_s, lut_e, lut_grp, grp_start, use_lut);
+    if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule launch");
     MOE_LAUNCH_CHECK("moe_vq2_expert_ffn: schedule launch");
 
     const size_t smem1 = mma_smem_bytes(H), smem2 = mma_smem_bytes(I);
@@ -339,19 +380,27 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
         set_error("moe_vq2_expert_ffn: H=%d / I=%d too large for the decode kernel's shared memory", H, I);
         return MOE_ERR_UNSUPPORTED;
     }
-    cudaError_t e;
-    e = cudaFuncSetAttribute(ffn_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
+    e = ensure_smem_attr(ffn_mma_kernel<2>, (int)smem1);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: smem attribute");
-    e = cudaFuncSetAttribute(ffn_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+    e = ensure_smem_attr(ffn_mma_kernel<1>, (int)smem2);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: smem attribute");
 
     const unsigned grid = (unsigned)num_sms();
-    ffn_mma_kernel<2><<<grid, 32 * WARPS, smem1, s>>>(t->d_desc, t->codebook, x, nullptr, sorted_pair, weights,
-                                                       k, H, I, header, chunks, abuf, nullptr, mode);
+    moe_status st;
+    if (use_lut && (st = launch_lut_fc(true, t, x, sorted_pair, k, w, L, s)) != MOE_OK) return st;
+    e = launch_pdl(ffn_mma_kernel<2>, dim3(grid), dim3(32 * WARPS), smem1, s, t->d_desc, t->codebook, x,
+                   (const float*)nullptr, sorted_pair, weights, k, H, I, (const int*)header, (const Chunk*)chunks,
+                   abuf, (float*)nullptr, mode);
+    if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: FC1 launch");
     MOE_LAUNCH_CHECK("moe_vq2_expert_ffn: FC1 launch");
-    ffn_mma_kernel<1><<<grid, 32 * WARPS, smem2, s>>>(t->d_desc, t->codebook, nullptr, abuf, sorted_pair,
-                                                       weights, k, I, H, header, chunks, nullptr, out, mode);
+    if (use_lut && (st = launch_lut_fc(false, t, x, sorted_pair, k, w, L, s)) != MOE_OK) return st;
+    e = launch_pdl(ffn_mma_kernel<1>, dim3(grid), dim3(32 * WARPS), smem2, s, t->d_desc, t->codebook,
+                   (const uint16_t*)nullptr, (const float*)abuf, sorted_pair, weights, k, I, H, (const int*)header,
+                   (const Chunk*)chunks, (float*)nullptr, out, mode);
+    if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: FC2 launch");
     MOE_LAUNCH_CHECK("moe_vq2_expert_ffn: FC2 launch");
+    if (use_lut && (st = launch_lut_finish(t, sorted_pair, weights, k, mode, out, w, L, L.max_lut, s)) != MOE_OK)
+        return st;
     return MOE_OK;
 }
 

@@ -1,0 +1,65 @@
+// Work description shared by the expert-FFN kernels: the workspace layout
+// and the schedule records.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int NT = 8;          // tokens per MMA chunk (one n8 MMA tile)
+constexpr int LUT_KB = 4;      // scale blocks (x 128 inputs) per activation-table job
+
+// A run of <= NT sorted positions of one expert (tensor-core path).
+struct Chunk {
+    int32_t expert, start, count, fmt;
+};
+
+// Header words at the start of the workspace.
+enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3 };
+
+// Activation-table pairs (single-token VQ2 experts) are listed sorted by
+// token: lut_s / lut_e (sorted position, expert), lut_grp (token group of
+// each), grp_start (first pair of each token group, then n_lut).
+struct WsLayout {
+    size_t chunks_off, lut_s_off, lut_e_off, lut_grp_off, grp_start_off, a_off, p1_off, p2_off, total;
+    int max_chunks, max_lut;
+};
+
+__host__ __device__ inline size_t ws_align(size_t v) { return (v + 255) / 256 * 256; }
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// K-ranges of the activation-table path for an input length K.
+__host__ __device__ inline int lut_jobs(int K) { return ceil_div(K / 128, LUT_KB); }
+
+__host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I) {
+    WsLayout L;
+    long long P = (long long)T * k;
+    L.max_chunks = (int)(P / NT + E);
+    L.max_lut = (int)(P < E ? P : E);  // single-token experts: at most one per expert
+    size_t o = 256;
+    L.chunks_off = o;
+    o = ws_align(o + sizeof(Chunk) * (size_t)L.max_chunks);
+    L.lut_s_off = o;
+    o = ws_align(o + sizeof(int32_t) * (size_t)L.max_lut);
+    L.lut_e_off = o;
+    o = ws_align(o + sizeof(int32_t) * (size_t)L.max_lut);
+    L.lut_grp_off = o;
+    o = ws_align(o + sizeof(int32_t) * (size_t)L.max_lut);
+    L.grp_start_off = o;
+    o = ws_align(o + sizeof(int32_t) * ((size_t)L.max_lut + 1));
+    L.a_off = o;
+    o = ws_align(o + sizeof(float) * (size_t)P * I);
+    L.p1_off = o;
+    o = ws_align(o + sizeof(float) * (size_t)L.max_lut * lut_jobs(H) * 2 * I);
+    L.p2_off = o;
+    o = ws_align(o + sizeof(float) * (size_t)L.max_lut * lut_jobs(I) * H);
+    L.total = o;
+    return L;
+}
+
+moe_status launch_lut_fc(bool fc1, const SlotTableHost* t, const uint16_t* x, const int32_t* sorted_pair,
+                         int k, char* ws, const WsLayout& L, cudaStream_t s);
+moe_status launch_lut_finish(const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
+                             int mode, float* out, char* ws, const WsLayout& L, int max_lut, cudaStream_t s);
+
+}  // namespace moe

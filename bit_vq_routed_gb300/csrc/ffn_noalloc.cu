@@ -62,11 +62,11 @@ moe_status moe_vq2_expert_ffn_noalloc(const moe_slot_table* table, const uint16_
                   "moe_vq2_expert_ffn_noalloc: null pointer");
     MOE_CHECK_SUPPORTED(aligned16(x) && aligned16(out_or_ypair),
                         "moe_vq2_expert_ffn_noalloc: x and out must be 16-byte aligned");
-    const size_t need = ffn_workspace_size(T, k, table->h.E, table->h.I);
+    const size_t need = ffn_workspace_size(T, k, table->h.E, table->h.H, table->h.I);
     if (need > kScratchBytes) {
-        set_error("moe_vq2_expert_ffn_noalloc: T=%d k=%d E=%d I=%d needs %zu bytes of scratch, above the "
-                  "fixed %zu (use moe_vq2_expert_ffn with a caller workspace)",
-                  T, k, table->h.E, table->h.I, need, kScratchBytes);
+        set_error("moe_vq2_expert_ffn_noalloc: T=%d k=%d E=%d H=%d I=%d needs %zu bytes of scratch, above "
+                  "the fixed %zu (use moe_vq2_expert_ffn with a caller workspace)",
+                  T, k, table->h.E, table->h.H, table->h.I, need, kScratchBytes);
         return MOE_ERR_UNSUPPORTED;
     }
     void* scratch = nullptr;

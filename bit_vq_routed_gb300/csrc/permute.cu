@@ -86,11 +86,12 @@ moe_status launch_permute(const int32_t* ids, int P, int E, int32_t* offsets, in
                           int32_t* pair_to_sorted, cudaStream_t s) {
     size_t smem = sizeof(int32_t) * (size_t)E * 33;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return cuda_status(e, "moe_permute: shared memory attribute");
+        cudaError_t ea = ensure_smem_attr(permute_kernel, (int)smem);
+        if (ea != cudaSuccess) return cuda_status(ea, "moe_permute: shared memory attribute");
     }
-    permute_kernel<<<1, PT, smem, s>>>(ids, P, E, offsets, sorted_pair, pair_to_sorted);
+    cudaError_t e = launch_pdl(permute_kernel, dim3(1), dim3(PT), smem, s, ids, P, E, offsets, sorted_pair,
+                               pair_to_sorted);
+    if (e != cudaSuccess) return cuda_status(e, "moe_permute: launch");
     MOE_LAUNCH_CHECK("moe_permute: launch");
     return MOE_OK;
 }

@@ -92,7 +92,53 @@ __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
     return v > bv || (v == bv && e < be);
 }
 
-// One warp per token: k rounds of a warp-wide arg-max over (logit desc, id asc).
+// Small-batch router: one CTA of 8 warps per (token, 8 experts); the token's
+// activations sit in shared memory and each lane first loads all of its
+// router-weight chunks, so a warp needs one memory round trip.  Same fixed
+// summation order as router_logits_kernel.
+__global__ void __launch_bounds__(256) router_logits_small_kernel(const uint16_t* __restrict__ x,
+                                                                  const uint16_t* __restrict__ w,
+                                                                  const float* __restrict__ bias,
+                                                                  float* __restrict__ logits, int T, int H,
+                                                                  int E) {
+    extern __shared__ __align__(16) uint4 xs[];
+    const int t = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + warp;
+    const int nch = H / 8;
+    pdl_wait();
+    for (int i = threadIdx.x; i < nch; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(x + (size_t)t * H)[i];
+    __syncthreads();
+    if (e >= E) return;
+    const uint4* wr = reinterpret_cast<const uint4*>(w + (size_t)e * H);
+    const int per = H / 256;  // chunks per lane
+    float acc = 0.0f;
+    constexpr int U = 16;
+    for (int m0 = 0; m0 < per; m0 += U) {
+        uint4 wv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (m0 + u < per) wv[u] = __ldg(wr + lane + 32 * (m0 + u));
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (m0 + u < per) {
+                float xf[8], wf[8];
+                unpack_bf16x8(xs[lane + 32 * (m0 + u)], xf);
+                unpack_bf16x8(wv[u], wf);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, __fmul_rn(xf[i], wf[i]));
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(FULL, acc, off));
+    if (lane == 0) logits[(size_t)t * E + e] = bias ? __fadd_rn(acc, bias[e]) : acc;
+    pdl_launch_dependents();
+}
+
+// One warp per token: lane l holds logits l, l+32, ...; each lane keeps its
+// best not-yet-taken (logit desc, id asc); k rounds of a warp-wide arg-max,
+// after which only the lane that owned the winner rescans its values.
+template <int NPER>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E,
                                                          int k, int renorm, int32_t* __restrict__ ids,
                                                          float* __restrict__ weights) {
@@ -101,58 +147,65 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     const long t = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= T) return;
     const float* l = logits + (size_t)t * E;
-    const int nper = (E + 31) / 32;  // <= 32
-    float v[32];
+    float v[NPER];
     uint32_t taken = 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        int e = lane + 32 * i;
-        if (i < nper && e < E)
+    for (int i = 0; i < NPER; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E)
             v[i] = l[e];
         else {
             v[i] = -INFINITY;
             taken |= 1u << i;
         }
     }
-    float sel_v = 0.0f;  // lane j keeps the j-th selected logit
-    int sel_e = 0;
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int be = INT_MAX;
+    float bv = -INFINITY;
+    int be = INT_MAX;
+    auto rescan = [&]() {
+        bv = -INFINITY;
+        be = INT_MAX;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            int e = lane + 32 * i;
+        for (int i = 0; i < NPER; ++i) {
+            const int e = lane + 32 * i;
             if (!((taken >> i) & 1) && better(v[i], e, bv, be)) {
                 bv = v[i];
                 be = e;
             }
         }
+    };
+    rescan();
+    float sel_v = 0.0f;  // lane j keeps the j-th selected logit
+    int sel_e = 0;
+    for (int j = 0; j < k; ++j) {
+        float wv = bv;
+        int we = be;
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) {
-            float ov = __shfl_xor_sync(FULL, bv, off);
-            int oe = __shfl_xor_sync(FULL, be, off);
-            if (better(ov, oe, bv, be)) {
-                bv = ov;
-                be = oe;
+            const float ov = __shfl_xor_sync(FULL, wv, off);
+            const int oe = __shfl_xor_sync(FULL, we, off);
+            if (better(ov, oe, wv, we)) {
+                wv = ov;
+                we = oe;
             }
         }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
         if (lane == j) {
-            sel_v = bv;
-            sel_e = be;
+            sel_v = wv;
+            sel_e = we;
+        }
+        if ((we & 31) == lane) {
+            taken |= 1u << (we >> 5);
+            rescan();
         }
     }
     const float top = __shfl_sync(FULL, sel_v, 0);
-    float num = lane < k ? expf(sel_v - top) : 0.0f;
+    const float num = lane < k ? expf(sel_v - top) : 0.0f;
     float den = 0.0f;
     if (renorm) {
         den = num;
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            int e = lane + 32 * i;
-            if (i < nper && e < E) den += expf(v[i] - top);
-        }
+        for (int i = 0; i < NPER; ++i)
+            if (lane + 32 * i < E) den += expf(v[i] - top);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(FULL, den, off);
@@ -168,14 +221,18 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 moe_status launch_router_logits(const uint16_t* x, const uint16_t* w, const float* bias, float* logits,
                                 int T, int H, int E, cudaStream_t s) {
     const int threads = 256;
-    if (T <= 16) {
-        long warps = (long)T * E;
-        long blocks = (warps * 32 + threads - 1) / threads;
-        router_logits_kernel<1><<<(unsigned)blocks, threads, 0, s>>>(x, w, bias, logits, T, H, E);
+    const size_t xs_bytes = (size_t)H * 2;
+    if (T <= 64 && xs_bytes <= 48 * 1024) {
+        dim3 grid((unsigned)((E + 7) / 8), (unsigned)T);
+        cudaError_t e = launch_pdl(router_logits_small_kernel, grid, dim3(threads), xs_bytes, s, x, w, bias, logits, T,
+                                   H, E);
+        if (e != cudaSuccess) return cuda_status(e, "moe_router_logits: launch");
     } else {
         long warps = (long)T * ((E + 3) / 4);
         long blocks = (warps * 32 + threads - 1) / threads;
-        router_logits_kernel<4><<<(unsigned)blocks, threads, 0, s>>>(x, w, bias, logits, T, H, E);
+        cudaError_t e = launch_pdl(router_logits_kernel<4>, dim3((unsigned)blocks), dim3(threads), 0, s, x, w, bias,
+                                   logits, T, H, E);
+        if (e != cudaSuccess) return cuda_status(e, "moe_router_logits: launch");
     }
     MOE_LAUNCH_CHECK("moe_router_logits: launch");
     return MOE_OK;
@@ -184,8 +241,15 @@ moe_status launch_router_logits(const uint16_t* x, const uint16_t* w, const floa
 moe_status launch_route_topk(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
                              float* weights, cudaStream_t s) {
     const int threads = 256;
-    long blocks = ((long)T * 32 + threads - 1) / threads;
-    route_topk_kernel<<<(unsigned)blocks, threads, 0, s>>>(logits, T, E, k, renorm, ids, weights);
+    const unsigned blocks = (unsigned)(((long)T * 32 + threads - 1) / threads);
+    auto kern = E <= 32    ? route_topk_kernel<1>
+                : E <= 64  ? route_topk_kernel<2>
+                : E <= 128 ? route_topk_kernel<4>
+                : E <= 256 ? route_topk_kernel<8>
+                : E <= 512 ? route_topk_kernel<16>
+                           : route_topk_kernel<32>;
+    cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(threads), 0, s, logits, T, E, k, renorm, ids, weights);
+    if (e != cudaSuccess) return cuda_status(e, "moe_route_topk: launch");
     MOE_LAUNCH_CHECK("moe_route_topk: launch");
     return MOE_OK;
 }

@@ -72,7 +72,7 @@ class MoELayer:
         self.pair_status = torch.empty(P, dtype=torch.uint8, device=device)
         self.ypair = torch.empty(P, H, dtype=f32, device=device)
         self.out = torch.empty(T_max, H, dtype=f32, device=device)
-        self.ws = torch.empty(moe_vq2_expert_ffn_workspace_size(T_max, k, E, I), dtype=torch.uint8,
+        self.ws = torch.empty(moe_vq2_expert_ffn_workspace_size(T_max, k, E, H, I), dtype=torch.uint8,
                               device=device)
 
     def set_expert(self, e: int, fmt: int, packed_codes, packed_scales, stream=None):
@@ -107,6 +107,25 @@ class MoELayer:
         moe_combine(self.ypair[:T * self.k], self.pair_to_sorted[:T * self.k], self.weights[:T],
                     self.pair_status[:T * self.k], self.k, o, None, stream)
         return o
+
+
+class GraphedForward:
+    """MoELayer.forward for a fixed batch of T tokens captured in a CUDA graph
+    (all of its kernels, no host work per step): write the tokens into
+    ``self.x``, call ``replay()``, read ``self.out``."""
+
+    def __init__(self, layer: MoELayer, T: int, device="cuda"):
+        self.layer = layer
+        self.x = torch.zeros(T, layer.H, dtype=torch.bfloat16, device=device)
+        layer.forward(self.x)  # first eager call: kernel attributes are set outside capture
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.out = layer.forward(self.x)
+
+    def replay(self):
+        self.graph.replay()
+        return self.out
 
 
 def upload_layer(H, I, E, k, T_max, codebook, w_router, bias, experts, renormalize=1, resident=None,

@@ -182,10 +182,11 @@ moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_
  * resident (such pairs are skipped, never substituted; their rows of ypair
  * are left untouched).  expert_offsets/sorted_pair come from moe_permute
  * over the same ids; weights fp32 [T,k] from moe_route_topk.
- * ws: moe_vq2_expert_ffn_workspace_size(T, k, E, I) bytes of device memory
- * (scratch: the schedule and the fp32 intermediate a [P, I]).
- * Requires H % 256 == 0, I % 128 == 0, x 16-byte aligned. */
-size_t moe_vq2_expert_ffn_workspace_size(int T, int k, int E, int I);
+ * ws: moe_vq2_expert_ffn_workspace_size(T, k, E, H, I) bytes of device
+ * memory (scratch: the schedule, the fp32 intermediate a [P, I] and the
+ * K-range partial sums of single-token experts).
+ * Requires H % 256 == 0, I % 128 == 0, k <= 32, x 16-byte aligned. */
+size_t moe_vq2_expert_ffn_workspace_size(int T, int k, int E, int H, int I);
 moe_status moe_vq2_expert_ffn(const moe_slot_table* table, const uint16_t* x,
                               const int32_t* expert_offsets, const int32_t* sorted_pair,
                               const float* weights, int T, int k, int mode, float* out_or_ypair,
@@ -209,7 +210,7 @@ moe_status moe_vq2_expert_ffn(const moe_slot_table* table, const uint16_t* x,
  *
  * Limits and rules:
  *   - the call fails with MOE_ERR_UNSUPPORTED, and enqueues nothing, when
- *     moe_vq2_expert_ffn_workspace_size(T, k, E, I) exceeds
+ *     moe_vq2_expert_ffn_workspace_size(T, k, E, H, I) exceeds
  *     MOE_NOALLOC_SCRATCH_BYTES (64 MiB: at H = 4096, I = 2048 this covers
  *     decode batches of up to 32 tokens at top-8, and more);
  *   - the first call on each device looks up the device address of the

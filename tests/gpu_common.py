@@ -65,6 +65,13 @@ def run(dev, x_bits):
                 out=out.cpu().numpy().copy())
 
 
+def device_error_word(dev):
+    """The bounded-wait error word of the expert-FFN workspace (0 = none)."""
+    import torch
+    torch.cuda.synchronize()
+    return int(dev.ws[8:12].view(torch.int32).item())
+
+
 def assert_routing_exact(g, r):
     assert np.array_equal(g["logits"].view(np.uint32), r["logits"].view(np.uint32)), "router logits bits"
     assert np.array_equal(g["ids"], r["ids"])

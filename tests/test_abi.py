@@ -91,7 +91,9 @@ def test_slot_table_and_ffn_reject_bad_args(lib):
 
 
 def test_workspace_sizes(lib):
-    n = lib.moe_vq2_expert_ffn_workspace_size(1, 8, 256, 2048)
+    n = lib.moe_vq2_expert_ffn_workspace_size(1, 8, 256, 4096, 2048)
     assert n >= 8 * 2048 * 4
-    assert lib.moe_vq2_expert_ffn_workspace_size(4096, 8, 256, 2048) >= 32768 * 2048 * 4
+    assert lib.moe_vq2_expert_ffn_workspace_size(4096, 8, 256, 4096, 2048) >= 32768 * 2048 * 4
+    # decode batch 32 at top-8 fits the scratch-free variant's fixed scratch
+    assert lib.moe_vq2_expert_ffn_workspace_size(32, 8, 256, 4096, 2048) <= bv.MOE_NOALLOC_SCRATCH_BYTES
     assert lib.moe_permute_workspace_size(4096, 8, 256) == 0

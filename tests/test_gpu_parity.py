@@ -7,8 +7,8 @@ import pytest
 
 import moe_synth as ms
 import oracle
-from gpu_common import (assert_close, assert_routing_exact, device_layer, run, torch_cuda,
-                        MAX_REL_RMS, MEAN_REL)
+from gpu_common import (assert_close, assert_routing_exact, device_error_word, device_layer, run,
+                        torch_cuda, MAX_REL_RMS, MEAN_REL)
 
 pytestmark = pytest.mark.gpu
 O = oracle.default
@@ -30,6 +30,7 @@ def _check_layer(spec, T, seed=0, resident=None):
     res = np.ones(spec.E, bool) if resident is None else resident
     assert np.array_equal(g["status"], res[r["ids"]].ravel().astype(np.uint8))
     assert_close(g["out"], r["partial"], f"T={T} E={spec.E} k={spec.k}")
+    assert device_error_word(dev) == 0
     return layer, x, dev, keep, g, r
 
 
@@ -46,6 +47,15 @@ def test_tiny_layer_fp4_experts(torch):
 @pytest.mark.parametrize("T,E,k", [(1, 8, 2), (37, 4, 2), (5, 16, 3), (64, 8, 8), (3, 1, 1), (17, 32, 1)])
 def test_ragged_and_degenerate_shapes(torch, T, E, k):
     spec = ms.LayerSpec(H=256, I=128, E=E, k=k, seed=T + 10 * E + k)
+    _check_layer(spec, T, seed=T)
+
+
+@pytest.mark.parametrize("H,I,T,E,k", [(512, 256, 1, 16, 4), (1024, 640, 2, 64, 8), (1536, 384, 3, 32, 6),
+                                        (4096, 2048, 1, 16, 8), (768, 128, 5, 128, 3)])
+def test_single_token_experts_table_path(torch, H, I, T, E, k):
+    # experts that get one token go through the activation-table kernels;
+    # K-ranges of 1-4 scale blocks (H, I not multiples of 512) included
+    spec = ms.LayerSpec(H=H, I=I, E=E, k=k, seed=H + I + T)
     _check_layer(spec, T, seed=T)
 
 

@@ -59,7 +59,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(torch):
     layer = ms.Layer(spec)
     dev, keep = device_layer(layer, 1)
     T = 4096  # needs T*k*I*4 = 256 MiB of scratch, above the fixed 64 MiB
-    assert bv.moe_vq2_expert_ffn_workspace_size(T, 8, 8, 2048) > bv.MOE_NOALLOC_SCRATCH_BYTES
+    assert bv.moe_vq2_expert_ffn_workspace_size(T, 8, 8, 256, 2048) > bv.MOE_NOALLOC_SCRATCH_BYTES
     x = torch.zeros(T, 256, dtype=torch.bfloat16, device="cuda")
     w = torch.zeros(T, 8, dtype=torch.float32, device="cuda")
     sp = torch.zeros(T * 8, dtype=torch.int32, device="cuda")
