@@ -83,8 +83,15 @@ moe_status moe_slot_table_create(int num_experts, int H, int I, const uint16_t* 
     t->h.H = H;
     t->h.I = I;
     t->h.codebook = codebook;
+    t->h.h_fmt = (uint8_t*)calloc((size_t)num_experts, 1);
+    if (!t->h.h_fmt) {
+        free(t);
+        set_error("moe_slot_table_create: out of host memory");
+        return MOE_ERR_NO_MEM;
+    }
     cudaError_t e = cudaMalloc(&t->h.d_desc, sizeof(SlotDesc) * (size_t)num_experts);
     if (e != cudaSuccess) {
+        free(t->h.h_fmt);
         free(t);
         set_error("moe_slot_table_create: cudaMalloc: %s", cudaGetErrorString(e));
         return MOE_ERR_NO_MEM;
@@ -92,6 +99,7 @@ moe_status moe_slot_table_create(int num_experts, int H, int I, const uint16_t* 
     e = cudaMemset(t->h.d_desc, 0, sizeof(SlotDesc) * (size_t)num_experts);
     if (e != cudaSuccess) {
         cudaFree(t->h.d_desc);
+        free(t->h.h_fmt);
         free(t);
         return cuda_status(e, "moe_slot_table_create: cudaMemset");
     }
@@ -116,7 +124,12 @@ moe_status moe_slot_table_set(moe_slot_table* t, int expert_id, const moe_expert
         s.codes[m] = d->codes[m];
         s.scales[m] = d->scales[m];
     }
-    return launch_slot_set(t->h.d_desc, expert_id, s, stream);
+    moe_status st = launch_slot_set(t->h.d_desc, expert_id, s, stream);
+    if (st == MOE_OK) {
+        t->h.n_fp4 += (d->format == MOE_FMT_FP4) - (t->h.h_fmt[expert_id] == 1 + MOE_FMT_FP4);
+        t->h.h_fmt[expert_id] = (uint8_t)(1 + d->format);
+    }
+    return st;
 }
 
 moe_status moe_slot_table_evict(moe_slot_table* t, int expert_id, cudaStream_t stream) {
@@ -124,12 +137,18 @@ moe_status moe_slot_table_evict(moe_slot_table* t, int expert_id, cudaStream_t s
     MOE_CHECK_ARG(expert_id >= 0 && expert_id < t->h.E,
                   "moe_slot_table_evict: expert_id=%d out of [0, %d)", expert_id, t->h.E);
     SlotDesc s = {};
-    return launch_slot_set(t->h.d_desc, expert_id, s, stream);
+    moe_status st = launch_slot_set(t->h.d_desc, expert_id, s, stream);
+    if (st == MOE_OK) {
+        t->h.n_fp4 -= (t->h.h_fmt[expert_id] == 1 + MOE_FMT_FP4);
+        t->h.h_fmt[expert_id] = 0;
+    }
+    return st;
 }
 
 moe_status moe_slot_table_destroy(moe_slot_table* t) {
     if (!t) return MOE_OK;
     cudaError_t e = cudaFree(t->h.d_desc);
+    free(t->h.h_fmt);
     free(t);
     if (e != cudaSuccess) return cuda_status(e, "moe_slot_table_destroy: cudaFree");
     return MOE_OK;

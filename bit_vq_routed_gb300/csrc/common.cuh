@@ -54,6 +54,8 @@ struct SlotTableHost {
     int E, H, I;
     const uint16_t* codebook;  // device fp16 [128*4]
     SlotDesc* d_desc;          // device [E]
+    uint8_t* h_fmt;            // host mirror: 0 = empty, 1 + format of each entry
+    int n_fp4;                 // FP4 entries currently set
 };
 
 // ---------------------------------------------------------------- layouts

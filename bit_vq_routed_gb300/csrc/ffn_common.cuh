@@ -6,23 +6,30 @@
 
 namespace moe {
 
-constexpr int NT = 8;          // tokens per MMA chunk (one n8 MMA tile)
+constexpr int MMA_NT = 32;     // tokens per mma.sync chunk (four n8 MMA tiles)
 constexpr int LUT_KB = 4;      // scale blocks (x 128 inputs) per activation-table job
+constexpr int UMMA_MIN = 64;   // tokens from which an expert takes the tcgen05 path
+constexpr int UMMA_NT = 128;   // tokens per tcgen05 chunk
 
-// A run of <= NT sorted positions of one expert (tensor-core path).
+// A run of sorted positions of one expert (tensor-core paths).
 struct Chunk {
     int32_t expert, start, count, fmt;
 };
 
 // Header words at the start of the workspace.
-enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3 };
+enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NUMMA = 4 };
 
 // Activation-table pairs (single-token VQ2 experts) are listed sorted by
 // token: lut_s / lut_e (sorted position, expert), lut_grp (token group of
 // each), grp_start (first pair of each token group, then n_lut).
+// Experts with at least UMMA_MIN pairs (possible once P >= UMMA_MIN) take
+// the tcgen05 path (uchunks: chunks of <= UMMA_NT sorted positions); the
+// tensor-core paths read x16s (fp16 activations gathered by sorted position)
+// and a16 (fp16 silu(g)*u by sorted position).
 struct WsLayout {
-    size_t chunks_off, lut_s_off, lut_e_off, lut_grp_off, grp_start_off, a_off, p1_off, p2_off, total;
-    int max_chunks, max_lut;
+    size_t chunks_off, lut_s_off, lut_e_off, lut_grp_off, grp_start_off, p1_off, p2_off;
+    size_t uchunks_off, x16s_off, a16_off, total;
+    int max_chunks, max_lut, max_uchunks;
 };
 
 __host__ __device__ inline size_t ws_align(size_t v) { return (v + 255) / 256 * 256; }
@@ -34,7 +41,7 @@ __host__ __device__ inline int lut_jobs(int K) { return ceil_div(K / 128, LUT_KB
 __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I) {
     WsLayout L;
     long long P = (long long)T * k;
-    L.max_chunks = (int)(P / NT + E);
+    L.max_chunks = (int)(P / MMA_NT + E);
     L.max_lut = (int)(P < E ? P : E);  // single-token experts: at most one per expert
     size_t o = 256;
     L.chunks_off = o;
@@ -47,18 +54,30 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I)
     o = ws_align(o + sizeof(int32_t) * (size_t)L.max_lut);
     L.grp_start_off = o;
     o = ws_align(o + sizeof(int32_t) * ((size_t)L.max_lut + 1));
-    L.a_off = o;
-    o = ws_align(o + sizeof(float) * (size_t)P * I);
     L.p1_off = o;
     o = ws_align(o + sizeof(float) * (size_t)L.max_lut * lut_jobs(H) * 2 * I);
     L.p2_off = o;
     o = ws_align(o + sizeof(float) * (size_t)L.max_lut * lut_jobs(I) * H);
+    const bool umma = P >= UMMA_MIN;
+    L.max_uchunks = umma ? (int)(P / UMMA_NT + E) : 0;
+    L.uchunks_off = o;
+    o = ws_align(o + sizeof(Chunk) * (size_t)L.max_uchunks);
+    L.x16s_off = o;
+    o = ws_align(o + sizeof(uint16_t) * (size_t)P * H);
+    L.a16_off = o;
+    o = ws_align(o + sizeof(uint16_t) * (size_t)P * I);
     L.total = o;
     return L;
 }
 
 moe_status launch_lut_fc(bool fc1, const SlotTableHost* t, const uint16_t* x, const int32_t* sorted_pair,
                          int k, char* ws, const WsLayout& L, cudaStream_t s);
+moe_status launch_gather_f16(const uint16_t* x, const int32_t* sorted_pair, int k, int H, int P, uint16_t* x16s,
+                             cudaStream_t s);
+moe_status launch_umma(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
+                       int P, int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s);
+moe_status launch_mma_fc(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
+                         int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s);
 moe_status launch_lut_finish(const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
                              int mode, float* out, char* ws, const WsLayout& L, int max_lut, cudaStream_t s);
 

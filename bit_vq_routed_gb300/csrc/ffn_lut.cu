@@ -18,14 +18,14 @@
 // silu(g) * u) and the finishing kernel.
 //
 // Each warp streams its units' code and scale tiles straight into registers
-// with 16-byte loads, fetching the next unit while it computes the current
-// one (16 warps per SM keep about 70 KB in flight).
+// with 16-byte loads, fetching two units ahead of the one it computes (12
+// warps per SM keep about 80 KB in flight).
 #include "ffn_common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int CW = 16;                    // warps
+constexpr int CW = 12;                    // warps
 constexpr int THREADS = 32 * CW;
 constexpr uint32_t LUT_ADDR = 0x10000;    // table: [0x10000, 0x30000) of the shared window
 constexpr uint32_t LUT_HALF = 0x10000;    // scale blocks 0-1 | 2-3
@@ -183,9 +183,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncthreads();
 
-        // this warp's units of the job: v = u + warp, u + warp + CW, ...
-        auto load_unit = [&](int v, UnitRegs& r) {
-            const int wj = v - job_start, pi = wj / RT, rt = wj - pi * RT;
+        // this warp's units of the job: v = u + warp, u + warp + CW, ...; the
+        // (pair, row tile) of a unit advances by CW row tiles per step
+        auto load_unit = [&](int pi, int rt, UnitRegs& r) {
             const bool second = FC1 && rt >= I / 16;  // an up-matrix row tile
             const int rtm = second ? rt - I / 16 : rt;
             const size_t tile = (size_t)rtm * KB + LUT_KB * kr + b;
@@ -198,11 +198,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                 r.sc[1] = ldg_stream(sp + 8);
             }
         };
-        UnitRegs cur, nxt;
+        auto advance = [&](int& pi, int& rt) {
+            rt += CW;
+            while (rt >= RT) {
+                rt -= RT;
+                ++pi;
+            }
+        };
+        UnitRegs cur, n1, n2;
         int v = u + warp;
-        if (v < seg_end) load_unit(v, cur);
+        int pi = (v - job_start) / RT, rt = (v - job_start) - ((v - job_start) / RT) * RT;
+        int pi1 = pi, rt1 = rt, pi2, rt2;
+        advance(pi1, rt1);
+        pi2 = pi1;
+        rt2 = rt1;
+        advance(pi2, rt2);
+        if (v < seg_end) load_unit(pi, rt, cur);
+        if (v + CW < seg_end) load_unit(pi1, rt1, n1);
         for (; v < seg_end; v += CW) {
-            if (v + CW < seg_end) load_unit(v + CW, nxt);
+            if (v + 2 * CW < seg_end) load_unit(pi2, rt2, n2);
             float acc[16];
             if (active) {
                 float s[16];
@@ -245,12 +259,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
             if ((lane & 1) == 0) {
-                const int wj = v - job_start, pi = wj / RT, rt = wj - pi * RT;
                 const int p = lane >> 1;
                 const int row = (p >> 1) + 8 * (p & 1);
                 pout[((size_t)(gs + pi) * KR + kr) * R + (size_t)rt * 16 + row] = acc[0];
             }
-            cur = nxt;
+            cur = n1;
+            n1 = n2;
+            pi = pi1;
+            rt = rt1;
+            pi1 = pi2;
+            rt1 = rt2;
+            advance(pi2, rt2);
         }
         u = seg_end;
     }

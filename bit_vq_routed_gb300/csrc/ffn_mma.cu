@@ -1,0 +1,315 @@
+// Tensor-core mma.sync path of the expert FFN for experts with 2..63 tokens
+// in the call (and FP4 experts with any count below the tcgen05 threshold).
+//
+// mma.sync m16n8k16 (fp16 in, fp32 accumulate) on weights decoded in
+// registers.  A VQ2 code byte indexes a sign-folded codebook (256 entries:
+// each index and its negation) held in shared memory 16 times over, so the two
+// half-warps of an 8-byte lookup hit distinct banks; the entry's 4 fp16
+// values are exactly one thread's A-fragment for one row: the K order inside
+// each 16-wide MMA step is permuted so a thread's 4 k-slots are one code's 4
+// inputs, and the activations use the same permutation.  The row scale is
+// applied in fp32 once per 128-input block.  FP4 (e2m1) bytes become f16x2
+// with cvt and are scaled per 32 inputs.
+//
+// A CTA of 8 warps takes items (chunk of <= 32 tokens of one expert, 8 x 32
+// weight rows); each warp owns two 16-row tiles (FC1: the gate and the up
+// tile of the same rows; FC2: two down tiles), so every activation fragment
+// feeds two tiles.  K is walked in slabs of 512 inputs: the chunk's fp16
+// activations (gathered by sorted position) and each warp's code and scale
+// tiles for the next slab stream into shared memory with cp.async while the
+// current slab is computed.
+#include "ffn_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int WARPS = 8;
+constexpr int THREADS = 32 * WARPS;
+constexpr int NTOK = MMA_NT;        // tokens per chunk (4 n8 tiles)
+constexpr int SLAB = 512;           // inputs per slab (VQ2; FP4 slabs are 256 inputs)
+constexpr int XSTRIDE = 2 * SLAB + 32;  // bytes per token row of a slab (padding: B-fragment banks)
+constexpr int TILE_CODES = 2048;    // one 16-row tile x one slab: 512 VQ2 inputs or 256 FP4 inputs
+constexpr int TILE_SCALES = 128;    // 16 rows x 4 fp16 (VQ2) or x 8 ue8m0 (FP4)
+constexpr int WARP_BYTES = 2 * (TILE_CODES + TILE_SCALES);  // per warp per slab (two tiles)
+constexpr int CB_COPIES = 16;
+
+struct __align__(16) Smem {
+    uint2 cbt[256 * CB_COPIES];
+    uint8_t xs[2][NTOK * XSTRIDE];
+    uint8_t w[2][WARPS][WARP_BYTES];
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds_u64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// FC1 = true: A tiles are the gate and up tiles of 16 I-rows, B = x16s (K = H);
+// FC1 = false: A tiles are two down tiles (32 H-rows), B = a16 (K = I).
+template <bool FC1>
+__global__ void __launch_bounds__(THREADS, 1)
+    ffn_mma_kernel(const SlotDesc* __restrict__ desc, const uint16_t* __restrict__ codebook,
+                   const uint16_t* __restrict__ bsrc, const int32_t* __restrict__ sorted_pair,
+                   const float* __restrict__ weights, int k, int H, int I, const int* __restrict__ header,
+                   const Chunk* __restrict__ chunks, uint16_t* __restrict__ a16, float* __restrict__ out, int mode) {
+    extern __shared__ __align__(16) uint8_t dyn[];
+    Smem& S = *reinterpret_cast<Smem*>(dyn);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int i = lane >> 2, j = lane & 3;
+    const int K = FC1 ? H : I;
+    const int R = FC1 ? I : H;                      // rows per matrix
+    const int ROWS = FC1 ? 16 * WARPS : 32 * WARPS;  // rows per item
+    const int n_rg = R / ROWS;
+
+    pdl_wait();
+    const int n_chunks = header[HDR_NCHUNKS];
+    const int n_items = n_chunks * n_rg;
+    if ((int)blockIdx.x >= n_items) return;
+    for (int idx = tid; idx < 256 * CB_COPIES; idx += THREADS) {
+        const int c = idx / CB_COPIES;
+        const uint2 e = reinterpret_cast<const uint2*>(codebook)[c & 127];
+        const uint32_t flip = (c & 0x80) ? 0x80008000u : 0u;
+        S.cbt[idx] = make_uint2(e.x ^ flip, e.y ^ flip);
+    }
+    const uint32_t cbt = smem_u32(&S.cbt[0]) + 8u * (lane & 15);
+
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const Chunk ch = chunks[item / n_rg];
+        const int rg = item % n_rg;
+        const SlotDesc& d = desc[ch.expert];
+        const bool vq2 = ch.fmt == MOE_FMT_VQ2;
+        const int n_nt = (ch.count + 7) >> 3;
+        // this warp's two 16-row tiles: (matrix, row tile)
+        int mt[2], rtt[2];
+        if (FC1) {
+            mt[0] = 0, mt[1] = 1;
+            rtt[0] = rtt[1] = rg * WARPS + warp;
+        } else {
+            mt[0] = mt[1] = 2;
+            rtt[0] = (rg * WARPS + warp) * 2;
+            rtt[1] = rtt[0] + 1;
+        }
+        const int KB = vq2 ? K / 128 : K / 32;  // scale blocks per row
+        const int KT = vq2 ? K / 128 : K / 64;  // 512-byte code tiles per row tile
+        const int slab_in = vq2 ? SLAB : SLAB / 2;
+        const int nslab = (K + slab_in - 1) / slab_in;
+
+        // issue the cp.async copies of slab sl into buffer sl & 1
+        auto issue = [&](int sl) {
+            const int buf = sl & 1;
+            const int k0 = sl * slab_in, kn = min(slab_in, K - k0);
+            // activations: NTOK rows x kn fp16, zero rows past the chunk
+            const int chunks_per_row = kn / 8;
+            for (int idx = tid; idx < NTOK * chunks_per_row; idx += THREADS) {
+                const int n = idx / chunks_per_row, c = idx - n * chunks_per_row;
+                const bool valid = n < ch.count;
+                const uint16_t* src = bsrc + (size_t)(ch.start + (valid ? n : 0)) * K + k0 + 8 * c;
+                cp_async16(smem_u32(&S.xs[buf][n * XSTRIDE + 16 * c]), src, valid);
+            }
+            // this warp's code tiles and scales
+            uint8_t* wb = &S.w[buf][warp][0];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const uint8_t* cbase = static_cast<const uint8_t*>(d.codes[mt[t]]);
+                const int ntile = vq2 ? kn / 128 : kn / 64;  // 512-byte tiles in this slab
+                const int tile0 = vq2 ? k0 / 128 : k0 / 64;
+                const uint8_t* src = cbase + ((size_t)rtt[t] * KT + tile0) * 512;
+                for (int c = lane; c < ntile * 32; c += 32)
+                    cp_async16(smem_u32(wb + t * TILE_CODES + 16 * c), src + 16 * c, true);
+                const int sblk = vq2 ? kn / 128 : kn / 32;  // scale blocks in this slab
+                const int sb0 = vq2 ? k0 / 128 : k0 / 32;
+                const int sbytes = vq2 ? 32 * sblk : 16 * sblk;  // 16 rows x (fp16 | ue8m0)
+                const uint8_t* ssrc = static_cast<const uint8_t*>(d.scales[mt[t]]) +
+                                      ((size_t)rtt[t] * KB + sb0) * (vq2 ? 32 : 16);
+                for (int c = lane; c < sbytes / 16; c += 32)
+                    cp_async16(smem_u32(wb + 2 * TILE_CODES + t * TILE_SCALES + 16 * c), ssrc + 16 * c, true);
+            }
+            cp_async_commit();
+        };
+
+        float acc[2][4][4];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[t][nt][q] = 0.0f;
+
+        __syncthreads();  // the previous item is done with both buffers
+        issue(0);
+        for (int sl = 0; sl < nslab; ++sl) {
+            if (sl + 1 < nslab) {
+                issue(sl + 1);
+                cp_async_wait1();
+            } else {
+                cp_async_wait0();
+            }
+            __syncthreads();  // everyone's copies of slab sl have landed
+            const int buf = sl & 1;
+            const int kn = min(slab_in, K - sl * slab_in);
+            const uint32_t xs = smem_u32(&S.xs[buf][0]);
+            const uint32_t wb = smem_u32(&S.w[buf][warp][0]);
+            if (vq2) {
+                for (int kb = 0; kb < kn / 128; ++kb) {
+                    float tmp[2][4][4];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) tmp[t][nt][q] = 0.0f;
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const int g = 4 * s + j;  // this thread's group in the scale block
+                        uint2 b[4];
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt)
+                            if (nt < n_nt) b[nt] = lds_u64(xs + (8 * nt + i) * XSTRIDE + 2 * (kb * 128 + 4 * g));
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            const uint32_t pr = lds_u16(wb + t * TILE_CODES + kb * 512 + 16 * g + 2 * i);
+                            const uint2 lo = lds_u64(cbt + 128u * (pr & 0xffu));
+                            const uint2 hi = lds_u64(cbt + 128u * (pr >> 8));
+#pragma unroll
+                            for (int nt = 0; nt < 4; ++nt)
+                                if (nt < n_nt) mma_16816(tmp[t][nt], lo.x, hi.x, lo.y, hi.y, b[nt].x, b[nt].y);
+                        }
+                    }
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const uint32_t sa = wb + 2 * TILE_CODES + t * TILE_SCALES + kb * 32;
+                        const float s_lo = __half2float(__ushort_as_half((unsigned short)lds_u16(sa + 2 * i)));
+                        const float s_hi = __half2float(__ushort_as_half((unsigned short)lds_u16(sa + 2 * (i + 8))));
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt) {
+                            acc[t][nt][0] = fmaf(s_lo, tmp[t][nt][0], acc[t][nt][0]);
+                            acc[t][nt][1] = fmaf(s_lo, tmp[t][nt][1], acc[t][nt][1]);
+                            acc[t][nt][2] = fmaf(s_hi, tmp[t][nt][2], acc[t][nt][2]);
+                            acc[t][nt][3] = fmaf(s_hi, tmp[t][nt][3], acc[t][nt][3]);
+                        }
+                    }
+                }
+            } else {
+                for (int kt = 0; kt < kn / 64; ++kt) {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {  // 32-element scale blocks
+                        float tmp[2][4][4];
+#pragma unroll
+                        for (int t = 0; t < 2; ++t)
+#pragma unroll
+                            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) tmp[t][nt][q] = 0.0f;
+#pragma unroll
+                        for (int s2 = 0; s2 < 2; ++s2) {
+                            const int s = 2 * half + s2;
+                            const int e0 = kt * 64 + 16 * s + 2 * j;  // element of k-slot 2j
+                            uint32_t b0[4], b1[4];
+#pragma unroll
+                            for (int nt = 0; nt < 4; ++nt)
+                                if (nt < n_nt) {
+                                    b0[nt] = lds_u32(xs + (8 * nt + i) * XSTRIDE + 2 * e0);
+                                    b1[nt] = lds_u32(xs + (8 * nt + i) * XSTRIDE + 2 * (e0 + 8));
+                                }
+#pragma unroll
+                            for (int t = 0; t < 2; ++t) {
+                                const uint32_t w = lds_u32(wb + t * TILE_CODES + kt * 512 + 16 * lane + 4 * s);
+                                uint32_t r0, r1, r2, r3;  // row i lo-k, row i hi-k, row i+8 lo-k, row i+8 hi-k
+                                e2m1x8_to_f16x8(w, r0, r1, r2, r3);
+#pragma unroll
+                                for (int nt = 0; nt < 4; ++nt)
+                                    if (nt < n_nt) mma_16816(tmp[t][nt], r0, r2, r1, r3, b0[nt], b1[nt]);
+                            }
+                        }
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            const uint32_t sa = wb + 2 * TILE_CODES + t * TILE_SCALES + (2 * kt + half) * 16;
+                            uint32_t e_lo, e_hi;
+                            asm volatile("ld.shared.u8 %0, [%1];" : "=r"(e_lo) : "r"(sa + i));
+                            asm volatile("ld.shared.u8 %0, [%1];" : "=r"(e_hi) : "r"(sa + i + 8));
+                            const float s_lo = e8m0_to_float(e_lo), s_hi = e8m0_to_float(e_hi);
+#pragma unroll
+                            for (int nt = 0; nt < 4; ++nt) {
+                                acc[t][nt][0] = fmaf(s_lo, tmp[t][nt][0], acc[t][nt][0]);
+                                acc[t][nt][1] = fmaf(s_lo, tmp[t][nt][1], acc[t][nt][1]);
+                                acc[t][nt][2] = fmaf(s_hi, tmp[t][nt][2], acc[t][nt][2]);
+                                acc[t][nt][3] = fmaf(s_hi, tmp[t][nt][3], acc[t][nt][3]);
+                            }
+                        }
+                    }
+                }
+            }
+            __syncthreads();  // buffer buf is free for the copies of slab sl + 2
+        }
+
+        // epilogue: acc[t][nt] holds (row i | i+8 of tile t, tokens 8nt + 2j | +1)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            if (nt >= n_nt) continue;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int tok = 8 * nt + 2 * j + (q & 1);
+                if (tok >= ch.count) continue;
+                const int spos = ch.start + tok;
+                const int r16 = i + ((q & 2) ? 8 : 0);
+                if (FC1) {
+                    const int row = rtt[0] * 16 + r16;
+                    const float g = acc[0][nt][q], u = acc[1][nt][q];
+                    a16[(size_t)spos * I + row] = __half_as_ushort(__float2half_rn(g / (1.0f + expf(-g)) * u));
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const int row = rtt[t] * 16 + r16;
+                        if (mode == MOE_PER_PAIR) {
+                            out[(size_t)spos * H + row] = acc[t][nt][q];
+                        } else {
+                            const int p = sorted_pair[spos];
+                            atomicAdd(out + (size_t)(p / k) * H + row, weights[p] * acc[t][nt][q]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    pdl_launch_dependents();
+}
+
+}  // namespace
+
+size_t mma_smem_bytes() { return sizeof(Smem); }
+
+moe_status launch_mma_fc(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
+                         int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s) {
+    const int* header = reinterpret_cast<const int*>(ws);
+    const Chunk* chunks = reinterpret_cast<const Chunk*>(ws + L.chunks_off);
+    const uint16_t* x16s = reinterpret_cast<const uint16_t*>(ws + L.x16s_off);
+    uint16_t* a16 = reinterpret_cast<uint16_t*>(ws + L.a16_off);
+    auto kern = fc1 ? ffn_mma_kernel<true> : ffn_mma_kernel<false>;
+    cudaError_t e = ensure_smem_attr(kern, (int)sizeof(Smem));
+    if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: mma kernel shared memory");
+    e = launch_pdl(kern, dim3((unsigned)num_sms()), dim3(THREADS), sizeof(Smem), s, (const SlotDesc*)t->d_desc,
+                   t->codebook, fc1 ? x16s : (const uint16_t*)a16, sorted_pair, weights, k, t->H, t->I, header,
+                   chunks, a16, out, mode);
+    if (e != cudaSuccess) return cuda_status(e, fc1 ? "moe_vq2_expert_ffn: FC1 launch" : "moe_vq2_expert_ffn: FC2 launch");
+    return MOE_OK;
+}
+
+}  // namespace moe
