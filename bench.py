@@ -219,8 +219,10 @@ def run_gpu(args, wl, world, rank, local):
         # stream between replays (event records cannot sit inside a capture).
         def piece(fn):
             g = torch.cuda.CUDAGraph()
+            n0 = bv.moe_launch_count()
             with torch.cuda.graph(g):
                 fn()
+            g.kernels = bv.moe_launch_count() - n0  # library kernel nodes in this graph
             return g
 
         def route_fn(L, s):
@@ -246,18 +248,25 @@ def run_gpu(args, wl, world, rank, local):
             graphs.append(seq)
 
         def run(s, evs=None):
+            n = 0
             for item in graphs[s % G]:
                 if item[0] == "g":
                     item[1].replay()
+                    n += item[1].kernels
                 else:
                     L, g = item[1], item[2]
                     if evs is not None:
                         evs[L][0].record()
                     g.replay()
+                    n += g.kernels
                     if evs is not None:
                         evs[L][1].record()
+            return n
     else:
-        run = step
+        def run(s, evs=None):
+            n0 = bv.moe_launch_count()
+            step(s, evs)
+            return bv.moe_launch_count() - n0
     stream = torch.cuda.current_stream()
     for s in range(args.warmup):
         run(s)
@@ -269,9 +278,10 @@ def run_gpu(args, wl, world, rank, local):
     clocks.start()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    launches = 0
     start.record(stream)
     for s in range(args.steps):
-        run(args.warmup + s, step_ev[s])
+        launches += run(args.warmup + s, step_ev[s])
     end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -321,7 +331,7 @@ def run_gpu(args, wl, world, rank, local):
         e2e_ms = float(t.item())
         torch.distributed.destroy_process_group()
     return dict(ms_total=ms_total, ffn_ms=ffn_ms, code_bytes=code_bytes, clocks=clk, e2e_ms=e2e_ms,
-                e2e_steps=e2e_steps, launches_per_layer=10)
+                e2e_steps=e2e_steps, launches=launches)
 
 
 def main():
@@ -390,7 +400,7 @@ def main():
         "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * 4096 * 2 * nL,
                 "d2h_bytes_per_step": T * 4096 * 4 * nL},
-        "gpu_launches": r["launches_per_layer"] * nL * args.steps,
+        "gpu_launches": r["launches"],
         "launch": ("CUDA graphs: per layer [route] [expert FFN] [combine], replayed; events between "
                    "replays time the expert-FFN call") if args.graph else "eager",
         "clocks": r["clocks"],

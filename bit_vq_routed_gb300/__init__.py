@@ -53,6 +53,7 @@ EXPORTED = [
     "moe_slot_table_set", "moe_slot_table_evict", "moe_slot_table_destroy", "moe_router_logits",
     "moe_route_topk", "moe_permute_workspace_size", "moe_permute",
     "moe_vq2_expert_ffn_workspace_size", "moe_vq2_expert_ffn", "moe_vq2_expert_ffn_noalloc", "moe_combine",
+    "moe_launch_count",
 ]
 
 
@@ -86,6 +87,7 @@ def load(path: Optional[str] = None, build_if_stale: bool = True):
         "moe_vq2_expert_ffn": ([P, P, P, P, P, I, I, I, P, P, P, Z, P], I),
         "moe_vq2_expert_ffn_noalloc": ([P, P, P, P, P, I, I, I, P, P, P], I),
         "moe_combine": ([P, P, P, P, I, I, I, P, P, P], I),
+        "moe_launch_count": ([], ctypes.c_uint64),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -237,3 +239,9 @@ def moe_combine(ypair, pair_to_sorted, weights, pair_status, k: int, out_f32=Non
 
 
 from .layer import GraphedForward, MoELayer, upload_layer  # noqa: E402  (the layer helper uses the functions above)
+
+
+def moe_launch_count() -> int:
+    """Kernel launches the library has issued since it was loaded (a launch
+    inside a stream capture counts once)."""
+    return int(load().moe_launch_count())

@@ -4,9 +4,15 @@
 #include <stdio.h>
 #include <stdlib.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace moe {
+
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 static thread_local char g_err[512] = "";
 
@@ -36,6 +42,8 @@ using namespace moe;
 extern "C" {
 
 int moe_version(void) { return 1; }
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* moe_last_error(void) { return g_err; }
 

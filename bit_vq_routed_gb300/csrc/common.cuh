@@ -77,9 +77,11 @@ __host__ __device__ inline int fp4_in_tile(int r16, int lb) {
 }
 
 // ---------------------------------------------------------------- PTX
+// (not volatile: a pure function of its registers, free to be scheduled
+// around the loads that feed it)
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -195,6 +197,10 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
 // while its predecessor on the stream finishes; every kernel of the library
 // calls pdl_wait() before it touches memory a predecessor may write or read,
 // so only the prologues (shared-memory set-up, constant weights) overlap.
+// Host-side count of kernel launches the library has issued (a launch made
+// inside a stream capture counts once: it becomes one graph node).
+void count_launch();
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args... args) {
@@ -208,6 +214,7 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    count_launch();
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 

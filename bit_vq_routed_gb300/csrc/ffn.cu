@@ -3,7 +3,7 @@
 // The schedule kernel sorts each resident expert of the call to one path by
 // its token count m_e:
 //   - VQ2, m_e == 1: the activation-table kernels (ffn_lut.cu);
-//   - VQ2, m_e >= 64: the tcgen05 kernels (ffn_umma.cu);
+//   - VQ2, m_e >= 32: the tcgen05 kernels (ffn_umma.cu);
 //   - otherwise: the mma.sync kernels (ffn_mma.cu), chunks of <= 32 tokens.
 #include "ffn_common.cuh"
 
@@ -159,7 +159,7 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     Chunk* uchunks = reinterpret_cast<Chunk*>(w + L.uchunks_off);
     uint16_t* x16s = reinterpret_cast<uint16_t*>(w + L.x16s_off);
     const int use_lut = 1;
-    const int use_umma = P >= UMMA_MIN ? 1 : 0;
+    const int use_umma = T >= UMMA_MIN ? 1 : 0;  // an expert gets at most T of the pairs
     // With one token no expert gets two pairs, so the mma.sync kernels only
     // have work if the table holds FP4 experts.
     const bool mma = T > 1 || t->n_fp4 > 0 || !use_lut;

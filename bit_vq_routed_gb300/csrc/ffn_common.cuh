@@ -8,7 +8,7 @@ namespace moe {
 
 constexpr int MMA_NT = 32;     // tokens per mma.sync chunk (four n8 MMA tiles)
 constexpr int LUT_KB = 4;      // scale blocks (x 128 inputs) per activation-table job
-constexpr int UMMA_MIN = 64;   // tokens from which an expert takes the tcgen05 path
+constexpr int UMMA_MIN = 32;   // tokens from which an expert takes the tcgen05 path
 constexpr int UMMA_NT = 128;   // tokens per tcgen05 chunk
 
 // A run of sorted positions of one expert (tensor-core paths).
@@ -22,7 +22,7 @@ enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NU
 // Activation-table pairs (single-token VQ2 experts) are listed sorted by
 // token: lut_s / lut_e (sorted position, expert), lut_grp (token group of
 // each), grp_start (first pair of each token group, then n_lut).
-// Experts with at least UMMA_MIN pairs (possible once P >= UMMA_MIN) take
+// Experts with at least UMMA_MIN pairs (possible once T >= UMMA_MIN) take
 // the tcgen05 path (uchunks: chunks of <= UMMA_NT sorted positions); the
 // tensor-core paths read x16s (fp16 activations gathered by sorted position)
 // and a16 (fp16 silu(g)*u by sorted position).
@@ -58,7 +58,7 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I)
     o = ws_align(o + sizeof(float) * (size_t)L.max_lut * lut_jobs(H) * 2 * I);
     L.p2_off = o;
     o = ws_align(o + sizeof(float) * (size_t)L.max_lut * lut_jobs(I) * H);
-    const bool umma = P >= UMMA_MIN;
+    const bool umma = T >= UMMA_MIN;
     L.max_uchunks = umma ? (int)(P / UMMA_NT + E) : 0;
     L.uchunks_off = o;
     o = ws_align(o + sizeof(Chunk) * (size_t)L.max_uchunks);

@@ -1,4 +1,4 @@
-// Tensor-core mma.sync path of the expert FFN for experts with 2..63 tokens
+// Tensor-core mma.sync path of the expert FFN for experts with 2..31 tokens
 // in the call (and FP4 experts with any count below the tcgen05 threshold).
 //
 // mma.sync m16n8k16 (fp16 in, fp32 accumulate) on weights decoded in
@@ -46,21 +46,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
-__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint2 lds_u64(uint32_t a) {
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-    return v;
-}
+// shared-memory reads as plain C++ accesses (the compiler may overlap them)
+__device__ __forceinline__ uint32_t sh_u16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
+__device__ __forceinline__ uint2 sh_u64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ uint32_t sh_u32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
 // FC1 = true: A tiles are the gate and up tiles of 16 I-rows, B = x16s (K = H);
 // FC1 = false: A tiles are two down tiles (32 H-rows), B = a16 (K = I).
@@ -89,7 +78,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t flip = (c & 0x80) ? 0x80008000u : 0u;
         S.cbt[idx] = make_uint2(e.x ^ flip, e.y ^ flip);
     }
-    const uint32_t cbt = smem_u32(&S.cbt[0]) + 8u * (lane & 15);
+    const uint8_t* cbt = reinterpret_cast<const uint8_t*>(&S.cbt[0]) + 8 * (lane & 15);
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         const Chunk ch = chunks[item / n_rg];
@@ -165,8 +154,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncthreads();  // everyone's copies of slab sl have landed
             const int buf = sl & 1;
             const int kn = min(slab_in, K - sl * slab_in);
-            const uint32_t xs = smem_u32(&S.xs[buf][0]);
-            const uint32_t wb = smem_u32(&S.w[buf][warp][0]);
+            const uint8_t* xs = &S.xs[buf][0];
+            const uint8_t* wb = &S.w[buf][warp][0];
             if (vq2) {
                 for (int kb = 0; kb < kn / 128; ++kb) {
                     float tmp[2][4][4];
@@ -182,12 +171,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         uint2 b[4];
 #pragma unroll
                         for (int nt = 0; nt < 4; ++nt)
-                            if (nt < n_nt) b[nt] = lds_u64(xs + (8 * nt + i) * XSTRIDE + 2 * (kb * 128 + 4 * g));
+                            if (nt < n_nt) b[nt] = sh_u64(xs + (8 * nt + i) * XSTRIDE + 2 * (kb * 128 + 4 * g));
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
-                            const uint32_t pr = lds_u16(wb + t * TILE_CODES + kb * 512 + 16 * g + 2 * i);
-                            const uint2 lo = lds_u64(cbt + 128u * (pr & 0xffu));
-                            const uint2 hi = lds_u64(cbt + 128u * (pr >> 8));
+                            const uint32_t pr = sh_u16(wb + t * TILE_CODES + kb * 512 + 16 * g + 2 * i);
+                            const uint2 lo = sh_u64(cbt + 128u * (pr & 0xffu));
+                            const uint2 hi = sh_u64(cbt + 128u * (pr >> 8));
 #pragma unroll
                             for (int nt = 0; nt < 4; ++nt)
                                 if (nt < n_nt) mma_16816(tmp[t][nt], lo.x, hi.x, lo.y, hi.y, b[nt].x, b[nt].y);
@@ -195,9 +184,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
-                        const uint32_t sa = wb + 2 * TILE_CODES + t * TILE_SCALES + kb * 32;
-                        const float s_lo = __half2float(__ushort_as_half((unsigned short)lds_u16(sa + 2 * i)));
-                        const float s_hi = __half2float(__ushort_as_half((unsigned short)lds_u16(sa + 2 * (i + 8))));
+                        const uint8_t* sa = wb + 2 * TILE_CODES + t * TILE_SCALES + kb * 32;
+                        const float s_lo = __half2float(__ushort_as_half((unsigned short)sh_u16(sa + 2 * i)));
+                        const float s_hi = __half2float(__ushort_as_half((unsigned short)sh_u16(sa + 2 * (i + 8))));
 #pragma unroll
                         for (int nt = 0; nt < 4; ++nt) {
                             acc[t][nt][0] = fmaf(s_lo, tmp[t][nt][0], acc[t][nt][0]);
@@ -226,12 +215,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                             for (int nt = 0; nt < 4; ++nt)
                                 if (nt < n_nt) {
-                                    b0[nt] = lds_u32(xs + (8 * nt + i) * XSTRIDE + 2 * e0);
-                                    b1[nt] = lds_u32(xs + (8 * nt + i) * XSTRIDE + 2 * (e0 + 8));
+                                    b0[nt] = sh_u32(xs + (8 * nt + i) * XSTRIDE + 2 * e0);
+                                    b1[nt] = sh_u32(xs + (8 * nt + i) * XSTRIDE + 2 * (e0 + 8));
                                 }
 #pragma unroll
                             for (int t = 0; t < 2; ++t) {
-                                const uint32_t w = lds_u32(wb + t * TILE_CODES + kt * 512 + 16 * lane + 4 * s);
+                                const uint32_t w = sh_u32(wb + t * TILE_CODES + kt * 512 + 16 * lane + 4 * s);
                                 uint32_t r0, r1, r2, r3;  // row i lo-k, row i hi-k, row i+8 lo-k, row i+8 hi-k
                                 e2m1x8_to_f16x8(w, r0, r1, r2, r3);
 #pragma unroll
@@ -241,10 +230,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
-                            const uint32_t sa = wb + 2 * TILE_CODES + t * TILE_SCALES + (2 * kt + half) * 16;
-                            uint32_t e_lo, e_hi;
-                            asm volatile("ld.shared.u8 %0, [%1];" : "=r"(e_lo) : "r"(sa + i));
-                            asm volatile("ld.shared.u8 %0, [%1];" : "=r"(e_hi) : "r"(sa + i + 8));
+                            const uint8_t* sa = wb + 2 * TILE_CODES + t * TILE_SCALES + (2 * kt + half) * 16;
+                            const uint32_t e_lo = sa[i], e_hi = sa[i + 8];
                             const float s_lo = e8m0_to_float(e_lo), s_hi = e8m0_to_float(e_hi);
 #pragma unroll
                             for (int nt = 0; nt < 4; ++nt) {

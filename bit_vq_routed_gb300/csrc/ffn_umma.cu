@@ -2,25 +2,27 @@
 // prefill-sized batch of tokens (m_e >= UMMA_MIN).  Here the expert FFN is a
 // dense contraction: FC1 is [m_e x H] x [H x 2I], FC2 [m_e x I] x [I x H].
 //
-// One CTA per SM loops over work items (chunk of <= 128 tokens of one expert,
-// tile of 128 weight rows).  Per 64-input K-block:
-//   - 4 decoder warps turn the tile's VQ2 codes into fp16 weights
+// One CTA per SM loops over work items (chunk of <= 128 tokens of one
+// expert, two 128-row weight tiles: FC1 the gate and the up tile of the same
+// 128 rows, FC2 two consecutive down tiles).  Warp roles:
+//   - 8 decoder warps turn the item's VQ2 codes into fp16 weights
 //     (sign-folded codebook entry x row scale, rounded once to fp16) and store
 //     them into shared memory in the 128-byte-swizzled K-major layout the
-//     tensor core reads (A operand, 128 rows x 64);
+//     tensor core reads (A operand, 128 rows x 64 per K-block); each thread
+//     fetches its codes three K-blocks ahead;
 //   - a TMA warp loads the chunk's activations (B operand, 128 tokens x 64,
 //     fp16, same swizzle) with cp.async.bulk.tensor from a token-gathered
 //     copy in the workspace;
 //   - one thread issues tcgen05.mma (M128 N128 K16, fp16 in, fp32 in TMEM)
-//     and tcgen05.commit frees the stage when the tensor core is done.
-// After the last K-block the decoder warps read the accumulator back with
-// tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = weight rows) and run the
-// epilogue: FC1 rows 0-63 are gate rows and 64-127 the matching up rows, so
-// the up half goes through shared memory and a = silu(g) * u is stored as
-// fp16 (the FC2 B operand, gathered by sorted position); FC2 stores y per
-// pair or adds w * y into the token's output.
-// Every wait is bounded: a wait that gives up records an error word and the
-// CTA runs on to its end without issuing more work.
+//     and tcgen05.commit frees each stage when the tensor core is done;
+//   - 4 epilogue warps read the accumulators back with tcgen05.ld (each warp
+//     owns one quarter of the TMEM lanes = weight rows) and store FC1's
+//     a = silu(g) * u as fp16 (the FC2 B operand) or FC2's y per pair / w*y
+//     into the token's output.
+// The accumulators are double-buffered in TMEM, so the epilogue of one item
+// overlaps the main loop of the next.  Every wait is bounded: a wait that
+// gives up records an error word and the CTA runs on to its end without
+// issuing more work.
 #include <cudaTypedefs.h>
 
 #include "ffn_common.cuh"
@@ -28,24 +30,22 @@
 namespace moe {
 namespace {
 
-constexpr int UM_M = 128, UM_N = 128, UM_K = 64;
+constexpr int UM_M = 128, UM_N = UMMA_NT, UM_K = 64;
 constexpr int STAGES = 4;
-constexpr int DEC_WARPS = 4;                  // decoder + epilogue warps
-constexpr int TMA_WARP = 4, MMA_WARP = 5;
-constexpr int THREADS = 32 * 6;
-constexpr int A_BYTES = UM_M * UM_K * 2;      // 16 KB
+constexpr int DEC_WARPS = 8, EPI_WARPS = 4;
+constexpr int TMA_WARP = DEC_WARPS, MMA_WARP = DEC_WARPS + 1;  // then the epilogue warps
+constexpr int THREADS = 32 * (DEC_WARPS + 2 + EPI_WARPS);
+constexpr int A_BYTES = UM_M * UM_K * 2;      // 16 KB per A tile
 constexpr int B_BYTES = UM_N * UM_K * 2;      // 16 KB
 constexpr int CB_COPIES = 16;
-constexpr uint32_t TMEM_COLS = 128;
 // instruction descriptor: D f32, A/B f16, both K-major, N = 128, M = 128
 constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(UM_N >> 3) << 17) | ((uint32_t)(UM_M >> 4) << 24);
 
 struct __align__(1024) Smem {
-    uint8_t a[STAGES][A_BYTES];
+    uint8_t a[STAGES][2][A_BYTES];  // FC1: gate tile, up tile; FC2: two down tiles
     uint8_t b[STAGES][B_BYTES];
-    float xch[64][UM_N + 1];      // FC1 epilogue: up half of the accumulator
-    uint2 cbt[256 * CB_COPIES];   // sign-folded codebook, 16 copies
-    uint64_t full[STAGES], empty[STAGES], acc_full, acc_empty;
+    uint2 cbt[256 * CB_COPIES];     // sign-folded codebook, 16 copies
+    uint64_t full[STAGES], empty[STAGES], acc_full[2], acc_empty[2];
     uint32_t tmem_base;
     int failed;
 };
@@ -56,12 +56,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// byte offset of (row r, 8-byte column block j of the 64-element row) in a
-// 128B-swizzled K-major tile
-__device__ __forceinline__ uint32_t sw128_off(int r, int j) {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((j >> 1) ^ (r & 7))) << 4) + ((j & 1) << 3));
-}
-
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -99,8 +93,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// FC1 (FC1 = true): items = (chunk, 64-row tile of I); A rows 0-63 gate,
-// 64-127 up.  FC2: items = (chunk, 128-row tile of H).
+// A decoder thread's share of one K-block: one chunk (16 rows x 1 group =
+// 16 code bytes) and the 16 row scales of its tile.
+struct DecRegs {
+    uint4 c, s0, s1;
+};
+
+// FC1 (FC1 = true): items = (chunk, 128-row tile of I), A = gate and up tiles.
+// FC2: items = (chunk, 256-row tile of H), A = two 128-row down tiles.
 template <bool FC1>
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_umma_kernel(const __grid_constant__ CUtensorMap bmap, const SlotDesc* __restrict__ desc,
@@ -113,17 +113,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     Smem& S = *reinterpret_cast<Smem*>(dyn + ((1024u - (smem_u32(dyn) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int* err = header + HDR_ERR;
+    constexpr int NA = 2;                        // A tiles (and accumulators) per item
+    constexpr uint32_t ACC_COLS = NA * UM_N;     // TMEM columns of one accumulator set
+    constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
     const int K = FC1 ? H : I;
-    const int R = FC1 ? I : H;          // weight rows covered by the items of one chunk
-    const int ROWS = FC1 ? 64 : 128;    // weight rows per item (FC1: 64 gate + 64 up)
-    const int n_rt = R / ROWS;
-    const int KB = K / 128;             // scale blocks per row
+    const int R = FC1 ? I : H;
+    const int n_rt = R / (FC1 ? UM_M : 2 * UM_M);
+    const int KB = K / 128;  // scale blocks per row
     const int n_kblk = K / UM_K;
 
-    if ((smem_u32(&S.a[0][0]) & 1023) != 0) {
-        if (tid == 0) atomicExch(err, MOE_DEVERR_SMEM_LAYOUT);
-        return;
-    }
     for (int idx = tid; idx < 256 * CB_COPIES; idx += THREADS) {
         const int c = idx / CB_COPIES;
         const uint2 e = reinterpret_cast<const uint2*>(codebook)[c & 127];
@@ -135,8 +133,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&S.full[s]), 32 * DEC_WARPS + 1);
             mbar_init(smem_u32(&S.empty[s]), 1);
         }
-        mbar_init(smem_u32(&S.acc_full), 1);
-        mbar_init(smem_u32(&S.acc_empty), 32 * DEC_WARPS);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&S.acc_full[b]), 1);
+            mbar_init(smem_u32(&S.acc_empty[b]), 32 * EPI_WARPS);
+        }
         S.failed = 0;
     }
     if (warp == MMA_WARP) {  // allocate the accumulator columns (whole warp)
@@ -165,112 +165,87 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
 
     if (warp < DEC_WARPS) {
-        // ------------------------------------------------ decoder + epilogue
-        const int rtile = tid >> 4, g = tid & 15;  // 16-row tile of the item, group of the K-block
-        int it = 0, nitem = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++nitem) {
+        // ------------------------------------------------ decoders
+        // 256 threads = (A tile) x 8 row tiles x 16 groups, one chunk each.
+        // A tile byte offset of (row R, 8-byte block g) = 128 R + swizzled
+        // block; R & 7 is the chunk row's & 7 (row tiles start at multiples
+        // of 16), so the 8 possible block offsets are precomputed.
+        const int mat = tid >> 7;
+        const int rtile = (tid >> 4) & 7;
+        const int g = tid & 15;
+        uint32_t boff[8];
+#pragma unroll
+        for (int r7 = 0; r7 < 8; ++r7)
+            boff[r7] = 128u * (uint32_t)(rtile * 16) + ((((uint32_t)(g >> 1)) ^ (uint32_t)r7) << 4) + ((uint32_t)(g & 1) << 3);
+        // warp-collective bounded wait: lane 0 polls, the warp follows
+        auto warp_wait = [&](uint64_t* bar, uint32_t parity, int code) {
+            int ok = 0;
+            if (lane == 0) ok = wait(bar, parity, code) ? 1 : 0;
+            __syncwarp();
+            return __shfl_sync(0xffffffffu, ok, 0) != 0;
+        };
+        int it = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
             const Chunk ch = uchunks[item / n_rt];
             const int rt = item % n_rt;
             const SlotDesc& d = desc[ch.expert];
-            int m, rtm;
-            if (FC1) {
-                m = rtile >> 2;                 // 0 gate, 1 up
-                rtm = rt * 4 + (rtile & 3);
-            } else {
-                m = 2;
-                rtm = rt * 8 + rtile;
-            }
+            const int m = FC1 ? mat : 2;
+            const int rtm = FC1 ? rt * 8 + rtile : rt * 16 + mat * 8 + rtile;
             const uint8_t* codes = static_cast<const uint8_t*>(d.codes[m]) + (size_t)rtm * KB * 512;
             const uint16_t* scales = static_cast<const uint16_t*>(d.scales[m]) + (size_t)rtm * KB * 16;
-            const int rbase = FC1 ? (rtile >> 2) * 64 + (rtile & 3) * 16 : rtile * 16;
-            for (int kb64 = 0; kb64 < n_kblk; ++kb64, ++it) {
-                const int stage = it % STAGES, use = it / STAGES;
+            auto fetch = [&](int kb64, DecRegs& r) {
+                if (kb64 >= n_kblk) return;
                 const int kb = kb64 >> 1, half = kb64 & 1;
-                // fetch this thread's chunk (16 rows x 1 group) and its 16 row scales
-                const uint4 cw = ldg_stream(codes + (size_t)kb * 512 + 16 * (16 * half + g));
-                const uint4 s0 = ldg_stream(scales + (size_t)kb * 16);
-                const uint4 s1 = ldg_stream(scales + (size_t)kb * 16 + 8);
-                if (use > 0 && !wait(&S.empty[stage], (use - 1) & 1, MOE_DEVERR_WAIT_EMPTY)) continue;
-                const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-                const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
-                const uint32_t abase = smem_u32(&S.a[stage][0]);
+                r.c = ldg_stream(codes + (size_t)kb * 512 + 16 * (16 * half + g));
+                r.s0 = ldg_stream(scales + (size_t)kb * 16);
+                r.s1 = ldg_stream(scales + (size_t)kb * 16 + 8);
+            };
+            auto step = [&](const DecRegs& r) {
+                const int stage = it % STAGES, use = it / STAGES;
+                ++it;
+                if (use > 0 && !warp_wait(&S.empty[stage], (use - 1) & 1, MOE_DEVERR_WAIT_EMPTY)) return;
+                uint8_t* abase = &S.a[stage][mat][0];
+                const uint32_t cw[4] = {r.c.x, r.c.y, r.c.z, r.c.w};
+                const uint32_t sw[8] = {r.s0.x, r.s0.y, r.s0.z, r.s0.w, r.s1.x, r.s1.y, r.s1.z, r.s1.w};
+                // plain shared-memory accesses, so the 16 independent
+                // lookup -> scale -> store chains can overlap
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int c = (cws[j >> 2] >> (8 * (j & 3))) & 0xff;
+                    const uint32_t c = (cw[j >> 2] >> (8 * (j & 3))) & 0xffu;
                     const int row = (j >> 1) + 8 * (j & 1);  // byte 2i+h holds row i + 8h
-                    const uint32_t sh = (sw[row >> 1] >> (16 * (row & 1))) & 0xffffu;
-                    const __half2 s2 = __halves2half2(__ushort_as_half((unsigned short)sh),
-                                                      __ushort_as_half((unsigned short)sh));
+                    // the row's fp16 scale in both halves
+                    const uint32_t s2 = prmt(sw[row >> 1], 0u, (row & 1) ? 0x3232u : 0x1010u);
                     const uint2 e = S.cbt[c * CB_COPIES + (lane & 15)];
-                    __half2 w0 = __hmul2(*reinterpret_cast<const __half2*>(&e.x), s2);
-                    __half2 w1 = __hmul2(*reinterpret_cast<const __half2*>(&e.y), s2);
-                    const uint32_t off = sw128_off(rbase + row, g);
-                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(abase + off),
-                                 "r"(*reinterpret_cast<uint32_t*>(&w0)), "r"(*reinterpret_cast<uint32_t*>(&w1)));
+                    __half2 w0 = __hmul2(*reinterpret_cast<const __half2*>(&e.x), *reinterpret_cast<const __half2*>(&s2));
+                    __half2 w1 = __hmul2(*reinterpret_cast<const __half2*>(&e.y), *reinterpret_cast<const __half2*>(&s2));
+                    *reinterpret_cast<uint2*>(abase + boff[row & 7] + 128u * (uint32_t)row) =
+                        make_uint2(*reinterpret_cast<uint32_t*>(&w0), *reinterpret_cast<uint32_t*>(&w1));
                 }
                 fence_async_smem();
                 mbar_arrive(smem_u32(&S.full[stage]));
-            }
-            // epilogue: accumulator rows 32*warp + lane, token columns 0..127
-            if (!wait(&S.acc_full, nitem & 1, MOE_DEVERR_WAIT_FULL)) {
-                mbar_arrive(smem_u32(&S.acc_empty));
-                continue;
-            }
-            tc_fence_after();
-            const int row = warp * 32 + lane;
-            const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-            if (FC1) {
-                if (warp >= 2) {  // up rows: hand them to the gate-row threads
-#pragma unroll 1
-                    for (int c0 = 0; c0 < UM_N; c0 += 32) {
-                        float v[32];
-                        tmem_ld32(taddr + c0, v);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) S.xch[row - 64][c0 + i] = v[i];
-                    }
+            };
+            // codes are fetched four K-blocks ahead of their decode
+            DecRegs r0, r1, r2, r3;
+            fetch(0, r0);
+            fetch(1, r1);
+            fetch(2, r2);
+            fetch(3, r3);
+            for (int kb64 = 0; kb64 < n_kblk; kb64 += 4) {
+                step(r0);
+                fetch(kb64 + 4, r0);
+                if (kb64 + 1 < n_kblk) {
+                    step(r1);
+                    fetch(kb64 + 5, r1);
                 }
-                named_barrier(1, 32 * DEC_WARPS);
-                if (warp < 2) {
-                    const int irow = rt * 64 + row;
-#pragma unroll 1
-                    for (int c0 = 0; c0 < UM_N; c0 += 32) {
-                        float v[32];
-                        tmem_ld32(taddr + c0, v);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int tok = c0 + i;
-                            if (tok < ch.count) {
-                                const float gv = v[i], uv = S.xch[row][tok];
-                                const float a = gv / (1.0f + expf(-gv)) * uv;
-                                a16[(size_t)(ch.start + tok) * I + irow] = __half_as_ushort(__float2half_rn(a));
-                            }
-                        }
-                    }
+                if (kb64 + 2 < n_kblk) {
+                    step(r2);
+                    fetch(kb64 + 6, r2);
                 }
-                named_barrier(1, 32 * DEC_WARPS);
-            } else {
-                const int h = rt * 128 + row;
-#pragma unroll 1
-                for (int c0 = 0; c0 < UM_N; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(taddr + c0, v);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int tok = c0 + i;
-                        if (tok < ch.count) {
-                            const int spos = ch.start + tok;
-                            if (mode == MOE_PER_PAIR) {
-                                out[(size_t)spos * H + h] = v[i];
-                            } else {
-                                const int p = sorted_pair[spos];
-                                atomicAdd(out + (size_t)(p / k) * H + h, weights[p] * v[i]);
-                            }
-                        }
-                    }
+                if (kb64 + 3 < n_kblk) {
+                    step(r3);
+                    fetch(kb64 + 7, r3);
                 }
             }
-            tc_fence_before();
-            mbar_arrive(smem_u32(&S.acc_empty));
         }
     } else if (warp == TMA_WARP) {
         // ------------------------------------------------ activations (B)
@@ -287,29 +262,89 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
         }
-    } else {
+    } else if (warp == MMA_WARP) {
         // ------------------------------------------------ MMA issue
         if (lane == 0) {
             int it = 0, nitem = 0;
             for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++nitem) {
-                // the epilogue of the previous item must have read the accumulator
-                if (nitem > 0 && !wait(&S.acc_empty, (nitem - 1) & 1, MOE_DEVERR_WAIT_EMPTY)) break;
+                const int buf = nitem & 1;
+                // the epilogue of item nitem - 2 must have read this accumulator set
+                if (nitem >= 2 && !wait(&S.acc_empty[buf], ((nitem >> 1) - 1) & 1, MOE_DEVERR_WAIT_EMPTY)) break;
                 tc_fence_after();
+                const uint32_t d0 = tmem + (uint32_t)buf * ACC_COLS;
                 for (int kb64 = 0; kb64 < n_kblk; ++kb64, ++it) {
                     const int stage = it % STAGES, use = it / STAGES;
                     if (!wait(&S.full[stage], use & 1, MOE_DEVERR_WAIT_FULL)) break;
                     tc_fence_after();
-                    const uint64_t ad = sw128_desc(smem_u32(&S.a[stage][0]));
                     const uint64_t bd = sw128_desc(smem_u32(&S.b[stage][0]));
 #pragma unroll
-                    for (int j = 0; j < UM_K / 16; ++j)  // 32 bytes of K per step inside the swizzle row
-                        umma_f16(tmem, ad + 2 * j, bd + 2 * j, (kb64 > 0 || j > 0) ? 1u : 0u);
+                    for (int t = 0; t < NA; ++t) {
+                        const uint64_t ad = sw128_desc(smem_u32(&S.a[stage][t][0]));
+#pragma unroll
+                        for (int j = 0; j < UM_K / 16; ++j)  // 32 bytes of K per step inside the swizzle row
+                            umma_f16(d0 + t * UM_N, ad + 2 * j, bd + 2 * j, (kb64 > 0 || j > 0) ? 1u : 0u);
+                    }
                     umma_commit(smem_u32(&S.empty[stage]));
                 }
-                umma_commit(smem_u32(&S.acc_full));
+                umma_commit(smem_u32(&S.acc_full[buf]));
             }
-            // the last epilogue must finish reading before the columns are freed
-            if (nitem > 0) wait(&S.acc_empty, (nitem - 1) & 1, MOE_DEVERR_WAIT_EMPTY);
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter.. are this warp's
+        const int row = quarter * 32 + lane;
+        int nitem = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++nitem) {
+            const Chunk ch = uchunks[item / n_rt];
+            const int rt = item % n_rt;
+            const int buf = nitem & 1;
+            int ok = 0;
+            if (lane == 0) ok = wait(&S.acc_full[buf], (nitem >> 1) & 1, MOE_DEVERR_WAIT_FULL) ? 1 : 0;
+            __syncwarp();
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)buf * ACC_COLS;
+#pragma unroll 1
+            for (int c0 = 0; c0 < UM_N; c0 += 32) {
+                if (c0 >= ch.count) break;
+                float v[32];
+                tmem_ld32(taddr + c0, v);
+                if (FC1) {
+                    float u[32];
+                    tmem_ld32(taddr + UM_N + c0, u);
+                    const int irow = rt * UM_M + row;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int tok = c0 + q;
+                        if (tok < ch.count) {
+                            const float gv = v[q];
+                            a16[(size_t)(ch.start + tok) * I + irow] =
+                                __half_as_ushort(__float2half_rn(gv / (1.0f + expf(-gv)) * u[q]));
+                        }
+                    }
+                } else {
+#pragma unroll 1
+                    for (int t = 0; t < 2; ++t) {
+                        if (t == 1) tmem_ld32(taddr + UM_N + c0, v);
+                        const int h = rt * 2 * UM_M + t * UM_M + row;
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) {
+                            const int tok = c0 + q;
+                            if (tok < ch.count) {
+                                const int spos = ch.start + tok;
+                                if (mode == MOE_PER_PAIR) {
+                                    out[(size_t)spos * H + h] = v[q];
+                                } else {
+                                    const int p = sorted_pair[spos];
+                                    atomicAdd(out + (size_t)(p / k) * H + h, weights[p] * v[q]);
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&S.acc_empty[buf]));
         }
     }
     tc_fence_before();

@@ -52,7 +52,9 @@ unsigned grid_for(long n) {
 
 moe_status launch_vq2_pack(const uint8_t* codes, const uint16_t* scales, int rows, int K, uint8_t* pc,
                            uint16_t* ps, cudaStream_t s) {
+    count_launch();
     vq2_pack_codes<<<grid_for((long)rows * K / 4), 256, 0, s>>>(codes, rows, K, pc);
+    count_launch();
     vq2_pack_scales<<<grid_for((long)rows * K / 128), 256, 0, s>>>(scales, rows, K, ps);
     MOE_LAUNCH_CHECK("moe_vq2_pack: launch");
     return MOE_OK;
@@ -60,13 +62,16 @@ moe_status launch_vq2_pack(const uint8_t* codes, const uint16_t* scales, int row
 
 moe_status launch_fp4_pack(const uint8_t* codes, const uint8_t* scales, int rows, int K, uint8_t* pc,
                            uint8_t* ps, cudaStream_t s) {
+    count_launch();
     fp4_pack_codes<<<grid_for((long)rows * K / 2), 256, 0, s>>>(codes, rows, K, pc);
+    count_launch();
     fp4_pack_scales<<<grid_for((long)rows * K / 32), 256, 0, s>>>(scales, rows, K, ps);
     MOE_LAUNCH_CHECK("moe_fp4_pack: launch");
     return MOE_OK;
 }
 
 moe_status launch_slot_set(SlotDesc* table, int expert_id, SlotDesc d, cudaStream_t s) {
+    count_launch();
     slot_set_kernel<<<1, 1, 0, s>>>(table, expert_id, d);
     MOE_LAUNCH_CHECK("moe_slot_table_set: launch");
     return MOE_OK;

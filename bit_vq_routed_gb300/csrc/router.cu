@@ -18,73 +18,93 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
     }
 }
 
-// One warp computes NE experts' logits for one token.  Lane l owns the
-// 16-byte chunks c = l + 32m (inputs 8c..8c+7) and adds their products in
-// increasing input order; bf16 x bf16 products are exact in fp32, so the
-// explicit mul + add below equals an FMA.  Then a butterfly over the lanes.
-template <int NE>
-__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ x,
-                                                            const uint16_t* __restrict__ w,
-                                                            const float* __restrict__ bias,
-                                                            float* __restrict__ logits, int T, int H,
-                                                            int E) {
+// Large-batch router: a CTA computes a tile of 16 tokens x 32 experts; warp
+// (tg, eg) owns 4 tokens x 16 experts and lane l is the lane-slot l of every
+// one of those 64 dot products, so each lane adds exactly the products of the
+// inputs h with (h/8) mod 32 == l, in increasing h (the fixed order), then the
+// butterfly.  The 256-input slabs of activations and router weights both
+// sides of the tile need are staged in shared memory (cp.async, two buffers).
+constexpr int RT_T = 16, RT_E = 32, RT_SLAB = 256;
+
+__global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t* __restrict__ x,
+                                                                  const uint16_t* __restrict__ w,
+                                                                  const float* __restrict__ bias,
+                                                                  float* __restrict__ logits, int T, int H,
+                                                                  int E) {
+    __shared__ __align__(16) uint16_t xs[2][RT_T][RT_SLAB];
+    __shared__ __align__(16) uint16_t ws[2][RT_E][RT_SLAB];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E;
+    const int tg = warp >> 1, eg = warp & 1;  // 4 token groups x 2 expert groups
+    const int nslab = H / RT_SLAB;
+    auto issue = [&](int sl) {
+        const int buf = sl & 1;
+        // (RT_T + RT_E) rows x 32 16-byte chunks = 1536 chunks, 6 per thread
+        for (int c = tid; c < (RT_T + RT_E) * 32; c += 256) {
+            const int row = c >> 5, col = (c & 31) * 8;
+            const uint16_t* src;
+            uint32_t dst;
+            bool valid;
+            if (row < RT_T) {
+                valid = t0 + row < T;
+                src = x + (size_t)(valid ? t0 + row : 0) * H + sl * RT_SLAB + col;
+                dst = smem_u32(&xs[buf][row][col]);
+            } else {
+                valid = e0 + row - RT_T < E;
+                src = w + (size_t)(valid ? e0 + row - RT_T : 0) * H + sl * RT_SLAB + col;
+                dst = smem_u32(&ws[buf][row - RT_T][col]);
+            }
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                         : "memory");
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+    };
     pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const long warp = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int egroups = (E + NE - 1) / NE;
-    const long t = warp / egroups;
-    if (t >= T) return;
-    const int e0 = (int)(warp % egroups) * NE;
-    const int nch = H / 256;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    const uint4* wr[NE];
+    float acc[4][16];
 #pragma unroll
-    for (int q = 0; q < NE; ++q) {
-        int e = min(e0 + q, E - 1);
-        wr[q] = reinterpret_cast<const uint4*>(w + (size_t)e * H);
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 16; ++b) acc[a][b] = 0.0f;
+    issue(0);
+    for (int sl = 0; sl < nslab; ++sl) {
+        if (sl + 1 < nslab) {
+            issue(sl + 1);
+            asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+        }
+        __syncthreads();
+        const int buf = sl & 1;
+        float xf[4][8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) unpack_bf16x8(*reinterpret_cast<const uint4*>(&xs[buf][tg * 4 + a][8 * lane]), xf[a]);
+#pragma unroll
+        for (int b = 0; b < 16; ++b) {
+            float wf[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(&ws[buf][eg * 16 + b][8 * lane]), wf);
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[a][b] = __fadd_rn(acc[a][b], __fmul_rn(xf[a][i], wf[i]));
+        }
+        __syncthreads();
     }
-    float acc[NE];
 #pragma unroll
-    for (int q = 0; q < NE; ++q) acc[q] = 0.0f;
-    constexpr int U = 4;  // chunks fetched per round trip
-    for (int m0 = 0; m0 < nch; m0 += U) {
-        uint4 xv[U], wv[U][NE];
+    for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (m0 + u < nch) {
-                xv[u] = __ldg(xr + lane + 32 * (m0 + u));
+        for (int b = 0; b < 16; ++b)
 #pragma unroll
-                for (int q = 0; q < NE; ++q) wv[u][q] = __ldg(wr[q] + lane + 32 * (m0 + u));
+            for (int off = 16; off >= 1; off >>= 1) acc[a][b] = __fadd_rn(acc[a][b], __shfl_xor_sync(FULL, acc[a][b], off));
+    // lane l writes entry (a, b) = (l >> 4 .. , l & 15): 2 passes of 32
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 16; ++b) {
+            if (lane == ((a & 1) * 16 + b)) {
+                const int t = t0 + tg * 4 + a, e = e0 + eg * 16 + b;
+                if (t < T && e < E) logits[(size_t)t * E + e] = bias ? __fadd_rn(acc[a][b], bias[e]) : acc[a][b];
             }
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (m0 + u < nch) {
-                float xf[8];
-                unpack_bf16x8(xv[u], xf);
-#pragma unroll
-                for (int q = 0; q < NE; ++q) {
-                    float wf[8];
-                    unpack_bf16x8(wv[u][q], wf);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[q] = __fadd_rn(acc[q], __fmul_rn(xf[i], wf[i]));
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < NE; ++q) {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) acc[q] = __fadd_rn(acc[q], __shfl_xor_sync(FULL, acc[q], off));
-    }
-    if (lane < NE) {
-        float v = acc[0];
-#pragma unroll
-        for (int q = 1; q < NE; ++q)
-            if (lane == q) v = acc[q];
-        int e = e0 + lane;
-        if (e < E) logits[(size_t)t * E + e] = bias ? __fadd_rn(v, bias[e]) : v;
-    }
     pdl_launch_dependents();
 }
 
@@ -95,7 +115,7 @@ __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
 // Small-batch router: one CTA of 8 warps per (token, 8 experts); the token's
 // activations sit in shared memory and each lane first loads all of its
 // router-weight chunks, so a warp needs one memory round trip.  Same fixed
-// summation order as router_logits_kernel.
+// summation order as router_logits_tiled_kernel (the order moe_vq2.h states).
 __global__ void __launch_bounds__(256) router_logits_small_kernel(const uint16_t* __restrict__ x,
                                                                   const uint16_t* __restrict__ w,
                                                                   const float* __restrict__ bias,
@@ -105,19 +125,26 @@ __global__ void __launch_bounds__(256) router_logits_small_kernel(const uint16_t
     const int t = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * 8 + warp;
     const int nch = H / 8;
+    const int per = H / 256;  // chunks per lane
+    constexpr int U = 16;
+    // the router weights do not depend on earlier kernels: fetch the first
+    // (for H <= 4096 the only) batch of them before waiting on the predecessor
+    const uint4* wr = reinterpret_cast<const uint4*>(w + (size_t)min(e, E - 1) * H);
+    uint4 wv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (u < per) wv[u] = __ldg(wr + lane + 32 * u);
     pdl_wait();
     for (int i = threadIdx.x; i < nch; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(x + (size_t)t * H)[i];
     __syncthreads();
     if (e >= E) return;
-    const uint4* wr = reinterpret_cast<const uint4*>(w + (size_t)e * H);
-    const int per = H / 256;  // chunks per lane
     float acc = 0.0f;
-    constexpr int U = 16;
     for (int m0 = 0; m0 < per; m0 += U) {
-        uint4 wv[U];
+        if (m0 > 0) {
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (m0 + u < per) wv[u] = __ldg(wr + lane + 32 * (m0 + u));
+            for (int u = 0; u < U; ++u)
+                if (m0 + u < per) wv[u] = __ldg(wr + lane + 32 * (m0 + u));
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (m0 + u < per) {
@@ -228,10 +255,8 @@ moe_status launch_router_logits(const uint16_t* x, const uint16_t* w, const floa
                                    H, E);
         if (e != cudaSuccess) return cuda_status(e, "moe_router_logits: launch");
     } else {
-        long warps = (long)T * ((E + 3) / 4);
-        long blocks = (warps * 32 + threads - 1) / threads;
-        cudaError_t e = launch_pdl(router_logits_kernel<4>, dim3((unsigned)blocks), dim3(threads), 0, s, x, w, bias,
-                                   logits, T, H, E);
+        dim3 grid((unsigned)((T + RT_T - 1) / RT_T), (unsigned)((E + RT_E - 1) / RT_E));
+        cudaError_t e = launch_pdl(router_logits_tiled_kernel, grid, dim3(threads), 0, s, x, w, bias, logits, T, H, E);
         if (e != cudaSuccess) return cuda_status(e, "moe_router_logits: launch");
     }
     MOE_LAUNCH_CHECK("moe_router_logits: launch");

@@ -237,6 +237,12 @@ moe_status moe_combine(const float* ypair, const int32_t* pair_to_sorted, const 
                        const uint8_t* pair_status, int T, int k, int H, float* out_f32,
                        uint16_t* out_bf16, cudaStream_t stream);
 
+/* Number of kernel launches the library has issued on the host since it was
+ * loaded, over all devices and threads (atomic).  A launch made while a
+ * stream is being captured counts once, as the one kernel node it adds to
+ * the graph; replays of the graph are not counted.  Never fails. */
+uint64_t moe_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

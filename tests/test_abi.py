@@ -97,3 +97,13 @@ def test_workspace_sizes(lib):
     # decode batch 32 at top-8 fits the scratch-free variant's fixed scratch
     assert lib.moe_vq2_expert_ffn_workspace_size(32, 8, 256, 4096, 2048) <= bv.MOE_NOALLOC_SCRATCH_BYTES
     assert lib.moe_permute_workspace_size(4096, 8, 256) == 0
+
+
+def test_launch_count_ignores_rejected_calls(lib):
+    # calls that fail their host-side checks enqueue no kernel
+    P = ctypes.c_void_p
+    before = bv.moe_launch_count()
+    assert lib.moe_router_logits(P(16), P(16), None, P(16), 1, 100, 8, None) == bv.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route_topk(P(16), 4, 8, 0, 1, P(16), P(16), None) == bv.MOE_ERR_INVALID_ARG
+    assert lib.moe_router_logits(None, None, None, None, 0, 256, 8, None) == bv.MOE_OK
+    assert bv.moe_launch_count() == before

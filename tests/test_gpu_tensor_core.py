@@ -1,5 +1,5 @@
 """GPU parity of the tcgen05 (tensor-core) path: experts that receive at
-least 64 tokens in one call run FC1 and FC2 as tcgen05.mma contractions over
+least 32 tokens in one call run FC1 and FC2 as tcgen05.mma contractions over
 fp16 weight tiles decoded into shared memory.  Shapes cover ragged token
 chunks (counts not a multiple of 128), several weight-row tiles, mixed FP4
 experts (which stay on the other path) and fused scatter mode."""
@@ -30,7 +30,7 @@ def test_tensor_core_experts_match_oracle(torch, H, I, T, E, k, fp4):
     r = O.moe_layer(layer, x)
     assert_routing_exact(g, r)
     counts = np.diff(g["offsets"])
-    assert (counts[layer.formats == ms.FMT_VQ2] >= 64).any()  # the tensor-core path is exercised
+    assert (counts[layer.formats == ms.FMT_VQ2] >= 32).any()  # the tensor-core path is exercised
     assert_close(g["out"], r["out"], f"H={H} I={I} T={T}")
     assert device_error_word(dev) == 0
 
