@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       float* __restrict__ out32,
                                                       uint16_t* __restrict__ out16) {
     pdl_wait();
+    pdl_launch_dependents();  // dependents may start their prologues now
     const int t = blockIdx.y, lane = threadIdx.x & 31;
     const int h = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
     int row = -1;
@@ -49,7 +50,6 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
             *reinterpret_cast<uint2*>(out16 + (size_t)t * H + h) = make_uint2(lo, hi);
         }
     }
-    pdl_launch_dependents();
 }
 
 }  // namespace

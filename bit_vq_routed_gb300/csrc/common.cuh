@@ -194,9 +194,14 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
 #define MOE_DEVERR_SMEM_LAYOUT 3
 
 // Launch with programmatic dependent launch allowed: the kernel may start
-// while its predecessor on the stream finishes; every kernel of the library
-// calls pdl_wait() before it touches memory a predecessor may write or read,
-// so only the prologues (shared-memory set-up, constant weights) overlap.
+// while its predecessor on the stream still runs.  Every kernel of the library
+// calls pdl_wait() before it touches memory an earlier kernel may write or
+// read, and pdl_launch_dependents() right after it.  So when a kernel starts,
+// its predecessor has at least passed its own wait, i.e. everything two
+// launches back is complete; the code before the wait (shared-memory set-up,
+// constant weights, and reads of results two launches back) overlaps the
+// predecessor's run.
+//
 // Host-side count of kernel launches the library has issued (a launch made
 // inside a stream capture counts once: it becomes one graph node).
 void count_launch();

@@ -11,24 +11,27 @@ namespace moe {
 namespace {
 
 // ---------------------------------------------------------------- schedule
-// Exclusive scan over the 1024 threads of the block; returns the block total
-// through *total.
-__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+// Scan of a 64-bit value over the 1024 threads of the block (up to three
+// counts packed in 21-bit fields); returns this thread's exclusive prefix and
+// the block total through *total.
+__device__ unsigned long long block_scan64(unsigned long long v, unsigned long long* warp_tot,
+                                           unsigned long long* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = v;
+    unsigned long long incl = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        int o = __shfl_up_sync(0xffffffffu, incl, off);
+        const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += o;
     }
-    __syncthreads();
+    __syncthreads();  // an earlier scan's readers are done with warp_tot
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int wv = warp_tot[lane], wi = wv;
+        const unsigned long long wv = warp_tot[lane];
+        unsigned long long wi = wv;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            int o = __shfl_up_sync(0xffffffffu, wi, off);
+            const unsigned long long o = __shfl_up_sync(0xffffffffu, wi, off);
             if (lane >= off) wi += o;
         }
         warp_tot[lane] = wi - wv;
@@ -39,81 +42,160 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
     return incl - v + warp_tot[warp];
 }
 
+constexpr int SP_SMEM = 4096;  // sorted_pair entries staged in shared memory
+
 // One CTA of 1024 threads.  Expert e with m_e pairs, if resident:
 //   VQ2 with m_e == 1 (and use_lut) -> one activation-table pair;
-//   otherwise -> ceil(m_e / NT) tensor-core chunks.
+//   VQ2 with m_e >= UMMA_MIN (and use_umma) -> ceil(m_e / UMMA_NT) tcgen05 chunks;
+//   otherwise -> ceil(m_e / MMA_NT) mma.sync chunks.
 // Table pairs are listed sorted by (token, expert) and grouped by token, so
 // the experts of one token share each activation table.  pair_status of every
 // pair from the residency of its expert; the header's error word is cleared.
+// All global inputs are read in one round trip at the start.
 __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restrict__ desc, int E,
                                                         const int32_t* __restrict__ offsets,
                                                         const int32_t* __restrict__ sorted_pair, int P, int k,
                                                         uint8_t* __restrict__ status, int* __restrict__ header,
-                                                        Chunk* __restrict__ chunks, int32_t* __restrict__ lut_s,
-                                                        int32_t* __restrict__ lut_e, int32_t* __restrict__ lut_grp,
+                                                        Chunk* __restrict__ chunks, LutRec* __restrict__ recs,
                                                         int32_t* __restrict__ grp_start, int use_lut,
-                                                        Chunk* __restrict__ uchunks, int use_umma) {
-    __shared__ int warp_tot[33];
+                                                        Chunk* __restrict__ uchunks, int use_umma, int H, int I,
+                                                        int C, int2* __restrict__ fc1_range) {
+    __shared__ unsigned long long warp_tot[33];
     __shared__ int s_off[1025];
-    __shared__ int s_tok[1024];  // token of each table pair, by expert (INT_MAX otherwise)
+    __shared__ __align__(16) int s_tok[1024];  // token of each table pair, by expert (INT_MAX otherwise)
     __shared__ int s_sorted_tok[1024];
+    __shared__ int s_gs[1025];
     __shared__ uint8_t s_res[1024];
-    __shared__ uint8_t s_fmt[1024];
+    __shared__ int s_sp[SP_SMEM];
+    __shared__ int s_lut_e[1024];  // table pairs in expert order
+    __shared__ int s_rank[1024];   // (token, expert) rank of each table pair, by expert
     pdl_wait();
+    pdl_launch_dependents();  // dependents may start their prologues now
     const int tid = threadIdx.x;
+    // the one round trip: offsets, this thread's slot descriptor, sorted_pair
     for (int i = tid; i <= E; i += 1024) s_off[i] = offsets[i];
-    if (tid < E) {
-        s_res[tid] = (uint8_t)(desc[tid].resident != 0);
-        s_fmt[tid] = (uint8_t)desc[tid].format;
-    }
+    SlotDesc d;
+    d.format = 0;
+    d.resident = 0;
+    if (tid < E) d = desc[tid];
+    const int nsp = min(P, SP_SMEM);
+    for (int i = tid; i < nsp; i += 1024) s_sp[i] = sorted_pair[i];
+    if (tid < E) s_res[tid] = (uint8_t)(d.resident != 0);
     __syncthreads();
+    auto sp_at = [&](int i) { return i < SP_SMEM ? s_sp[i] : sorted_pair[i]; };
+
     const int m = tid < E ? s_off[tid + 1] - s_off[tid] : 0;
-    const bool res = tid < E && s_res[tid] && m > 0;
-    const bool lut = res && use_lut && m == 1 && s_fmt[tid] == MOE_FMT_VQ2;
-    const bool um = res && use_umma && m >= UMMA_MIN && s_fmt[tid] == MOE_FMT_VQ2;
+    const bool res = tid < E && d.resident != 0 && m > 0;
+    const bool lut = res && use_lut && m == 1 && d.format == MOE_FMT_VQ2;
+    const bool um = res && use_umma && m >= UMMA_MIN && d.format == MOE_FMT_VQ2;
     const int n = (res && !lut && !um) ? (m + MMA_NT - 1) / MMA_NT : 0;
     const int nu = um ? (m + UMMA_NT - 1) / UMMA_NT : 0;
-    const int tok = lut ? sorted_pair[s_off[tid]] / k : 0x7fffffff;
+    const int tok = lut ? sp_at(s_off[tid]) / k : 0x7fffffff;
     s_tok[tid] = tok;
-    int n_chunks, n_lut;
-    const int cbase = block_exclusive_scan(n, warp_tot, &n_chunks);
+    // one scan for the three counts (fields of 21 bits: n, nu, table pair)
+    unsigned long long tot;
+    const unsigned long long ex =
+        block_scan64((unsigned long long)n | ((unsigned long long)nu << 21) | ((unsigned long long)lut << 42),
+                     warp_tot, &tot);  // (its barriers also publish s_tok)
+    const int cbase = (int)(ex & 0x1fffff), ubase = (int)((ex >> 21) & 0x1fffff);
+    const int n_chunks = (int)(tot & 0x1fffff), n_umma = (int)((tot >> 21) & 0x1fffff), n_lut = (int)(tot >> 42);
     for (int c = 0; c < n; ++c) {
         Chunk ch;
         ch.expert = tid;
         ch.start = s_off[tid] + c * MMA_NT;
         ch.count = min(MMA_NT, m - c * MMA_NT);
-        ch.fmt = s_fmt[tid];
+        ch.fmt = d.format;
         chunks[cbase + c] = ch;
     }
-    int n_umma;
-    const int ubase = block_exclusive_scan(nu, warp_tot, &n_umma);
     for (int c = 0; c < nu; ++c) {
         Chunk ch;
         ch.expert = tid;
         ch.start = s_off[tid] + c * UMMA_NT;
         ch.count = min(UMMA_NT, m - c * UMMA_NT);
-        ch.fmt = s_fmt[tid];
+        ch.fmt = d.format;
         uchunks[ubase + c] = ch;
     }
-    block_exclusive_scan(lut ? 1 : 0, warp_tot, &n_lut);  // (its barriers also publish s_tok)
-    if (lut) {
-        // rank by (token, expert id): a stable sort of the table pairs by token
-        int rank = 0;
-        for (int e2 = 0; e2 < E; ++e2) {
-            const int t2 = s_tok[e2];
-            rank += (t2 < tok) || (t2 == tok && e2 < tid);
+    // rank of each table pair in (token, expert) order, one warp per pair:
+    // the pairs with a smaller token, or the same token and a smaller expert
+    if (lut) s_lut_e[(int)(ex >> 42)] = tid;
+    __syncthreads();
+    {
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int i = warp; i < n_lut; i += 32) {
+            const int e = s_lut_e[i], te = s_tok[e];
+            int c = 0;
+            for (int e2 = lane; e2 < E; e2 += 32) c += (s_tok[e2] < te) || (s_tok[e2] == te && e2 < e);
+            c = __reduce_add_sync(0xffffffffu, c);
+            if (lane == 0) {
+                s_rank[e] = c;
+                s_sorted_tok[c] = te;
+            }
         }
-        lut_s[rank] = s_off[tid];
-        lut_e[rank] = tid;
-        s_sorted_tok[rank] = tok;
     }
     __syncthreads();
+    const int rank = lut ? s_rank[tid] : 0;
     const bool first = tid < n_lut && (tid == 0 || s_sorted_tok[tid] != s_sorted_tok[tid - 1]);
-    int n_groups;
-    const int gid = block_exclusive_scan(first ? 1 : 0, warp_tot, &n_groups) + (first ? 1 : 0) - 1;
-    if (tid < n_lut) {
-        lut_grp[tid] = gid;
-        if (first) grp_start[gid] = tid;
+    unsigned long long n_groups64;
+    const int gid = (int)block_scan64(first ? 1ull : 0ull, warp_tot, &n_groups64);
+    const int n_groups = (int)n_groups64;
+    if (first) {
+        grp_start[gid] = tid;
+        s_gs[gid] = tid;
+    }
+    if (tid == 0) s_gs[n_groups] = n_lut;
+    __syncthreads();
+    if (lut) {
+        // the expert's own thread writes its record at its rank
+        LutRec r;
+        for (int mtx = 0; mtx < 3; ++mtx) {
+            r.codes[mtx] = d.codes[mtx];
+            r.scales[mtx] = d.scales[mtx];
+        }
+        r.sorted = s_off[tid];
+        r.token = tok;
+        // the token group of sorted table pair 'rank': the last group start <= rank
+        int lo = 0, hi = n_groups;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_gs[mid] <= rank) lo = mid; else hi = mid;
+        }
+        r.gs = s_gs[lo];
+        r.gc = s_gs[lo + 1] - r.gs;
+        recs[rank] = r;
+    }
+    // FC1 unit ranges of the C table-kernel CTAs (jobs = (token group, K-range))
+    {
+        const int KR1 = lut_jobs(H), RT1 = 2 * I / 16;
+        const int J = n_groups * KR1, U = n_lut * KR1 * RT1;
+        auto start = [&](int j) {
+            const int g = j / KR1, kr = j - g * KR1;
+            const int gs = s_gs[g], gc = g < n_groups ? s_gs[g + 1] - gs : 0;
+            return (gs * KR1 + kr * gc) * RT1;
+        };
+        int* s_a = s_lut_e;  // (free after the ranking; C + 1 <= 1024 entries)
+        __syncthreads();
+        bool ok = J > 0 && J <= C;
+        if (ok && tid <= J) s_a[tid] = tid == J ? C : lut_cta_of(start(tid), C, U);
+        __syncthreads();
+        ok = __syncthreads_and(!ok || tid >= J || s_a[tid + 1] > s_a[tid]) && ok;
+        if (tid < C) {
+            int u0, u1;
+            if (ok) {
+                int lo = 0, hi = J;  // the job j with s_a[j] <= tid < s_a[j+1]
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (s_a[mid] <= tid) lo = mid; else hi = mid;
+                }
+                const int st0 = start(lo), st1 = lo + 1 < J ? start(lo + 1) : U;
+                const int n = s_a[lo + 1] - s_a[lo], r = tid - s_a[lo];
+                u0 = st0 + (int)((long long)(st1 - st0) * r / n);
+                u1 = st0 + (int)((long long)(st1 - st0) * (r + 1) / n);
+            } else {
+                u0 = (int)((long long)U * tid / C);
+                u1 = (int)((long long)U * (tid + 1) / C);
+            }
+            fc1_range[tid] = make_int2(u0, u1);
+        }
     }
     if (tid == 0) {
         grp_start[n_groups] = n_lut;
@@ -123,15 +205,14 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
         header[HDR_NGROUPS] = n_groups;
         header[HDR_NUMMA] = n_umma;
     }
-    for (int s = tid; s < P; s += 1024) {
-        int lo = 0, hi = E;  // find e with off[e] <= s < off[e+1]
+    for (int s2 = tid; s2 < P; s2 += 1024) {
+        int lo = 0, hi = E;  // find e with off[e] <= s2 < off[e+1]
         while (hi - lo > 1) {
-            int mid = (lo + hi) >> 1;
-            if (s_off[mid] <= s) lo = mid; else hi = mid;
+            const int mid = (lo + hi) >> 1;
+            if (s_off[mid] <= s2) lo = mid; else hi = mid;
         }
-        status[sorted_pair[s]] = s_res[lo];
+        status[sp_at(s2)] = s_res[lo];
     }
-    pdl_launch_dependents();
 }
 
 }  // namespace
@@ -144,6 +225,10 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     (void)ws_bytes;
     const int E = t->E, H = t->H, I = t->I;
     const int P = T * k;
+    if (num_sms() >= MAX_LUT_CTAS) {
+        set_error("moe_vq2_expert_ffn: %d SMs above the supported %d", num_sms(), MAX_LUT_CTAS - 1);
+        return MOE_ERR_UNSUPPORTED;
+    }
     if (k > 32) {  // the experts of one token are handled as one group of at most 32
         set_error("moe_vq2_expert_ffn: k=%d above 32", k);
         return MOE_ERR_UNSUPPORTED;
@@ -152,9 +237,7 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     char* w = static_cast<char*>(ws);
     int* header = reinterpret_cast<int*>(w);
     Chunk* chunks = reinterpret_cast<Chunk*>(w + L.chunks_off);
-    int32_t* lut_s = reinterpret_cast<int32_t*>(w + L.lut_s_off);
-    int32_t* lut_e = reinterpret_cast<int32_t*>(w + L.lut_e_off);
-    int32_t* lut_grp = reinterpret_cast<int32_t*>(w + L.lut_grp_off);
+    LutRec* recs = reinterpret_cast<LutRec*>(w + L.rec_off);
     int32_t* grp_start = reinterpret_cast<int32_t*>(w + L.grp_start_off);
     Chunk* uchunks = reinterpret_cast<Chunk*>(w + L.uchunks_off);
     uint16_t* x16s = reinterpret_cast<uint16_t*>(w + L.x16s_off);
@@ -165,19 +248,19 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     const bool mma = T > 1 || t->n_fp4 > 0 || !use_lut;
 
     cudaError_t e = launch_pdl(schedule_kernel, dim3(1), dim3(1024), 0, s, (const SlotDesc*)t->d_desc, E, offsets,
-                               sorted_pair, P, k, status, header, chunks, lut_s, lut_e, lut_grp, grp_start, use_lut,
-                               uchunks, use_umma);
+                               sorted_pair, P, k, status, header, chunks, recs, grp_start, use_lut,
+                               uchunks, use_umma, H, I, num_sms(), reinterpret_cast<int2*>(w + L.range_off));
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule launch");
     moe_status st;
     if ((mma || use_umma) && (st = launch_gather_f16(x, sorted_pair, k, H, P, x16s, s)) != MOE_OK) return st;
-    if (use_lut && (st = launch_lut_fc(true, t, x, sorted_pair, k, w, L, s)) != MOE_OK) return st;
+    if (use_lut && (st = launch_lut_fc(true, t, x, sorted_pair, weights, k, mode, out, w, L, s)) != MOE_OK)
+        return st;
     if (mma && (st = launch_mma_fc(true, t, sorted_pair, weights, k, mode, out, w, L, s)) != MOE_OK) return st;
     if (use_umma && (st = launch_umma(true, t, sorted_pair, weights, k, P, mode, out, w, L, s)) != MOE_OK) return st;
-    if (use_lut && (st = launch_lut_fc(false, t, x, sorted_pair, k, w, L, s)) != MOE_OK) return st;
+    if (use_lut && (st = launch_lut_fc(false, t, x, sorted_pair, weights, k, mode, out, w, L, s)) != MOE_OK)
+        return st;
     if (mma && (st = launch_mma_fc(false, t, sorted_pair, weights, k, mode, out, w, L, s)) != MOE_OK) return st;
     if (use_umma && (st = launch_umma(false, t, sorted_pair, weights, k, P, mode, out, w, L, s)) != MOE_OK) return st;
-    if (use_lut && (st = launch_lut_finish(t, sorted_pair, weights, k, mode, out, w, L, L.max_lut, s)) != MOE_OK)
-        return st;
     return MOE_OK;
 }
 

@@ -2,32 +2,48 @@
 // and the schedule records.
 #pragma once
 
+#include <cstddef>
+
 #include "common.cuh"
 
 namespace moe {
 
 constexpr int MMA_NT = 32;     // tokens per mma.sync chunk (four n8 MMA tiles)
-constexpr int LUT_KB = 4;      // scale blocks (x 128 inputs) per activation-table job
+constexpr int LUT_KB = 8;      // scale blocks (x 128 inputs) per activation-table K-range
 constexpr int UMMA_MIN = 32;   // tokens from which an expert takes the tcgen05 path
 constexpr int UMMA_NT = 128;   // tokens per tcgen05 chunk
+constexpr int MAX_LUT_CTAS = 1024;  // grid of the activation-table kernels (one CTA per SM) at most
 
 // A run of sorted positions of one expert (tensor-core paths).
 struct Chunk {
     int32_t expert, start, count, fmt;
 };
 
+// One activation-table pair: its expert's code and scale buffers, its sorted
+// position and token, and its token group (first table pair, pair count).
+struct __align__(16) LutRec {
+    const void* codes[3];
+    const void* scales[3];
+    int32_t sorted, token, gs, gc;
+};
+static_assert(sizeof(LutRec) == 64 && offsetof(LutRec, codes) == 0 && offsetof(LutRec, scales) == 24,
+              "table pair record layout");
+
 // Header words at the start of the workspace.
 enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NUMMA = 4 };
 
 // Activation-table pairs (single-token VQ2 experts) are listed sorted by
-// token: lut_s / lut_e (sorted position, expert), lut_grp (token group of
-// each), grp_start (first pair of each token group, then n_lut).
+// (token, expert) in lut_rec, grouped by token: grp_start holds the first
+// pair of each token group, then n_lut.  p1 / p2
+// hold their FC1 / FC2 K-range partial sums, lut_cnt one arrival counter per
+// (table pair, FC2 row tile of 16 outputs); range holds each FC1 CTA's unit
+// range, computed by the schedule.
 // Experts with at least UMMA_MIN pairs (possible once T >= UMMA_MIN) take
 // the tcgen05 path (uchunks: chunks of <= UMMA_NT sorted positions); the
 // tensor-core paths read x16s (fp16 activations gathered by sorted position)
 // and a16 (fp16 silu(g)*u by sorted position).
 struct WsLayout {
-    size_t chunks_off, lut_s_off, lut_e_off, lut_grp_off, grp_start_off, p1_off, p2_off;
+    size_t chunks_off, rec_off, grp_start_off, p1_off, p2_off, cnt_off, range_off;
     size_t uchunks_off, x16s_off, a16_off, total;
     int max_chunks, max_lut, max_uchunks;
 };
@@ -38,6 +54,13 @@ __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; 
 // K-ranges of the activation-table path for an input length K.
 __host__ __device__ inline int lut_jobs(int K) { return ceil_div(K / 128, LUT_KB); }
 
+// Units [u0, u1) of CTA i of C for jobs j = 0..J-1 covering the units
+// [start(j), start(j+1)), start(J) = U, where a0(j) = floor(C start(j) / U).
+// With J <= C and every a0(j+1) > a0(j), job j takes the CTAs a0(j) ..
+// a0(j+1) - 1, each a contiguous share of it (no CTA builds two tables);
+// otherwise CTA i takes [U i / C, U (i+1) / C).
+__host__ __device__ inline int lut_cta_of(long long start, int C, int U) { return (int)((long long)C * start / U); }
+
 __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I) {
     WsLayout L;
     long long P = (long long)T * k;
@@ -46,18 +69,18 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I)
     size_t o = 256;
     L.chunks_off = o;
     o = ws_align(o + sizeof(Chunk) * (size_t)L.max_chunks);
-    L.lut_s_off = o;
-    o = ws_align(o + sizeof(int32_t) * (size_t)L.max_lut);
-    L.lut_e_off = o;
-    o = ws_align(o + sizeof(int32_t) * (size_t)L.max_lut);
-    L.lut_grp_off = o;
-    o = ws_align(o + sizeof(int32_t) * (size_t)L.max_lut);
+    L.rec_off = o;
+    o = ws_align(o + sizeof(LutRec) * (size_t)L.max_lut);
     L.grp_start_off = o;
     o = ws_align(o + sizeof(int32_t) * ((size_t)L.max_lut + 1));
     L.p1_off = o;
     o = ws_align(o + sizeof(float) * (size_t)L.max_lut * lut_jobs(H) * 2 * I);
     L.p2_off = o;
     o = ws_align(o + sizeof(float) * (size_t)L.max_lut * lut_jobs(I) * H);
+    L.cnt_off = o;
+    o = ws_align(o + sizeof(int32_t) * (size_t)L.max_lut * (H / 16));
+    L.range_off = o;
+    o = ws_align(o + sizeof(int2) * (size_t)MAX_LUT_CTAS);
     const bool umma = T >= UMMA_MIN;
     L.max_uchunks = umma ? (int)(P / UMMA_NT + E) : 0;
     L.uchunks_off = o;
@@ -71,14 +94,12 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I)
 }
 
 moe_status launch_lut_fc(bool fc1, const SlotTableHost* t, const uint16_t* x, const int32_t* sorted_pair,
-                         int k, char* ws, const WsLayout& L, cudaStream_t s);
+                         const float* weights, int k, int mode, float* out, char* ws, const WsLayout& L,
+                         cudaStream_t s);
 moe_status launch_gather_f16(const uint16_t* x, const int32_t* sorted_pair, int k, int H, int P, uint16_t* x16s,
                              cudaStream_t s);
 moe_status launch_umma(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
                        int P, int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s);
 moe_status launch_mma_fc(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
                          int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s);
-moe_status launch_lut_finish(const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
-                             int mode, float* out, char* ws, const WsLayout& L, int max_lut, cudaStream_t s);
-
 }  // namespace moe

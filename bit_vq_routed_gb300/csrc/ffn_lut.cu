@@ -2,64 +2,136 @@
 // single token in this call (every expert at decode batch 1, most of them at
 // small batches).
 //
-// For one token, every code byte c of group G contributes
-//     scale[r, G/32] * dot(sign(c) * codebook[c & 127], x[4G .. 4G+3])
-// and the dot product depends only on (c, G), not on the row.  So a CTA first
-// builds, in shared memory, the table L[c][G] of those 256 x 128 values for a
-// K-range of 512 inputs (128 KB of fp32, the negated half included so the sign
-// costs nothing), then streams the code tiles of many rows through it: one
-// 4-byte table read per code byte instead of an 8-byte codebook read plus four
-// multiply-adds.  Lanes own groups (8 lanes per 128-input scale block, 4 groups
-// each), so at every table read the 32 lanes hit 32 distinct banks.  A lane's
-// 4 values of one row share a scale and are summed before one FMA; the 16 row
-// sums of a tile are reduced across the warp by a reduce-scatter.  K-range
-// partial sums go to the workspace (deterministic, no atomics) and are added
-// in a fixed order by the consumer: FC2's table build (which also applies
-// silu(g) * u) and the finishing kernel.
+// For one token, every code byte c of group G (inputs 4G .. 4G+3) adds
+//     scale[r, G/32] * sign(c) * dot(codebook[c & 127], x[4G .. 4G+3])
+// to output row r, and the signed dot product depends on (c, G) only.  A CTA
+// first builds the table L[c][G] of those values for a K-range of 1024 inputs
+// (256 codes x 256 groups in fp16, 128 KB; the negated half is stored too, so
+// the sign costs nothing), then streams the code tiles of many rows through
+// it: per code byte one byte permute (the table address), one 2-byte shared
+// load and one mixed-precision add of the fp16 entry into an fp32 sum.
 //
-// Each warp streams its units' code and scale tiles straight into registers
-// with 16-byte loads, fetching two units ahead of the one it computes (12
-// warps per SM keep about 80 KB in flight).
+// Lanes own groups: lane l = 4b + m takes, in scale block b of the K-range,
+// the 8 groups m, m+4, ..., m+28 (one 16-byte load each, so each load
+// instruction of the warp reads whole 64-byte runs), and its 8 values of a
+// row share one scale.  The table puts every entry a lane reads in bank l,
+// whatever the code, so the 32 table reads of a warp never conflict, and the
+// group slot becomes the load's immediate offset.  The 16 row sums of a tile
+// are reduced across the warp by a reduce-scatter.
+//
+// K-range partial sums go to the workspace: FC2's table build adds FC1's
+// partials in a fixed order and applies silu(g) * u; of FC2's partials, the
+// warp that completes a row tile last (one counter per row tile) adds them in
+// K-range order and writes y, so every result is independent of timing.
+//
+// Code tiles are streamed by the copy engine (bulk copies, one per 512-byte
+// tile) into two shared-memory slots per warp, so the code stream never sits
+// in the load/store queue in front of the table reads; a warp copies a slot
+// to registers, hands the slot to the next copy and computes from registers,
+// with two units in flight.  Waits on the slots are bounded: a wait that runs
+// out records an error in the workspace header and the CTA stops.
 #include "ffn_common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int CW = 12;                    // warps
-constexpr int THREADS = 32 * CW;
-constexpr uint32_t LUT_ADDR = 0x10000;    // table: [0x10000, 0x30000) of the shared window
-constexpr uint32_t LUT_HALF = 0x10000;    // scale blocks 0-1 | 2-3
-constexpr uint32_t DYN_SMEM = 0x30000;    // dynamic shared memory requested
-constexpr int MAX_GROUP = 32;             // table pairs of one token (<= k <= 32)
+constexpr int LW = 16;                   // warps
+constexpr int THREADS = 32 * LW;
+constexpr int KR_IN = 128 * LUT_KB;      // inputs per K-range: 32 lanes x 8 groups x 4
+constexpr uint32_t TAB = 0x10000;        // table: [0x10000, 0x30000) of the shared window
+constexpr uint32_t PLANE = 0x10000;      // group slots 0-3 | 4-7
+constexpr uint32_t DYN_SMEM = 227 * 1024;  // dynamic shared memory requested (the maximum)
+constexpr int MAX_GROUP = 32;            // table pairs of one token (<= k <= 32)
+// One code slot per warp, filled by three bulk copies: tiles 0-3 of the unit
+// (2 KB), tiles 4-7 after 64 bytes of skew, then the 8 tiles' row scales (32
+// bytes each).  The lanes of a quarter-warp take scale blocks b and b + 4, so
+// their 16-byte reads of one group slot hit 8 distinct bank groups.
+constexpr uint32_t HALF_OFF = 4 * 512 + 64;
+constexpr uint32_t SCALE_OFF = HALF_OFF + 4 * 512;
+constexpr uint32_t SLOT_BYTES = SCALE_OFF + 8 * 32;
+constexpr int NSLOT = LW;
+constexpr int LOW_SLOTS = 12;            // slots below the table; the rest above it
+// scale block of lane l (the 4 lanes 4q .. 4q+3 share one): blocks b and b + 4
+// for the two lane quads of each quarter-warp
+__host__ __device__ constexpr int lane_block(int l) { return (((l >> 2) & 1) << 2) | (l >> 3); }
+constexpr uint32_t HIGH_BASE = TAB + 2 * PLANE;
+
+// Inputs of the K-range in shared memory: float i at xs_at(i), a float4 of
+// padding after every 32 groups (one scale block), so the table build's
+// 16-byte reads of one group in each of the 8 blocks spread over all banks.
+__device__ __forceinline__ int xs_at(int i) { return i + 4 * (i >> 7); }
 
 struct __align__(16) Smem {
-    float xs[128 * LUT_KB];
+    unsigned long long full[NSLOT];  // slot mbarriers (one arrival + the copied bytes)
+    float xs[KR_IN + KR_IN / 32];
+    uint8_t lastf[256];  // FC2: the row tiles whose partials this CTA adds up
     float cb[128 * 4];
     const void* pa[MAX_GROUP];  // per pair of the current group: FC1 gate / FC2 down codes
     const void* pb[MAX_GROUP];  // FC1 up codes
     const void* sa[MAX_GROUP];  // matching scales
     const void* sb[MAX_GROUP];
+    int ys[MAX_GROUP];          // FC2: sorted position of the pair
+    int failed;
 };
+static_assert(0x400 + ((sizeof(Smem) + 127) / 128 * 128) + LOW_SLOTS * SLOT_BYTES <= TAB &&
+                  HIGH_BASE + (NSLOT - LOW_SLOTS) * SLOT_BYTES <= 0x400 + DYN_SMEM && NSLOT >= LOW_SLOTS,
+              "shared layout");
 
-// shared-window byte address of table entry (code c, group g of the K-range)
-__device__ __forceinline__ uint32_t lut_addr(int c, int g) {
-    const int b = g >> 5, gg = g & 31;
-    const int pos = 32 * (b & 1) + ((gg + 8 * b) & 31);
-    return LUT_ADDR + (uint32_t)(b >> 1) * LUT_HALF + (uint32_t)c * 256u + 4u * pos;
+// Table entry of lane l, group slot j, code c sits at shared-window byte
+//     TAB + (j/4)*PLANE + c*256 + 128*((j/2)&1) + 4*l + 2*(j&1):
+// the code fills bits 8-15 (one byte permute), the slot is an immediate.
+template <int J>
+__device__ __forceinline__ float tab_add(uint32_t addr, float t) {
+    constexpr int IMM = (J >> 2) * (int)PLANE + 128 * ((J >> 1) & 1) + 2 * (J & 1);
+    uint16_t v;
+    asm volatile("ld.shared.b16 %0, [%1+%2];" : "=h"(v) : "r"(addr), "n"(IMM));
+    float d;
+    asm("add.rn.f32.f16 %0, %1, %2;" : "=f"(d) : "h"(v), "f"(t));
+    return d;
+}
+
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t prmt_i(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "n"(SEL));
+    return d;
 }
 
 struct UnitRegs {
-    uint4 cw[4];  // this lane's 4 chunks: 16 rows x 4 groups
+    uint4 cw[8];  // group slot j: the 16 code bytes (rows) of group 4j + m
     uint4 sc[2];  // the 16 row scales of this lane's scale block
 };
 
+// Sum over the lane's 8 groups of row byte RB (row (RB >> 1) + 8 (RB & 1)).
+template <int RB>
+__device__ __forceinline__ float row_sum(const UnitRegs& u, uint32_t lb) {
+    constexpr uint32_t SEL = 0x7604u | ((uint32_t)(RB & 3) << 4);
+    float t = 0.0f;
+    t = tab_add<0>(prmt_i<SEL>((&u.cw[0].x)[RB >> 2], lb), t);
+    t = tab_add<1>(prmt_i<SEL>((&u.cw[1].x)[RB >> 2], lb), t);
+    t = tab_add<2>(prmt_i<SEL>((&u.cw[2].x)[RB >> 2], lb), t);
+    t = tab_add<3>(prmt_i<SEL>((&u.cw[3].x)[RB >> 2], lb), t);
+    t = tab_add<4>(prmt_i<SEL>((&u.cw[4].x)[RB >> 2], lb), t);
+    t = tab_add<5>(prmt_i<SEL>((&u.cw[5].x)[RB >> 2], lb), t);
+    t = tab_add<6>(prmt_i<SEL>((&u.cw[6].x)[RB >> 2], lb), t);
+    t = tab_add<7>(prmt_i<SEL>((&u.cw[7].x)[RB >> 2], lb), t);
+    constexpr int ROW = (RB >> 1) + 8 * (RB & 1);
+    const uint32_t s2 = (&u.sc[ROW >> 3].x)[(ROW & 7) >> 1];
+    const __half2 h = *reinterpret_cast<const __half2*>(&s2);
+    return t * ((ROW & 1) ? __high2float(h) : __low2float(h));
+}
+
+// Register cap: each of the SM's four schedulers holds 16384 registers for
+// its share of the CTA's warps (ceil(LW / 4) warps).
+constexpr int MAX_REG = 16384 / (32 * ((LW + 3) / 4)) > 255 ? 255 : 16384 / (32 * ((LW + 3) / 4)) / 8 * 8;
+
 template <bool FC1>
-__global__ void __launch_bounds__(THREADS, 1)
-    ffn_lut_kernel(const SlotDesc* __restrict__ desc, const uint16_t* __restrict__ codebook,
-                   const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_pair, int k, int H, int I,
-                   int* __restrict__ header, const int32_t* __restrict__ lut_s, const int32_t* __restrict__ lut_e,
-                   const int32_t* __restrict__ lut_grp, const int32_t* __restrict__ grp_start,
-                   const float* __restrict__ p1, float* __restrict__ pout) {
+__global__ void __maxnreg__(MAX_REG)
+    ffn_lut_kernel(const uint16_t* __restrict__ codebook, const uint16_t* __restrict__ x,
+                   const int32_t* __restrict__ sorted_pair, const float* __restrict__ weights, int k, int H, int I,
+                   int* __restrict__ header, const LutRec* __restrict__ recs,
+                   const int2* __restrict__ fc1_range, const float* __restrict__ p1, float* __restrict__ pout,
+                   int* __restrict__ cnt, int mode, float* __restrict__ out) {
     extern __shared__ __align__(1024) uint8_t dyn[];
     Smem& S = *reinterpret_cast<Smem*>(dyn);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -71,285 +143,389 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int KR = lut_jobs(K);
     const int RT = R / 16;
     const int KR1 = lut_jobs(H);
+    const int per_pair = KR * RT;          // units of one pair
+    const int C = gridDim.x;
 
-    // the fixed table address needs the low part of dynamic shared memory
-    // below it and the allocation to reach past its end
+    // The fixed table address needs the low part of dynamic shared memory
+    // below it and the allocation to reach past its end; the code slots sit
+    // around it.
     const uint32_t base = smem_u32(dyn);
-    if (base + (uint32_t)sizeof(Smem) > LUT_ADDR || base + DYN_SMEM < LUT_ADDR + 2 * LUT_HALF) {
+    const uint32_t low_base = (base + (uint32_t)sizeof(Smem) + 127u) & ~127u;
+    if (low_base + LOW_SLOTS * SLOT_BYTES > TAB || base + DYN_SMEM < HIGH_BASE + (NSLOT - LOW_SLOTS) * SLOT_BYTES) {
         if (tid == 0) atomicExch(err, MOE_DEVERR_SMEM_LAYOUT);
         return;
     }
+    const uint32_t slot = warp < LOW_SLOTS ? low_base + warp * SLOT_BYTES : HIGH_BASE + (warp - LOW_SLOTS) * SLOT_BYTES;
+    const uint32_t bar = smem_u32(&S.full[warp]);
     for (int i = tid; i < 128 * 4; i += THREADS) S.cb[i] = __half2float(__ushort_as_half(codebook[i]));
-    pdl_wait();
+    if (tid < NSLOT) mbar_init(smem_u32(&S.full[tid]), 1);
+    if (tid == 0) S.failed = 0;
+    mbar_fence_init();
 
-    const int n_lut = header[HDR_NLUT];
     // Units are (job, row tile) with job = (group, K-range).  FC1 groups are
     // the table pairs of one token (they share the activation table); FC2
     // groups are single pairs (the table depends on the pair's silu(g)*u).
-    // A group of gc pairs starting at sorted pair gs owns the units
-    // [KR*RT*gs, KR*RT*(gs+gc)), ordered (K-range, pair, row tile).
-    // CTA blockIdx.x owns the contiguous range [u0, u1).
-    const int per_pair = KR * RT;
-    const int U = n_lut * per_pair;
-    const int u0 = (int)((long long)U * blockIdx.x / gridDim.x);
-    const int u1 = (int)((long long)U * (blockIdx.x + 1) / gridDim.x);
-
-    const int b = lane >> 3;  // scale block of this lane inside the K-range
-    uint32_t lbase[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int gg = (lane & 7) + 8 * q;
-        const int pos = 32 * (b & 1) + ((gg + 8 * b) & 31);
-        lbase[q] = ((uint32_t)(LUT_ADDR + (b >> 1) * LUT_HALF) & 0xffff0000u) | (uint32_t)(4 * pos);
+    // A group of gc pairs starting at table pair gs owns the units
+    // [per_pair*gs, per_pair*(gs+gc)), ordered (K-range, pair, row tile).
+    int n_lut, u0, u1;
+    bool waited = FC1;  // FC2 waits for FC1 once its first job's code copies are issued
+    if (FC1) {
+        pdl_wait();
+        // everything a dependent kernel may touch before its own wait is complete
+        pdl_launch_dependents();
+        n_lut = header[HDR_NLUT];
+        const int2 rg = fc1_range[blockIdx.x];  // computed by the schedule
+        u0 = rg.x;
+        u1 = rg.y;
+        // FC2's arrival counters start at zero
+        const int nc = n_lut * (H / 16);
+        for (int i = blockIdx.x * THREADS + tid; i < nc; i += C * THREADS) cnt[i] = 0;
+    } else {
+        // The schedule is two kernels back, so complete: this CTA's units and
+        // their code bytes are known before FC1 completes.  FC2 jobs (pair,
+        // K-range) are all RT units, so the proportional split is direct.
+        n_lut = __ldcg(header + HDR_NLUT);
+        const int J = n_lut * KR, U = n_lut * per_pair;
+        if (J > 0 && J <= C) {
+            const int jb = (int)(((long long)(blockIdx.x + 1) * J - 1) / C);  // a0(jb) <= i < a0(jb + 1)
+            const int a0 = lut_cta_of((long long)jb * RT, C, U), a1 = lut_cta_of((long long)(jb + 1) * RT, C, U);
+            const int n = a1 - a0, r = blockIdx.x - a0;
+            u0 = jb * RT + RT * r / n;
+            u1 = jb * RT + RT * (r + 1) / n;
+        } else {
+            u0 = (int)((long long)U * blockIdx.x / C);
+            u1 = (int)((long long)U * (blockIdx.x + 1) / C);
+        }
     }
+
+    const int b = lane_block(lane), m = lane & 3;  // scale block and group phase of this lane
+    const uint32_t lb = TAB | (uint32_t)(4 * lane);
+    uint32_t phase = 0;                     // parity of the slot's next completion
+    bool pend = false;                      // the slot has a copy in flight
+    bool ok = true;                         // this warp's slot waits all completed
 
     int u = u0;
     while (u < u1) {
-        int gs, gc;
-        {
-            const int p0 = u / per_pair;
-            if (FC1) {
-                const int g = lut_grp[p0];
-                gs = grp_start[g];
-                gc = grp_start[g + 1] - gs;
-            } else {
-                gs = p0;
-                gc = 1;
-            }
-        }
+        __syncthreads();  // every warp is done with the previous table and pointers
+        if (S.failed) break;
+        const LutRec& r0 = recs[u / per_pair];
+        const int gs = FC1 ? r0.gs : u / per_pair;
+        const int gc = FC1 ? r0.gc : 1;
         const int kr = (u - per_pair * gs) / (RT * gc);
         const int job_start = per_pair * gs + kr * RT * gc;
         const int seg_end = min(u1, job_start + RT * gc);
         const int nkb = min(LUT_KB, KB - LUT_KB * kr);
         const int nin = 128 * nkb;
         const bool active = b < nkb;
-
-        __syncthreads();  // every warp is done with the previous table and pointers
         if (tid < gc) {
-            const SlotDesc& d = desc[lut_e[gs + tid]];
-            S.pa[tid] = d.codes[FC1 ? 0 : 2];
-            S.sa[tid] = d.scales[FC1 ? 0 : 2];
-            S.pb[tid] = d.codes[1];
-            S.sb[tid] = d.scales[1];
+            const LutRec& r = recs[gs + tid];
+            S.pa[tid] = r.codes[FC1 ? 0 : 2];
+            S.sa[tid] = r.scales[FC1 ? 0 : 2];
+            S.pb[tid] = r.codes[1];
+            S.sb[tid] = r.scales[1];
+            S.ys[tid] = r.sorted;
         }
-        // inputs of this K-range: FC1 the token's activations, FC2 silu(g)*u
-        // of the pair, from FC1's K-range partial sums added in a fixed order
-        if (FC1) {
-            const int t = sorted_pair[lut_s[gs]] / k;
+        if (FC1) {  // the token's activations of this K-range
+            const int t = r0.token;
             for (int i = tid; i < nin; i += THREADS)
-                S.xs[i] = __uint_as_float((uint32_t)x[(size_t)t * H + LUT_KB * 128 * kr + i] << 16);
-        } else {
-            const float* pp = p1 + (size_t)gs * KR1 * 2 * I;
-            for (int i = tid; i < nin; i += THREADS) {
-                const int gi = LUT_KB * 128 * kr + i;
-                float g = 0.0f, up = 0.0f;
-                for (int j0 = 0; j0 < KR1; j0 += 8) {  // 8 partials in flight, added in order
-                    float pg[8], pu[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        pg[j] = j0 + j < KR1 ? pp[(size_t)(j0 + j) * 2 * I + gi] : 0.0f;
-                        pu[j] = j0 + j < KR1 ? pp[(size_t)(j0 + j) * 2 * I + I + gi] : 0.0f;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (j0 + j < KR1) {
-                            g += pg[j];
-                            up += pu[j];
-                        }
-                    }
-                }
-                S.xs[i] = g / (1.0f + expf(-g)) * up;
-            }
-        }
-        __syncthreads();
-        // table entries: +dot for code c, -dot for c + 128; a thread takes one
-        // group and the four codes c, c+32, c+64, c+96
-        const int G = 32 * nkb;
-        for (int idx = tid; idx < 32 * G; idx += THREADS) {
-            const int c0 = idx / G, g = idx - c0 * G;
-            const float4 xv = *reinterpret_cast<const float4*>(&S.xs[4 * g]);
-            const uint32_t a0 = lut_addr(c0, g);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 e4 = *reinterpret_cast<const float4*>(&S.cb[4 * (c0 + 32 * q)]);
-                float v = e4.x * xv.x;
-                v = fmaf(e4.y, xv.y, v);
-                v = fmaf(e4.z, xv.z, v);
-                v = fmaf(e4.w, xv.w, v);
-                const uint32_t a = a0 + 32u * 256u * q;
-                sts_f32(a, v);
-                sts_f32(a + 128u * 256u, -v);
-            }
+                S.xs[xs_at(i)] = __uint_as_float((uint32_t)x[(size_t)t * H + KR_IN * kr + i] << 16);
         }
         __syncthreads();
 
-        // this warp's units of the job: v = u + warp, u + warp + CW, ...; the
-        // (pair, row tile) of a unit advances by CW row tiles per step
-        auto load_unit = [&](int pi, int rt, UnitRegs& r) {
-            const bool second = FC1 && rt >= I / 16;  // an up-matrix row tile
-            const int rtm = second ? rt - I / 16 : rt;
-            const size_t tile = (size_t)rtm * KB + LUT_KB * kr + b;
-            if (active) {
-                const uint8_t* c = static_cast<const uint8_t*>(second ? S.pb[pi] : S.pa[pi]) + tile * 512;
-                const uint16_t* sp = static_cast<const uint16_t*>(second ? S.sb[pi] : S.sa[pi]) + tile * 16;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) r.cw[q] = ldg_stream(c + 16 * ((lane & 7) + 8 * q));
-                r.sc[0] = ldg_stream(sp);
-                r.sc[1] = ldg_stream(sp + 8);
+        // unit v of the job <-> (pair pi of the group, row tile rt); cursors
+        // move by LW units without divisions
+        struct Cur {
+            int pi, rt;
+        };
+        auto cur_at = [&](int off) {
+            Cur c;
+            c.pi = off / RT;
+            c.rt = off - c.pi * RT;
+            return c;
+        };
+        auto advance = [&](Cur c) {
+            c.rt += LW;
+            while (c.rt >= RT) {
+                c.rt -= RT;
+                ++c.pi;
+            }
+            return c;
+        };
+        auto unit_ptrs = [&](Cur cu, const uint8_t*& c, const uint16_t*& sp) {
+            const bool second = FC1 && cu.rt >= I / 16;  // an up-matrix row tile
+            const int rtm = second ? cu.rt - I / 16 : cu.rt;
+            const size_t tile = (size_t)rtm * KB + LUT_KB * kr;
+            c = static_cast<const uint8_t*>(second ? S.pb[cu.pi] : S.pa[cu.pi]) + tile * 512;
+            sp = static_cast<const uint16_t*>(second ? S.sb[cu.pi] : S.sa[cu.pi]) + tile * 16;
+        };
+        // Unit at cursor cu into the warp's slot: lane 0 arms the barrier
+        // with the byte count, lanes < nkb copy one tile each, lane 31 the
+        // scales.
+        auto issue = [&](Cur cu) {
+            pend = true;
+            const uint8_t* c;
+            const uint16_t* sp;
+            unit_ptrs(cu, c, sp);
+            if (lane == 0) mbar_arrive_expect_tx(bar, 544u * nkb);
+            __syncwarp();
+            if (lane == 0) bulk_g2s(slot, c, 512u * min(nkb, 4), bar);
+            if (lane == 1 && nkb > 4) bulk_g2s(slot + HALF_OFF, c + 2048, 512u * (nkb - 4), bar);
+            if (lane == 2) bulk_g2s(slot + SCALE_OFF, sp, 32u * nkb, bar);
+        };
+        auto prefetch = [&](Cur cu) {  // ask L2 for the unit at cu
+            if (lane == 0) {
+                const uint8_t* c;
+                const uint16_t* sp;
+                unit_ptrs(cu, c, sp);
+                (void)sp;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c), "r"(512u * nkb) : "memory");
             }
         };
-        auto advance = [&](int& pi, int& rt) {
-            rt += CW;
-            while (rt >= RT) {
-                rt -= RT;
-                ++pi;
-            }
-        };
-        UnitRegs cur, n1, n2;
         int v = u + warp;
-        int pi = (v - job_start) / RT, rt = (v - job_start) - ((v - job_start) / RT) * RT;
-        int pi1 = pi, rt1 = rt, pi2, rt2;
-        advance(pi1, rt1);
-        pi2 = pi1;
-        rt2 = rt1;
-        advance(pi2, rt2);
-        if (v < seg_end) load_unit(pi, rt, cur);
-        if (v + CW < seg_end) load_unit(pi1, rt1, n1);
-        for (; v < seg_end; v += CW) {
-            if (v + 2 * CW < seg_end) load_unit(pi2, rt2, n2);
-            float acc[16];
-            if (active) {
-                float s[16];
-                const uint32_t sw[8] = {cur.sc[0].x, cur.sc[0].y, cur.sc[0].z, cur.sc[0].w,
-                                        cur.sc[1].x, cur.sc[1].y, cur.sc[1].z, cur.sc[1].w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&sw[i]));
-                    s[2 * i] = f.x;
-                    s[2 * i + 1] = f.y;
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {  // byte position r of each chunk
-                    const uint32_t sel = 0x7604u | ((uint32_t)(r & 3) << 4);
-                    float t = 0.0f;
+        Cur c0 = cur_at(v - job_start);   // the unit computed next
+        Cur c1 = advance(c0);             // the one after it
+        Cur c2 = advance(c1);
+        if (v < seg_end) issue(c0);
+        if (v + LW < seg_end) prefetch(c1);
+
+        if (!waited) {
+            pdl_wait();
+            // everything a dependent kernel may touch before its own wait is complete
+            pdl_launch_dependents();
+            waited = true;
+        }
+        if (!FC1) {
+            // silu(g) * u of the pair from FC1's K-range partial sums, added in
+            // order: a thread's (up to 4) inputs with 4 partials each in flight
+            const float* pp = p1 + (size_t)gs * KR1 * 2 * I;
+            for (int i0 = tid; i0 < nin; i0 += 4 * THREADS) {
+                float g[4] = {0.0f, 0.0f, 0.0f, 0.0f}, up[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int j0 = 0; j0 < KR1; j0 += 4) {
+                    float pg[4][4], pu[4][4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const uint32_t w = (&cur.cw[q].x)[r >> 2];
-                        t += lds_f32(prmt(w, lbase[q], sel));
+                        const int i = i0 + q * THREADS, gi = KR_IN * kr + i;
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const bool in = i < nin && j0 + jj < KR1;
+                            pg[q][jj] = in ? pp[(size_t)(j0 + jj) * 2 * I + gi] : 0.0f;
+                            pu[q][jj] = in ? pp[(size_t)(j0 + jj) * 2 * I + I + gi] : 0.0f;
+                        }
                     }
-                    const int row = (r >> 1) + 8 * (r & 1);  // byte 2i+h holds row i + 8h
-                    acc[r] = t * s[row];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            if (j0 + jj < KR1) {
+                                g[q] += pg[q][jj];
+                                up[q] += pu[q][jj];
+                            }
                 }
-            } else {
 #pragma unroll
-                for (int r = 0; r < 16; ++r) acc[r] = 0.0f;
+                for (int q = 0; q < 4; ++q) {
+                    const int i = i0 + q * THREADS;
+                    if (i < nin) S.xs[xs_at(i)] = g[q] / (1.0f + expf(-g[q])) * up[q];
+                }
             }
-            // reduce-scatter over the warp: lanes 2p and 2p+1 end with position p
+            __syncthreads();
+        }
+
+        // Table: a thread takes a quad of words (the 4 lanes 4 lq .. 4 lq + 3 of
+        // scale block bq, in group-slot pair (j0, j0 + 1), j0 = 4p + 2jj: the
+        // 8 consecutive groups 32 bq + 4 j0 + 0..7) and every LW-th code.
+        {
+            const int q = tid & 31, lq = q & 7, jj = (q >> 3) & 1, p = q >> 4, bq = lane_block(4 * lq);
+            if (bq < nkb) {
+                const int g0 = 32 * bq + 4 * (4 * p + 2 * jj);
+                // xp[m][i] = (x[4(g0+m)+i], x[4(g0+4+m)+i]): the low / high half of word m
+                float2 xp[4][4];
 #pragma unroll
-            for (int o = 16, n8 = 8; o >= 2; o >>= 1, n8 >>= 1) {
-                const bool up = lane & o;
+                for (int mm = 0; mm < 4; ++mm) {
+                    const float4 lo = *reinterpret_cast<const float4*>(&S.xs[xs_at(4 * (g0 + mm))]);
+                    const float4 hi = *reinterpret_cast<const float4*>(&S.xs[xs_at(4 * (g0 + 4 + mm))]);
+                    xp[mm][0] = make_float2(lo.x, hi.x);
+                    xp[mm][1] = make_float2(lo.y, hi.y);
+                    xp[mm][2] = make_float2(lo.z, hi.z);
+                    xp[mm][3] = make_float2(lo.w, hi.w);
+                }
+                const uint32_t a0 = TAB + (uint32_t)p * PLANE + 128u * jj + 16u * lq;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int it = 0; it < 128 / LW; ++it) {
+                    const int c0 = warp + it * LW;
+                    const float4 e = *reinterpret_cast<const float4*>(&S.cb[4 * c0]);
+                    const float2 ex = make_float2(e.x, e.x), ey = make_float2(e.y, e.y);
+                    const float2 ez = make_float2(e.z, e.z), ew = make_float2(e.w, e.w);
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int mm = 0; mm < 4; ++mm) {
+                        float2 v2 = __fmul2_rn(ex, xp[mm][0]);
+                        v2 = __ffma2_rn(ey, xp[mm][1], v2);
+                        v2 = __ffma2_rn(ez, xp[mm][2], v2);
+                        v2 = __ffma2_rn(ew, xp[mm][3], v2);
+                        const __half2 hv = __floats2half2_rn(v2.x, v2.y);
+                        wv[mm] = *reinterpret_cast<const uint32_t*>(&hv);
+                    }
+                    const uint32_t a = a0 + 256u * (uint32_t)c0;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wv[0]), "r"(wv[1]),
+                                 "r"(wv[2]), "r"(wv[3]));
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + 128u * 256u),
+                                 "r"(wv[0] ^ 0x80008000u), "r"(wv[1] ^ 0x80008000u), "r"(wv[2] ^ 0x80008000u),
+                                 "r"(wv[3] ^ 0x80008000u));
+                }
+            }
+        }
+        __syncthreads();
+
+        auto compute_store = [&](const UnitRegs& r, Cur cu) {
+            const int pi = cu.pi, rt = cu.rt;
+            // Reduce-scatter over the warp (lanes 2p and 2p+1 end with byte
+            // position p); its first step (lanes 16 apart) runs as each pair
+            // of row sums (i, i + 8) is ready, so only 8 sums stay live.
+            float acc[8];
+            const bool up16 = lane & 16;
+#define MOE_LUT_PAIR(I)                                                                  \
+    {                                                                                    \
+        const float lo = active ? row_sum<I>(r, lb) : 0.0f;                              \
+        const float hi = active ? row_sum<I + 8>(r, lb) : 0.0f;                          \
+        acc[I] = (up16 ? hi : lo) + __shfl_xor_sync(0xffffffffu, up16 ? lo : hi, 16);   \
+    }
+            MOE_LUT_PAIR(0)
+            MOE_LUT_PAIR(1)
+            MOE_LUT_PAIR(2)
+            MOE_LUT_PAIR(3)
+            MOE_LUT_PAIR(4)
+            MOE_LUT_PAIR(5)
+            MOE_LUT_PAIR(6)
+            MOE_LUT_PAIR(7)
+#undef MOE_LUT_PAIR
+#pragma unroll
+            for (int o = 8, n8 = 4; o >= 2; o >>= 1, n8 >>= 1) {
+                const bool upo = lane & o;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
                     if (i < n8) {
-                        const float send = up ? acc[i] : acc[i + n8];
-                        const float keep = up ? acc[i + n8] : acc[i];
+                        const float send = upo ? acc[i] : acc[i + n8];
+                        const float keep = upo ? acc[i + n8] : acc[i];
                         acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
                     }
                 }
             }
             acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
-            if ((lane & 1) == 0) {
-                const int p = lane >> 1;
-                const int row = (p >> 1) + 8 * (p & 1);
-                pout[((size_t)(gs + pi) * KR + kr) * R + (size_t)rt * 16 + row] = acc[0];
+            const int pp = lane >> 1;
+            const int h = rt * 16 + (pp >> 1) + 8 * (pp & 1);  // output row of this lane pair
+            auto emit = [&](float y) {  // FC2: the finished y of row h
+                const int s = S.ys[pi];
+                if (mode == MOE_PER_PAIR) {
+                    out[(size_t)s * H + h] = y;
+                } else {
+                    const int pr = sorted_pair[s];
+                    atomicAdd(out + (size_t)(pr / k) * H + h, weights[pr] * y);
+                }
+            };
+            if (FC1 || KR > 1) {
+                if ((lane & 1) == 0) pout[((size_t)(gs + pi) * KR + kr) * R + h] = acc[0];
+            } else if ((lane & 1) == 0) {
+                emit(acc[0]);
             }
-            cur = n1;
-            n1 = n2;
-            pi = pi1;
-            rt = rt1;
-            pi1 = pi2;
-            rt1 = rt2;
-            advance(pi2, rt2);
+        };
+
+        // This warp's units of the job: v, v + LW, ...  The slot is copied to
+        // registers and handed to the copy of the next unit (the one after
+        // that is asked of L2), then the unit is computed from registers.
+        for (; v < seg_end; v += LW) {
+            if (!mbar_wait_bounded(bar, phase, err, MOE_DEVERR_WAIT_FULL)) {
+                ok = false;
+                break;
+            }
+            phase ^= 1u;
+            pend = false;
+            UnitRegs r;
+            if (active) {
+                const uint32_t tb = slot + (b < 4 ? 512u * b : HALF_OFF + 512u * (b - 4)) + 16u * m;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) r.cw[jj] = lds_u128(tb + 64 * jj);
+                r.sc[0] = lds_u128(slot + SCALE_OFF + 32 * b);
+                r.sc[1] = lds_u128(slot + SCALE_OFF + 32 * b + 16);
+            }
+            __syncwarp();
+            // the generic-proxy reads of the slot come before the next copy's writes
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (v + LW < seg_end) issue(c1);
+            if (v + 2 * LW < seg_end) prefetch(c2);
+            compute_store(r, c0);
+            c0 = c1;
+            c1 = c2;
+            c2 = advance(c2);
+        }
+        if (!ok) {
+            // stop the CTA; a copy this warp still has in flight lands before
+            // it leaves (bounded wait again)
+            S.failed = 1;
+            if (pend) mbar_wait_bounded(bar, phase, nullptr, 0);
+            pend = false;
+        }
+        if (!FC1 && KR > 1) {
+            // FC2 partials of this job's row tiles are all stored: one fence per
+            // thread, then per row tile one arrival; the last of the KR units of
+            // a row tile adds the partials in K-range order and writes y.
+            __threadfence();
+            __syncthreads();
+            const int pr = gs;  // FC2 groups are single pairs
+            const int s = S.ys[0];
+            for (int tb = u - job_start; tb < seg_end - job_start; tb += 256) {
+                const int nt = min(256, seg_end - job_start - tb);
+                for (int t = tid; t < nt; t += THREADS) {
+                    int* c = cnt + (size_t)pr * RT + tb + t;
+                    const bool last = atomicAdd(c, 1) == KR - 1;
+                    S.lastf[t] = last;
+                    if (last) *c = 0;
+                }
+                __threadfence();
+                __syncthreads();
+                // the row tiles this CTA finishes: one output row per thread
+                for (int idx = tid; idx < 16 * nt; idx += THREADS) {
+                    const int t = idx >> 4;
+                    if (!S.lastf[t]) continue;
+                    const int h = (tb + t) * 16 + (idx & 15);
+                    const float* src = pout + (size_t)pr * KR * R + h;
+                    float y = __ldcg(src);
+                    for (int jj = 1; jj < KR; ++jj) y += __ldcg(src + (size_t)jj * R);
+                    if (mode == MOE_PER_PAIR) {
+                        out[(size_t)s * H + h] = y;
+                    } else {
+                        const int p = sorted_pair[s];
+                        atomicAdd(out + (size_t)(p / k) * H + h, weights[p] * y);
+                    }
+                }
+                __syncthreads();  // flags are reused by the next chunk
+            }
         }
         u = seg_end;
     }
-    pdl_launch_dependents();
-}
-
-// y = sum of the FC2 K-range partials (fixed order); per-pair store or
-// weighted scatter-add.
-__global__ void __launch_bounds__(256) lut_finish_kernel(const int* __restrict__ header,
-                                                         const int32_t* __restrict__ lut_s,
-                                                         const int32_t* __restrict__ sorted_pair,
-                                                         const float* __restrict__ weights, int k, int H, int I,
-                                                         const float* __restrict__ p2, int mode,
-                                                         float* __restrict__ out) {
-    pdl_wait();
-    const int n_lut = header[HDR_NLUT];
-    const int KR2 = lut_jobs(I);
-    const int n = n_lut * (H / 4);
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-        const int li = i / (H / 4), h = 4 * (i - li * (H / 4));
-        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < KR2; ++j) {
-            const float4 v = *reinterpret_cast<const float4*>(p2 + ((size_t)li * KR2 + j) * H + h);
-            y.x += v.x;
-            y.y += v.y;
-            y.z += v.z;
-            y.w += v.w;
-        }
-        const int s = lut_s[li];
-        if (mode == MOE_PER_PAIR) {
-            *reinterpret_cast<float4*>(out + (size_t)s * H + h) = y;
-        } else {
-            const int p = sorted_pair[s];
-            const float w = weights[p];
-            float* o = out + (size_t)(p / k) * H + h;
-            atomicAdd(o + 0, w * y.x);
-            atomicAdd(o + 1, w * y.y);
-            atomicAdd(o + 2, w * y.z);
-            atomicAdd(o + 3, w * y.w);
-        }
+    if (!waited) {  // a CTA without units still waits for FC1 before it leaves
+        pdl_wait();
+        pdl_launch_dependents();
     }
-    pdl_launch_dependents();
 }
 
 }  // namespace
 
-moe_status launch_lut_fc(bool fc1, const SlotTableHost* t, const uint16_t* x, const int32_t* sorted_pair, int k,
-                         char* ws, const WsLayout& L, cudaStream_t s) {
-    static_assert(sizeof(Smem) + 1024 <= LUT_ADDR, "shared layout");
+moe_status launch_lut_fc(bool fc1, const SlotTableHost* t, const uint16_t* x, const int32_t* sorted_pair,
+                         const float* weights, int k, int mode, float* out, char* ws, const WsLayout& L,
+                         cudaStream_t s) {
     int* header = reinterpret_cast<int*>(ws);
-    const int32_t* lut_s = reinterpret_cast<const int32_t*>(ws + L.lut_s_off);
-    const int32_t* lut_e = reinterpret_cast<const int32_t*>(ws + L.lut_e_off);
-    const int32_t* lut_grp = reinterpret_cast<const int32_t*>(ws + L.lut_grp_off);
-    const int32_t* grp_start = reinterpret_cast<const int32_t*>(ws + L.grp_start_off);
+    const LutRec* recs = reinterpret_cast<const LutRec*>(ws + L.rec_off);
+    const int2* fc1_range = reinterpret_cast<const int2*>(ws + L.range_off);
     const float* p1 = reinterpret_cast<const float*>(ws + L.p1_off);
     float* pout = reinterpret_cast<float*>(ws + (fc1 ? L.p1_off : L.p2_off));
+    int* cnt = reinterpret_cast<int*>(ws + L.cnt_off);
     auto kern = fc1 ? ffn_lut_kernel<true> : ffn_lut_kernel<false>;
     cudaError_t e = ensure_smem_attr(kern, (int)DYN_SMEM);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: table kernel shared memory");
-    e = launch_pdl(kern, dim3((unsigned)num_sms()), dim3(THREADS), DYN_SMEM, s, (const SlotDesc*)t->d_desc,
-                   t->codebook, x, sorted_pair, k, t->H, t->I, header, lut_s, lut_e, lut_grp, grp_start, p1, pout);
+    e = launch_pdl(kern, dim3((unsigned)num_sms()), dim3(THREADS), DYN_SMEM, s, t->codebook, x, sorted_pair, weights,
+                   k, t->H, t->I, header, recs, fc1_range, p1, pout, cnt, mode, out);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: table kernel launch");
     MOE_LAUNCH_CHECK("moe_vq2_expert_ffn: table kernel launch");
-    return MOE_OK;
-}
-
-moe_status launch_lut_finish(const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
-                             int mode, float* out, char* ws, const WsLayout& L, int max_lut, cudaStream_t s) {
-    const int* header = reinterpret_cast<const int*>(ws);
-    const int32_t* lut_s = reinterpret_cast<const int32_t*>(ws + L.lut_s_off);
-    const float* p2 = reinterpret_cast<const float*>(ws + L.p2_off);
-    long long n = (long long)max_lut * (t->H / 4);
-    long long blocks = (n + 255) / 256;
-    long long cap = (long long)num_sms() * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    cudaError_t e = launch_pdl(lut_finish_kernel, dim3((unsigned)blocks), dim3(256), 0, s, header, lut_s, sorted_pair,
-                               weights, k, t->H, t->I, p2, mode, out);
-    if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: table finish launch");
-    MOE_LAUNCH_CHECK("moe_vq2_expert_ffn: table finish launch");
     return MOE_OK;
 }
 

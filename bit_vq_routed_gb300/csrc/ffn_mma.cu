@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int n_rg = R / ROWS;
 
     pdl_wait();
+    pdl_launch_dependents();  // dependents may start their prologues now
     const int n_chunks = header[HDR_NCHUNKS];
     const int n_items = n_chunks * n_rg;
     if ((int)blockIdx.x >= n_items) return;
@@ -276,7 +277,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     }
-    pdl_launch_dependents();
 }
 
 }  // namespace

@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
     pdl_wait();
+    pdl_launch_dependents();  // dependents may start their prologues now
 
     const int n_chunks = header[HDR_NUMMA];
     const int n_items = n_chunks * n_rt;
@@ -353,7 +354,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
     }
-    pdl_launch_dependents();
 }
 
 // x16s[s, :] = fp16(x[token of sorted position s, :]) for the tensor-core B operand
@@ -361,6 +361,7 @@ __global__ void __launch_bounds__(256) gather_f16_kernel(const uint16_t* __restr
                                                          const int32_t* __restrict__ sorted_pair, int k, int H,
                                                          int P, uint16_t* __restrict__ x16s) {
     pdl_wait();
+    pdl_launch_dependents();  // dependents may start their prologues now
     const long long n = (long long)P * (H / 8);
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
         const int s = (int)(i / (H / 8)), c = (int)(i % (H / 8));
@@ -375,7 +376,6 @@ __global__ void __launch_bounds__(256) gather_f16_kernel(const uint16_t* __restr
         }
         *reinterpret_cast<uint4*>(x16s + (size_t)s * H + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    pdl_launch_dependents();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

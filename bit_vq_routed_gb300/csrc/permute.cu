@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(PT) permute_kernel(const int32_t* __restrict__
     __shared__ int32_t warp_tot[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();
+    pdl_launch_dependents();  // dependents may start their prologues now
     for (int i = tid; i < E * 33; i += PT) sm[i] = 0;
     __syncthreads();
     for (int p = tid; p < P; p += PT) atomicAdd(&cursor[ids[p]], 1);
@@ -77,7 +78,6 @@ __global__ void __launch_bounds__(PT) permute_kernel(const int32_t* __restrict__
         }
         __syncthreads();
     }
-    pdl_launch_dependents();
 }
 
 }  // namespace

@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t
         asm volatile("cp.async.commit_group;\n" ::: "memory");
     };
     pdl_wait();
+    pdl_launch_dependents();  // dependents may start their prologues now
     float acc[4][16];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
@@ -105,7 +106,6 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t
                 if (t < T && e < E) logits[(size_t)t * E + e] = bias ? __fadd_rn(acc[a][b], bias[e]) : acc[a][b];
             }
         }
-    pdl_launch_dependents();
 }
 
 __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(256) router_logits_small_kernel(const uint16_t
     for (int u = 0; u < U; ++u)
         if (u < per) wv[u] = __ldg(wr + lane + 32 * u);
     pdl_wait();
+    pdl_launch_dependents();  // dependents may start their prologues now
     for (int i = threadIdx.x; i < nch; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(x + (size_t)t * H)[i];
     __syncthreads();
     if (e >= E) return;
@@ -159,7 +160,6 @@ __global__ void __launch_bounds__(256) router_logits_small_kernel(const uint16_t
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(FULL, acc, off));
     if (lane == 0) logits[(size_t)t * E + e] = bias ? __fadd_rn(acc, bias[e]) : acc;
-    pdl_launch_dependents();
 }
 
 // One warp per token: lane l holds logits l, l+32, ...; each lane keeps its
@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
                                                          int k, int renorm, int32_t* __restrict__ ids,
                                                          float* __restrict__ weights) {
     pdl_wait();
+    pdl_launch_dependents();  // dependents may start their prologues now
     const int lane = threadIdx.x & 31;
     const long t = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= T) return;
@@ -240,7 +241,6 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
         ids[(size_t)t * k + lane] = sel_e;
         weights[(size_t)t * k + lane] = num / den;
     }
-    pdl_launch_dependents();
 }
 
 }  // namespace
