@@ -212,56 +212,26 @@ def run_gpu(args, wl, world, rank, local):
 
     step(0)  # first eager step: the library sets its kernel attributes outside any capture
     torch.cuda.synchronize()
+    def piece(fn):
+        g = torch.cuda.CUDAGraph()
+        n0 = bv.moe_launch_count()
+        with torch.cuda.graph(g):
+            fn()
+        g.kernels = bv.moe_launch_count() - n0  # library kernel nodes in this graph
+        return g
+
     if args.graph:
-        # Per token batch s of the pool: CUDA graphs of the step's pieces
-        # [route 0] [ffn 0] [combine 0 + route 1] [ffn 1] ... [combine last];
-        # the expert-FFN graphs are bracketed by events recorded on the
-        # stream between replays (event records cannot sit inside a capture).
-        def piece(fn):
-            g = torch.cuda.CUDAGraph()
-            n0 = bv.moe_launch_count()
-            with torch.cuda.graph(g):
-                fn()
-            g.kernels = bv.moe_launch_count() - n0  # library kernel nodes in this graph
-            return g
-
-        def route_fn(L, s):
-            return lambda: devs[L].route(pools[L][s])
-
-        def ffn_fn(L, s):
-            return lambda: devs[L].experts(pools[L][s], bv.MOE_PER_PAIR)
-
-        def comb(L):
-            d = devs[L]
-            bv.moe_combine(d.ypair[:T * d.k], d.pair_to_sorted[:T * d.k], d.weights[:T],
-                           d.pair_status[:T * d.k], d.k, d.out[:T])
-
-        graphs = []
-        for s in range(G):
-            seq = [("g", piece(route_fn(0, s)))]
-            for L in range(nL):
-                seq.append(("ffn", L, piece(ffn_fn(L, s))))
-                if L + 1 < nL:
-                    seq.append(("g", piece(lambda L=L, s=s: (comb(L), devs[L + 1].route(pools[L + 1][s])))))
-                else:
-                    seq.append(("g", piece(lambda L=L: comb(L))))
-            graphs.append(seq)
+        # Per token batch s of the pool: one CUDA graph of the whole step (every
+        # layer's route, expert FFN and combine, back to back with programmatic
+        # dependent launch), and one of the step's expert-FFN calls alone.
+        step_graphs = [piece(lambda s=s: step(s)) for s in range(G)]
+        ffn_graphs = [piece(lambda s=s: [devs[L].experts(pools[L][s], bv.MOE_PER_PAIR) for L in range(nL)])
+                      for s in range(G)]
 
         def run(s, evs=None):
-            n = 0
-            for item in graphs[s % G]:
-                if item[0] == "g":
-                    item[1].replay()
-                    n += item[1].kernels
-                else:
-                    L, g = item[1], item[2]
-                    if evs is not None:
-                        evs[L][0].record()
-                    g.replay()
-                    n += g.kernels
-                    if evs is not None:
-                        evs[L][1].record()
-            return n
+            g = step_graphs[s % G]
+            g.replay()
+            return g.kernels
     else:
         def run(s, evs=None):
             n0 = bv.moe_launch_count()
@@ -273,7 +243,7 @@ def run_gpu(args, wl, world, rank, local):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    step_ev = [new_events() for _ in range(args.steps)]
+    step_ev = [new_events() for _ in range(args.steps)] if not args.graph else None
     clocks = ClockSampler(local)
     clocks.start()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -281,24 +251,40 @@ def run_gpu(args, wl, world, rank, local):
     launches = 0
     start.record(stream)
     for s in range(args.steps):
-        launches += run(args.warmup + s, step_ev[s])
+        launches += run(args.warmup + s, None if step_ev is None else step_ev[s])
     end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     ms_total = start.elapsed_time(end)
     timed_slots = [(args.warmup + s) % G for s in range(args.steps)]
-    ffn_ms = [step_ev[s][L][0].elapsed_time(step_ev[s][L][1]) for s in range(args.steps) for L in range(nL)]
+    if args.graph:
+        # The expert-FFN call alone: per pool batch, the step graph (untimed)
+        # leaves every layer routed, then the graph of the step's nL FFN calls
+        # runs between two events; a call's time is that span / nL.
+        ffn_slots = timed_slots[:min(len(timed_slots), 64)]
+        ffn_ms = []
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ffn_slots]
+        for (a, b), sl in zip(ev, ffn_slots):
+            step_graphs[sl].replay()
+            a.record(stream)
+            ffn_graphs[sl].replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        for (a, b), sl in zip(ev, ffn_slots):
+            ffn_ms += [a.elapsed_time(b) / nL] * nL
+    else:
+        ffn_slots = timed_slots
+        ffn_ms = [step_ev[s][L][0].elapsed_time(step_ev[s][L][1]) for s in range(args.steps) for L in range(nL)]
     # distinct experts touched per FFN launch (read back after timing)
-    code_bytes = []
     per_slot = {}
-    for sl in sorted(set(timed_slots)):
+    for sl in sorted(set(ffn_slots)):
         for L, dev in enumerate(devs):
             dev.route(pools[L][sl])
             ids = np.unique(dev.ids[:T].cpu().numpy())
             fmts = layers[L].formats[ids]
             per_slot[(sl, L)] = (int((fmts == ms.FMT_VQ2).sum()) * VQ2_EXPERT_BYTES
                                  + int((fmts == ms.FMT_FP4).sum()) * FP4_EXPERT_BYTES)
-    code_bytes = [per_slot[(sl, L)] for sl in timed_slots for L in range(nL)]
+    code_bytes = [per_slot[(sl, L)] for sl in ffn_slots for L in range(nL)]
     if world > 1:
         t = torch.tensor([ms_total], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -401,8 +387,9 @@ def main():
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * 4096 * 2 * nL,
                 "d2h_bytes_per_step": T * 4096 * 4 * nL},
         "gpu_launches": r["launches"],
-        "launch": ("CUDA graphs: per layer [route] [expert FFN] [combine], replayed; events between "
-                   "replays time the expert-FFN call") if args.graph else "eager",
+        "launch": ("one CUDA graph per step (every layer's route, expert FFN and combine; programmatic "
+                   "dependent launch between kernels); the expert-FFN time is a graph of the step's FFN calls "
+                   "back to back, divided by the calls") if args.graph else "eager",
         "clocks": r["clocks"],
     }
     print(json.dumps(line))

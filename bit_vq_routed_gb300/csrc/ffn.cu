@@ -247,17 +247,29 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     // have work if the table holds FP4 experts.
     const bool mma = T > 1 || t->n_fp4 > 0 || !use_lut;
 
+    moe_status st;
+    if (T == 1 && t->n_fp4 == 0) {
+        // one token, VQ2 experts only: every pair takes the table path and the
+        // two table kernels list the pairs themselves (no schedule kernel)
+        if ((st = launch_lut_fc(true, true, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s)) !=
+            MOE_OK)
+            return st;
+        return launch_lut_fc(false, true, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s);
+    }
     cudaError_t e = launch_pdl(schedule_kernel, dim3(1), dim3(1024), 0, s, (const SlotDesc*)t->d_desc, E, offsets,
                                sorted_pair, P, k, status, header, chunks, recs, grp_start, use_lut,
                                uchunks, use_umma, H, I, num_sms(), reinterpret_cast<int2*>(w + L.range_off));
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule launch");
-    moe_status st;
     if ((mma || use_umma) && (st = launch_gather_f16(x, sorted_pair, k, H, P, x16s, s)) != MOE_OK) return st;
-    if (use_lut && (st = launch_lut_fc(true, t, x, sorted_pair, weights, k, mode, out, w, L, s)) != MOE_OK)
+    if (use_lut &&
+        (st = launch_lut_fc(true, false, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s)) !=
+            MOE_OK)
         return st;
     if (mma && (st = launch_mma_fc(true, t, sorted_pair, weights, k, mode, out, w, L, s)) != MOE_OK) return st;
     if (use_umma && (st = launch_umma(true, t, sorted_pair, weights, k, P, mode, out, w, L, s)) != MOE_OK) return st;
-    if (use_lut && (st = launch_lut_fc(false, t, x, sorted_pair, weights, k, mode, out, w, L, s)) != MOE_OK)
+    if (use_lut &&
+        (st = launch_lut_fc(false, false, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s)) !=
+            MOE_OK)
         return st;
     if (mma && (st = launch_mma_fc(false, t, sorted_pair, weights, k, mode, out, w, L, s)) != MOE_OK) return st;
     if (use_umma && (st = launch_umma(false, t, sorted_pair, weights, k, P, mode, out, w, L, s)) != MOE_OK) return st;

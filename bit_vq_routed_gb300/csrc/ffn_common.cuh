@@ -93,9 +93,9 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I)
     return L;
 }
 
-moe_status launch_lut_fc(bool fc1, const SlotTableHost* t, const uint16_t* x, const int32_t* sorted_pair,
-                         const float* weights, int k, int mode, float* out, char* ws, const WsLayout& L,
-                         cudaStream_t s);
+moe_status launch_lut_fc(bool fc1, bool self, const SlotTableHost* t, const uint16_t* x, const int32_t* offsets,
+                         const int32_t* sorted_pair, const float* weights, int k, int P, int mode, float* out,
+                         uint8_t* status, char* ws, const WsLayout& L, cudaStream_t s);
 moe_status launch_gather_f16(const uint16_t* x, const int32_t* sorted_pair, int k, int H, int P, uint16_t* x16s,
                              cudaStream_t s);
 moe_status launch_umma(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,

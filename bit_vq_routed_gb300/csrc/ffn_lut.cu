@@ -71,6 +71,12 @@ struct __align__(16) Smem {
     const void* sa[MAX_GROUP];  // matching scales
     const void* sb[MAX_GROUP];
     int ys[MAX_GROUP];          // FC2: sorted position of the pair
+    // single-token calls (no schedule kernel): every pair's buffers
+    const void* all_c[3][MAX_GROUP];
+    const void* all_s[3][MAX_GROUP];
+    int all_ys[MAX_GROUP];
+    int e_of_s[MAX_GROUP];
+    int n_self;
     int failed;
 };
 static_assert(0x400 + ((sizeof(Smem) + 127) / 128 * 128) + LOW_SLOTS * SLOT_BYTES <= TAB &&
@@ -125,9 +131,14 @@ __device__ __forceinline__ float row_sum(const UnitRegs& u, uint32_t lb) {
 // its share of the CTA's warps (ceil(LW / 4) warps).
 constexpr int MAX_REG = 16384 / (32 * ((LW + 3) / 4)) > 255 ? 255 : 16384 / (32 * ((LW + 3) / 4)) / 8 * 8;
 
-template <bool FC1>
+// SELF: a single-token call whose experts are all VQ2 (no schedule kernel):
+// the kernel lists the call's pairs itself from the expert offsets and the
+// slot table (one token group; pairs in sorted order, non-resident ones
+// reported and skipped).
+template <bool FC1, bool SELF>
 __global__ void __maxnreg__(MAX_REG)
-    ffn_lut_kernel(const uint16_t* __restrict__ codebook, const uint16_t* __restrict__ x,
+    ffn_lut_kernel(const SlotDesc* __restrict__ desc, const int32_t* __restrict__ offsets, int E, int P,
+                   uint8_t* __restrict__ status, const uint16_t* __restrict__ codebook, const uint16_t* __restrict__ x,
                    const int32_t* __restrict__ sorted_pair, const float* __restrict__ weights, int k, int H, int I,
                    int* __restrict__ header, const LutRec* __restrict__ recs,
                    const int2* __restrict__ fc1_range, const float* __restrict__ p1, float* __restrict__ pout,
@@ -169,7 +180,66 @@ __global__ void __maxnreg__(MAX_REG)
     // [per_pair*gs, per_pair*(gs+gc)), ordered (K-range, pair, row tile).
     int n_lut, u0, u1;
     bool waited = FC1;  // FC2 waits for FC1 once its first job's code copies are issued
-    if (FC1) {
+    // every job is RT units (SELF FC1: one token group of n_lut pairs, KR jobs
+    // of n_lut * RT units) -> the proportional split is direct
+    auto uniform_range = [&](int J, int job_units) {
+        const int U = J * job_units;
+        if (U == 0) {
+            u0 = u1 = 0;
+        } else if (J <= C) {
+            const int jb = (int)(((long long)(blockIdx.x + 1) * J - 1) / C);  // a0(jb) <= i < a0(jb + 1)
+            const int a0 = lut_cta_of((long long)jb * job_units, C, U);
+            const int a1 = lut_cta_of((long long)(jb + 1) * job_units, C, U);
+            const int n = a1 - a0, r = blockIdx.x - a0;
+            u0 = jb * job_units + (int)((long long)job_units * r / n);
+            u1 = jb * job_units + (int)((long long)job_units * (r + 1) / n);
+        } else {
+            u0 = (int)((long long)U * blockIdx.x / C);
+            u1 = (int)((long long)U * (blockIdx.x + 1) / C);
+        }
+    };
+    if (SELF) {
+        // FC1: the offsets come from the kernel just before (wait first); FC2:
+        // they are two kernels back (complete), so FC2 lists its pairs first.
+        if (FC1) {
+            pdl_wait();
+            pdl_launch_dependents();
+            if (blockIdx.x == 0 && tid == 0) *err = 0;  // this call's error word
+        }
+        int* s_off = reinterpret_cast<int*>(S.xs);  // (the inputs are built later)
+        for (int i = tid; i <= E; i += THREADS) s_off[i] = FC1 ? offsets[i] : __ldcg(offsets + i);
+        if (tid < MAX_GROUP) S.e_of_s[tid] = -1;
+        __syncthreads();
+        for (int e = tid; e < E; e += THREADS)  // the expert of each sorted position < P
+            for (int sp = max(s_off[e], 0); sp < min(s_off[e + 1], P); ++sp) S.e_of_s[sp] = e;
+        __syncthreads();
+        if (warp == 0) {
+            SlotDesc d;
+            d.resident = 0;
+            d.format = MOE_FMT_VQ2;
+            if (lane < P && S.e_of_s[lane] >= 0) d = desc[S.e_of_s[lane]];
+            const bool res = lane < P && d.resident != 0 && d.format == MOE_FMT_VQ2;
+            const unsigned mask = __ballot_sync(0xffffffffu, res);
+            const int idx = __popc(mask & ((1u << lane) - 1u));
+            if (res) {
+#pragma unroll
+                for (int mtx = 0; mtx < 3; ++mtx) {
+                    S.all_c[mtx][idx] = d.codes[mtx];
+                    S.all_s[mtx][idx] = d.scales[mtx];
+                }
+                S.all_ys[idx] = lane;
+            }
+            if (FC1 && blockIdx.x == 0 && lane < P) status[sorted_pair[lane]] = res ? 1 : 0;
+            if (lane == 0) S.n_self = __popc(mask);
+        }
+        __syncthreads();
+        n_lut = S.n_self;
+        uniform_range(FC1 ? KR : n_lut * KR, FC1 ? n_lut * RT : RT);
+        if (FC1) {
+            const int nc = n_lut * (H / 16);
+            for (int i = blockIdx.x * THREADS + tid; i < nc; i += C * THREADS) cnt[i] = 0;
+        }
+    } else if (FC1) {
         pdl_wait();
         // everything a dependent kernel may touch before its own wait is complete
         pdl_launch_dependents();
@@ -182,20 +252,9 @@ __global__ void __maxnreg__(MAX_REG)
         for (int i = blockIdx.x * THREADS + tid; i < nc; i += C * THREADS) cnt[i] = 0;
     } else {
         // The schedule is two kernels back, so complete: this CTA's units and
-        // their code bytes are known before FC1 completes.  FC2 jobs (pair,
-        // K-range) are all RT units, so the proportional split is direct.
+        // their code bytes are known before FC1 completes.
         n_lut = __ldcg(header + HDR_NLUT);
-        const int J = n_lut * KR, U = n_lut * per_pair;
-        if (J > 0 && J <= C) {
-            const int jb = (int)(((long long)(blockIdx.x + 1) * J - 1) / C);  // a0(jb) <= i < a0(jb + 1)
-            const int a0 = lut_cta_of((long long)jb * RT, C, U), a1 = lut_cta_of((long long)(jb + 1) * RT, C, U);
-            const int n = a1 - a0, r = blockIdx.x - a0;
-            u0 = jb * RT + RT * r / n;
-            u1 = jb * RT + RT * (r + 1) / n;
-        } else {
-            u0 = (int)((long long)U * blockIdx.x / C);
-            u1 = (int)((long long)U * (blockIdx.x + 1) / C);
-        }
+        uniform_range(n_lut * KR, RT);
     }
 
     const int b = lane_block(lane), m = lane & 3;  // scale block and group phase of this lane
@@ -208,9 +267,9 @@ __global__ void __maxnreg__(MAX_REG)
     while (u < u1) {
         __syncthreads();  // every warp is done with the previous table and pointers
         if (S.failed) break;
-        const LutRec& r0 = recs[u / per_pair];
-        const int gs = FC1 ? r0.gs : u / per_pair;
-        const int gc = FC1 ? r0.gc : 1;
+        const LutRec& r0 = recs[SELF ? 0 : u / per_pair];
+        const int gs = FC1 ? (SELF ? 0 : r0.gs) : u / per_pair;
+        const int gc = FC1 ? (SELF ? n_lut : r0.gc) : 1;
         const int kr = (u - per_pair * gs) / (RT * gc);
         const int job_start = per_pair * gs + kr * RT * gc;
         const int seg_end = min(u1, job_start + RT * gc);
@@ -218,15 +277,23 @@ __global__ void __maxnreg__(MAX_REG)
         const int nin = 128 * nkb;
         const bool active = b < nkb;
         if (tid < gc) {
-            const LutRec& r = recs[gs + tid];
-            S.pa[tid] = r.codes[FC1 ? 0 : 2];
-            S.sa[tid] = r.scales[FC1 ? 0 : 2];
-            S.pb[tid] = r.codes[1];
-            S.sb[tid] = r.scales[1];
-            S.ys[tid] = r.sorted;
+            if (SELF) {
+                S.pa[tid] = S.all_c[FC1 ? 0 : 2][gs + tid];
+                S.sa[tid] = S.all_s[FC1 ? 0 : 2][gs + tid];
+                S.pb[tid] = S.all_c[1][gs + tid];
+                S.sb[tid] = S.all_s[1][gs + tid];
+                S.ys[tid] = S.all_ys[gs + tid];
+            } else {
+                const LutRec& r = recs[gs + tid];
+                S.pa[tid] = r.codes[FC1 ? 0 : 2];
+                S.sa[tid] = r.scales[FC1 ? 0 : 2];
+                S.pb[tid] = r.codes[1];
+                S.sb[tid] = r.scales[1];
+                S.ys[tid] = r.sorted;
+            }
         }
         if (FC1) {  // the token's activations of this K-range
-            const int t = r0.token;
+            const int t = SELF ? 0 : r0.token;
             for (int i = tid; i < nin; i += THREADS)
                 S.xs[xs_at(i)] = __uint_as_float((uint32_t)x[(size_t)t * H + KR_IN * kr + i] << 16);
         }
@@ -510,20 +577,22 @@ __global__ void __maxnreg__(MAX_REG)
 
 }  // namespace
 
-moe_status launch_lut_fc(bool fc1, const SlotTableHost* t, const uint16_t* x, const int32_t* sorted_pair,
-                         const float* weights, int k, int mode, float* out, char* ws, const WsLayout& L,
-                         cudaStream_t s) {
+moe_status launch_lut_fc(bool fc1, bool self, const SlotTableHost* t, const uint16_t* x, const int32_t* offsets,
+                         const int32_t* sorted_pair, const float* weights, int k, int P, int mode, float* out,
+                         uint8_t* status, char* ws, const WsLayout& L, cudaStream_t s) {
     int* header = reinterpret_cast<int*>(ws);
     const LutRec* recs = reinterpret_cast<const LutRec*>(ws + L.rec_off);
     const int2* fc1_range = reinterpret_cast<const int2*>(ws + L.range_off);
     const float* p1 = reinterpret_cast<const float*>(ws + L.p1_off);
     float* pout = reinterpret_cast<float*>(ws + (fc1 ? L.p1_off : L.p2_off));
     int* cnt = reinterpret_cast<int*>(ws + L.cnt_off);
-    auto kern = fc1 ? ffn_lut_kernel<true> : ffn_lut_kernel<false>;
+    auto kern = self ? (fc1 ? ffn_lut_kernel<true, true> : ffn_lut_kernel<false, true>)
+                     : (fc1 ? ffn_lut_kernel<true, false> : ffn_lut_kernel<false, false>);
     cudaError_t e = ensure_smem_attr(kern, (int)DYN_SMEM);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: table kernel shared memory");
-    e = launch_pdl(kern, dim3((unsigned)num_sms()), dim3(THREADS), DYN_SMEM, s, t->codebook, x, sorted_pair, weights,
-                   k, t->H, t->I, header, recs, fc1_range, p1, pout, cnt, mode, out);
+    e = launch_pdl(kern, dim3((unsigned)num_sms()), dim3(THREADS), DYN_SMEM, s, (const SlotDesc*)t->d_desc, offsets,
+                   t->E, P, status, t->codebook, x, sorted_pair, weights, k, t->H, t->I, header, recs, fc1_range, p1,
+                   pout, cnt, mode, out);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: table kernel launch");
     MOE_LAUNCH_CHECK("moe_vq2_expert_ffn: table kernel launch");
     return MOE_OK;
