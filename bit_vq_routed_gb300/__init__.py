@@ -53,7 +53,7 @@ EXPORTED = [
     "moe_slot_table_set", "moe_slot_table_evict", "moe_slot_table_destroy", "moe_router_logits",
     "moe_route_topk", "moe_permute_workspace_size", "moe_permute",
     "moe_vq2_expert_ffn_workspace_size", "moe_vq2_expert_ffn", "moe_vq2_expert_ffn_noalloc", "moe_combine",
-    "moe_launch_count",
+    "moe_launch_count", "moe_route_workspace_size", "moe_route",
 ]
 
 
@@ -88,6 +88,8 @@ def load(path: Optional[str] = None, build_if_stale: bool = True):
         "moe_vq2_expert_ffn_noalloc": ([P, P, P, P, P, I, I, I, P, P, P], I),
         "moe_combine": ([P, P, P, P, I, I, I, P, P, P], I),
         "moe_launch_count": ([], ctypes.c_uint64),
+        "moe_route_workspace_size": ([I, I, I], Z),
+        "moe_route": ([P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, Z, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -238,10 +240,28 @@ def moe_combine(ypair, pair_to_sorted, weights, pair_status, k: int, out_f32=Non
                               H, _ptr(out_f32), _ptr(out_bf16), _stream(stream)))
 
 
-from .layer import GraphedForward, MoELayer, upload_layer  # noqa: E402  (the layer helper uses the functions above)
 
 
 def moe_launch_count() -> int:
     """Kernel launches the library has issued since it was loaded (a launch
     inside a stream capture counts once)."""
     return int(load().moe_launch_count())
+
+
+def moe_route_workspace_size(T: int, k: int, E: int) -> int:
+    return int(load().moe_route_workspace_size(T, k, E))
+
+
+def moe_route(x, w_router, bias, k: int, renormalize: int, logits, ids, weights, expert_offsets, sorted_pair,
+              pair_to_sorted, ws, stream=None):
+    """Router logits, top-k softmax and permutation in one call (one kernel
+    for small batches).  ws: a zero-filled device buffer of at least
+    moe_route_workspace_size bytes, left zeroed by the call."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    _check(load().moe_route(_ptr(x), _ptr(w_router), _ptr(bias), T, H, E, k, renormalize, _ptr(logits), _ptr(ids),
+                            _ptr(weights), _ptr(expert_offsets), _ptr(sorted_pair), _ptr(pair_to_sorted), _ptr(ws),
+                            ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
+
+
+from .layer import GraphedForward, MoELayer, upload_layer  # noqa: E402  (the layer helper uses the functions above)

@@ -184,6 +184,43 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k, int renormal
     return launch_route_topk(logits, T, E, k, renormalize, ids, weights, stream);
 }
 
+size_t moe_route_workspace_size(int T, int k, int E) {
+    (void)T;
+    (void)k;
+    (void)E;
+    return 256;
+}
+
+moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E, int k,
+                     int renormalize, float* logits, int32_t* ids, float* weights, int32_t* expert_offsets,
+                     int32_t* sorted_pair, int32_t* pair_to_sorted, void* ws, size_t ws_bytes,
+                     cudaStream_t stream) {
+    MOE_CHECK_ARG(T >= 0 && H > 0 && E > 0, "moe_route: T=%d H=%d E=%d", T, H, E);
+    MOE_CHECK_ARG(k >= 1 && k <= E && k <= 32, "moe_route: k=%d must be in [1, min(E, 32)]", k);
+    MOE_CHECK_SUPPORTED(E <= 1024, "moe_route: E=%d above 1024", E);
+    MOE_CHECK_ARG(renormalize == 0 || renormalize == 1, "moe_route: renormalize must be 0 or 1");
+    MOE_CHECK_SUPPORTED((long long)T * k <= (1 << 24), "moe_route: T*k above 2^24");
+    MOE_CHECK_ARG(expert_offsets, "moe_route: expert_offsets is null");
+    if (T == 0) return launch_permute(ids, 0, E, expert_offsets, sorted_pair, pair_to_sorted, stream);
+    MOE_CHECK_ARG(x && w_router && logits && ids && weights && sorted_pair && pair_to_sorted,
+                  "moe_route: null pointer");
+    MOE_CHECK_SUPPORTED(H % 256 == 0, "moe_route: H=%d must be a multiple of 256", H);
+    MOE_CHECK_SUPPORTED(aligned16(x) && aligned16(w_router) && aligned16(logits) && aligned16(bias),
+                        "moe_route: pointers must be 16-byte aligned");
+    if (route_fused_ok(T, k, H, E)) {
+        if (!ws || ws_bytes < moe_route_workspace_size(T, k, E)) {
+            set_error("moe_route: workspace of %zu bytes, %zu required", ws_bytes, moe_route_workspace_size(T, k, E));
+            return MOE_ERR_WORKSPACE;
+        }
+        return launch_route_fused(x, w_router, bias, T, H, E, k, renormalize, logits, ids, weights, expert_offsets,
+                                  sorted_pair, pair_to_sorted, static_cast<int*>(ws), stream);
+    }
+    moe_status st = launch_router_logits(x, w_router, bias, logits, T, H, E, stream);
+    if (st != MOE_OK) return st;
+    if ((st = launch_route_topk(logits, T, E, k, renormalize, ids, weights, stream)) != MOE_OK) return st;
+    return launch_permute(ids, T * k, E, expert_offsets, sorted_pair, pair_to_sorted, stream);
+}
+
 size_t moe_permute_workspace_size(int T, int k, int E) {
     (void)T;
     (void)k;

@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
                                                         Chunk* __restrict__ chunks, LutRec* __restrict__ recs,
                                                         int32_t* __restrict__ grp_start, int use_lut,
                                                         Chunk* __restrict__ uchunks, int use_umma, int H, int I,
-                                                        int C, int2* __restrict__ fc1_range) {
+                                                        int C, int4* __restrict__ fc1_range) {
     __shared__ unsigned long long warp_tot[33];
     __shared__ int s_off[1025];
     __shared__ __align__(16) int s_tok[1024];  // token of each table pair, by expert (INT_MAX otherwise)
@@ -179,22 +179,18 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
         __syncthreads();
         ok = __syncthreads_and(!ok || tid >= J || s_a[tid + 1] > s_a[tid]) && ok;
         if (tid < C) {
-            int u0, u1;
+            int4 rg;  // (u0, u1, first offset, stride): one job, its CTAs interleaved
             if (ok) {
                 int lo = 0, hi = J;  // the job j with s_a[j] <= tid < s_a[j+1]
                 while (hi - lo > 1) {
                     const int mid = (lo + hi) >> 1;
                     if (s_a[mid] <= tid) lo = mid; else hi = mid;
                 }
-                const int st0 = start(lo), st1 = lo + 1 < J ? start(lo + 1) : U;
-                const int n = s_a[lo + 1] - s_a[lo], r = tid - s_a[lo];
-                u0 = st0 + (int)((long long)(st1 - st0) * r / n);
-                u1 = st0 + (int)((long long)(st1 - st0) * (r + 1) / n);
-            } else {
-                u0 = (int)((long long)U * tid / C);
-                u1 = (int)((long long)U * (tid + 1) / C);
+                rg = make_int4(start(lo), lo + 1 < J ? start(lo + 1) : U, tid - s_a[lo], s_a[lo + 1] - s_a[lo]);
+            } else {  // a contiguous range of units (over jobs)
+                rg = make_int4((int)((long long)U * tid / C), (int)((long long)U * (tid + 1) / C), 0, 0);
             }
-            fc1_range[tid] = make_int2(u0, u1);
+            fc1_range[tid] = rg;
         }
     }
     if (tid == 0) {
@@ -258,7 +254,7 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     }
     cudaError_t e = launch_pdl(schedule_kernel, dim3(1), dim3(1024), 0, s, (const SlotDesc*)t->d_desc, E, offsets,
                                sorted_pair, P, k, status, header, chunks, recs, grp_start, use_lut,
-                               uchunks, use_umma, H, I, num_sms(), reinterpret_cast<int2*>(w + L.range_off));
+                               uchunks, use_umma, H, I, num_sms(), reinterpret_cast<int4*>(w + L.range_off));
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule launch");
     if ((mma || use_umma) && (st = launch_gather_f16(x, sorted_pair, k, H, P, x16s, s)) != MOE_OK) return st;
     if (use_lut &&

@@ -80,7 +80,7 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I)
     L.cnt_off = o;
     o = ws_align(o + sizeof(int32_t) * (size_t)L.max_lut * (H / 16));
     L.range_off = o;
-    o = ws_align(o + sizeof(int2) * (size_t)MAX_LUT_CTAS);
+    o = ws_align(o + sizeof(int4) * (size_t)MAX_LUT_CTAS);
     const bool umma = T >= UMMA_MIN;
     L.max_uchunks = umma ? (int)(P / UMMA_NT + E) : 0;
     L.uchunks_off = o;

@@ -62,23 +62,24 @@ constexpr uint32_t HIGH_BASE = TAB + 2 * PLANE;
 __device__ __forceinline__ int xs_at(int i) { return i + 4 * (i >> 7); }
 
 struct __align__(16) Smem {
-    unsigned long long full[NSLOT];  // slot mbarriers (one arrival + the copied bytes)
-    float xs[KR_IN + KR_IN / 32];
-    uint8_t lastf[256];  // FC2: the row tiles whose partials this CTA adds up
-    float cb[128 * 4];
+    unsigned long long full[NSLOT];        // slot mbarriers (one arrival + the copied bytes)
+    alignas(16) float xs[KR_IN + KR_IN / 32];  // (read as float4)
+    alignas(16) float cb[128 * 4];         // (read as float4)
     const void* pa[MAX_GROUP];  // per pair of the current group: FC1 gate / FC2 down codes
     const void* pb[MAX_GROUP];  // FC1 up codes
     const void* sa[MAX_GROUP];  // matching scales
     const void* sb[MAX_GROUP];
-    int ys[MAX_GROUP];          // FC2: sorted position of the pair
     // single-token calls (no schedule kernel): every pair's buffers
     const void* all_c[3][MAX_GROUP];
     const void* all_s[3][MAX_GROUP];
+    int ys[MAX_GROUP];          // FC2: sorted position of the pair
     int all_ys[MAX_GROUP];
     int e_of_s[MAX_GROUP];
+    uint8_t lastf[256];         // FC2: the row tiles whose partials this CTA adds up
     int n_self;
     int failed;
 };
+static_assert(offsetof(Smem, xs) % 16 == 0 && offsetof(Smem, cb) % 16 == 0, "float4 reads of xs and cb");
 static_assert(0x400 + ((sizeof(Smem) + 127) / 128 * 128) + LOW_SLOTS * SLOT_BYTES <= TAB &&
                   HIGH_BASE + (NSLOT - LOW_SLOTS) * SLOT_BYTES <= 0x400 + DYN_SMEM && NSLOT >= LOW_SLOTS,
               "shared layout");
@@ -141,7 +142,7 @@ __global__ void __maxnreg__(MAX_REG)
                    uint8_t* __restrict__ status, const uint16_t* __restrict__ codebook, const uint16_t* __restrict__ x,
                    const int32_t* __restrict__ sorted_pair, const float* __restrict__ weights, int k, int H, int I,
                    int* __restrict__ header, const LutRec* __restrict__ recs,
-                   const int2* __restrict__ fc1_range, const float* __restrict__ p1, float* __restrict__ pout,
+                   const int4* __restrict__ fc1_range, const float* __restrict__ p1, float* __restrict__ pout,
                    int* __restrict__ cnt, int mode, float* __restrict__ out) {
     extern __shared__ __align__(1024) uint8_t dyn[];
     Smem& S = *reinterpret_cast<Smem*>(dyn);
@@ -178,7 +179,11 @@ __global__ void __maxnreg__(MAX_REG)
     // groups are single pairs (the table depends on the pair's silu(g)*u).
     // A group of gc pairs starting at table pair gs owns the units
     // [per_pair*gs, per_pair*(gs+gc)), ordered (K-range, pair, row tile).
-    int n_lut, u0, u1;
+    // A CTA's work: units [u0, u1) in job order; with s_step > 0 (no more jobs
+    // than CTAs) a single job of which it takes the units s_off0 + s_step * i,
+    // the job's CTAs interleaved, so that every CTA meets the same mix of
+    // pairs and rows.
+    int n_lut, u0, u1, s_off0 = 0, s_step = 0;
     bool waited = FC1;  // FC2 waits for FC1 once its first job's code copies are issued
     // every job is RT units (SELF FC1: one token group of n_lut pairs, KR jobs
     // of n_lut * RT units) -> the proportional split is direct
@@ -190,9 +195,10 @@ __global__ void __maxnreg__(MAX_REG)
             const int jb = (int)(((long long)(blockIdx.x + 1) * J - 1) / C);  // a0(jb) <= i < a0(jb + 1)
             const int a0 = lut_cta_of((long long)jb * job_units, C, U);
             const int a1 = lut_cta_of((long long)(jb + 1) * job_units, C, U);
-            const int n = a1 - a0, r = blockIdx.x - a0;
-            u0 = jb * job_units + (int)((long long)job_units * r / n);
-            u1 = jb * job_units + (int)((long long)job_units * (r + 1) / n);
+            u0 = jb * job_units;
+            u1 = u0 + job_units;
+            s_off0 = blockIdx.x - a0;
+            s_step = a1 - a0;
         } else {
             u0 = (int)((long long)U * blockIdx.x / C);
             u1 = (int)((long long)U * (blockIdx.x + 1) / C);
@@ -244,9 +250,11 @@ __global__ void __maxnreg__(MAX_REG)
         // everything a dependent kernel may touch before its own wait is complete
         pdl_launch_dependents();
         n_lut = header[HDR_NLUT];
-        const int2 rg = fc1_range[blockIdx.x];  // computed by the schedule
+        const int4 rg = fc1_range[blockIdx.x];  // computed by the schedule
         u0 = rg.x;
         u1 = rg.y;
+        s_off0 = rg.z;
+        s_step = rg.w;
         // FC2's arrival counters start at zero
         const int nc = n_lut * (H / 16);
         for (int i = blockIdx.x * THREADS + tid; i < nc; i += C * THREADS) cnt[i] = 0;
@@ -310,14 +318,23 @@ __global__ void __maxnreg__(MAX_REG)
             c.rt = off - c.pi * RT;
             return c;
         };
+        // this CTA's units of the job: offsets v_first + v_inc * i < v_end;
+        // warp w takes i = w, w + LW, ...
+        const int v_first = s_step ? s_off0 : u - job_start, v_inc = s_step ? s_step : 1;
+        const int v_end = s_step ? RT * gc : seg_end - job_start;
+        const int vstep = v_inc * LW;
+        int v0 = v_first + v_inc * warp;
         auto advance = [&](Cur c) {
-            c.rt += LW;
+            c.rt += vstep;
             while (c.rt >= RT) {
                 c.rt -= RT;
                 ++c.pi;
             }
             return c;
         };
+        Cur c0 = cur_at(v0);              // the unit computed next
+        Cur c1 = advance(c0);             // the one after it
+        Cur c2 = advance(c1);
         auto unit_ptrs = [&](Cur cu, const uint8_t*& c, const uint16_t*& sp) {
             const bool second = FC1 && cu.rt >= I / 16;  // an up-matrix row tile
             const int rtm = second ? cu.rt - I / 16 : cu.rt;
@@ -348,12 +365,8 @@ __global__ void __maxnreg__(MAX_REG)
                 asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c), "r"(512u * nkb) : "memory");
             }
         };
-        int v = u + warp;
-        Cur c0 = cur_at(v - job_start);   // the unit computed next
-        Cur c1 = advance(c0);             // the one after it
-        Cur c2 = advance(c1);
-        if (v < seg_end) issue(c0);
-        if (v + LW < seg_end) prefetch(c1);
+        if (v0 < v_end) issue(c0);
+        if (v0 + vstep < v_end) prefetch(c1);
 
         if (!waited) {
             pdl_wait();
@@ -499,7 +512,7 @@ __global__ void __maxnreg__(MAX_REG)
         // This warp's units of the job: v, v + LW, ...  The slot is copied to
         // registers and handed to the copy of the next unit (the one after
         // that is asked of L2), then the unit is computed from registers.
-        for (; v < seg_end; v += LW) {
+        for (; v0 < v_end; v0 += vstep) {
             if (!mbar_wait_bounded(bar, phase, err, MOE_DEVERR_WAIT_FULL)) {
                 ok = false;
                 break;
@@ -517,8 +530,8 @@ __global__ void __maxnreg__(MAX_REG)
             __syncwarp();
             // the generic-proxy reads of the slot come before the next copy's writes
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            if (v + LW < seg_end) issue(c1);
-            if (v + 2 * LW < seg_end) prefetch(c2);
+            if (v0 + vstep < v_end) issue(c1);
+            if (v0 + 2 * vstep < v_end) prefetch(c2);
             compute_store(r, c0);
             c0 = c1;
             c1 = c2;
@@ -539,10 +552,11 @@ __global__ void __maxnreg__(MAX_REG)
             __syncthreads();
             const int pr = gs;  // FC2 groups are single pairs
             const int s = S.ys[0];
-            for (int tb = u - job_start; tb < seg_end - job_start; tb += 256) {
-                const int nt = min(256, seg_end - job_start - tb);
+            const int n_my = (v_end - v_first + v_inc - 1) / v_inc;  // this CTA's row tiles
+            for (int tb = 0; tb < n_my; tb += 256) {
+                const int nt = min(256, n_my - tb);
                 for (int t = tid; t < nt; t += THREADS) {
-                    int* c = cnt + (size_t)pr * RT + tb + t;
+                    int* c = cnt + (size_t)pr * RT + v_first + v_inc * (tb + t);
                     const bool last = atomicAdd(c, 1) == KR - 1;
                     S.lastf[t] = last;
                     if (last) *c = 0;
@@ -553,7 +567,7 @@ __global__ void __maxnreg__(MAX_REG)
                 for (int idx = tid; idx < 16 * nt; idx += THREADS) {
                     const int t = idx >> 4;
                     if (!S.lastf[t]) continue;
-                    const int h = (tb + t) * 16 + (idx & 15);
+                    const int h = (v_first + v_inc * (tb + t)) * 16 + (idx & 15);
                     const float* src = pout + (size_t)pr * KR * R + h;
                     float y = __ldcg(src);
                     for (int jj = 1; jj < KR; ++jj) y += __ldcg(src + (size_t)jj * R);
@@ -582,7 +596,7 @@ moe_status launch_lut_fc(bool fc1, bool self, const SlotTableHost* t, const uint
                          uint8_t* status, char* ws, const WsLayout& L, cudaStream_t s) {
     int* header = reinterpret_cast<int*>(ws);
     const LutRec* recs = reinterpret_cast<const LutRec*>(ws + L.rec_off);
-    const int2* fc1_range = reinterpret_cast<const int2*>(ws + L.range_off);
+    const int4* fc1_range = reinterpret_cast<const int4*>(ws + L.range_off);
     const float* p1 = reinterpret_cast<const float*>(ws + L.p1_off);
     float* pout = reinterpret_cast<float*>(ws + (fc1 ? L.p1_off : L.p2_off));
     int* cnt = reinterpret_cast<int*>(ws + L.cnt_off);

@@ -243,6 +243,212 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     }
 }
 
+
+// Whole routing of a small batch in one launch (the three steps above,
+// bit for bit): CTA (e8, t) computes the logits of token t for 8 experts as
+// router_logits_small_kernel does; the CTA that finishes last (a counter in
+// the caller's workspace, back at zero afterwards) then runs the top-k +
+// softmax of every token (route_topk_kernel's rounds, one warp per token) and
+// the stable counting sort of the pairs by expert (moe_permute's order) on
+// its 256 threads.  Shared memory: the token's activations, then ids[P],
+// cursor[E] and per-warp counts wcnt[8][E].
+template <int NPER>
+__global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __restrict__ x,
+                                                          const uint16_t* __restrict__ w,
+                                                          const float* __restrict__ bias, int T, int H, int E,
+                                                          int k, int renorm, float* __restrict__ logits,
+                                                          int32_t* __restrict__ ids, float* __restrict__ weights,
+                                                          int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ sorted_pair,
+                                                          int32_t* __restrict__ pair_to_sorted,
+                                                          int* __restrict__ counter) {
+    extern __shared__ __align__(16) uint4 xs[];
+    __shared__ int s_last;
+    const int t = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int e = blockIdx.x * 8 + warp;
+    const int nch = H / 8;
+    const int per = H / 256;
+    constexpr int U = 16;
+    const uint4* wr = reinterpret_cast<const uint4*>(w + (size_t)min(e, E - 1) * H);
+    uint4 wv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (u < per) wv[u] = __ldg(wr + lane + 32 * u);
+    pdl_wait();
+    pdl_launch_dependents();  // dependents may start their prologues now
+    for (int i = tid; i < nch; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(x + (size_t)t * H)[i];
+    __syncthreads();
+    if (e < E) {
+        float acc = 0.0f;
+        for (int m0 = 0; m0 < per; m0 += U) {
+            if (m0 > 0) {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (m0 + u < per) wv[u] = __ldg(wr + lane + 32 * (m0 + u));
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (m0 + u < per) {
+                    float xf[8], wf[8];
+                    unpack_bf16x8(xs[lane + 32 * (m0 + u)], xf);
+                    unpack_bf16x8(wv[u], wf);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, __fmul_rn(xf[i], wf[i]));
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(FULL, acc, off));
+        if (lane == 0) logits[(size_t)t * E + e] = bias ? __fadd_rn(acc, bias[e]) : acc;
+    }
+    // the last CTA to finish goes on
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int n = gridDim.x * gridDim.y;
+        s_last = atomicAdd(counter, 1) == n - 1;
+        if (s_last) *counter = 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    const int P = T * k;
+    int32_t* s_ids = reinterpret_cast<int32_t*>(xs);  // (the activations are done with)
+    int32_t* cursor = s_ids + P;
+    int32_t* wcnt = cursor + E;
+    // top-k + softmax, one warp per token
+    for (int tt = warp; tt < T; tt += 8) {
+        const float* l = logits + (size_t)tt * E;
+        float v[NPER];
+        uint32_t taken = 0;
+#pragma unroll
+        for (int i = 0; i < NPER; ++i) {
+            const int ee = lane + 32 * i;
+            if (ee < E) {
+                v[i] = __ldcg(l + ee);
+            } else {
+                v[i] = -INFINITY;
+                taken |= 1u << i;
+            }
+        }
+        float bv = -INFINITY;
+        int be = INT_MAX;
+        auto rescan = [&]() {
+            bv = -INFINITY;
+            be = INT_MAX;
+#pragma unroll
+            for (int i = 0; i < NPER; ++i) {
+                const int ee = lane + 32 * i;
+                if (!((taken >> i) & 1) && better(v[i], ee, bv, be)) {
+                    bv = v[i];
+                    be = ee;
+                }
+            }
+        };
+        rescan();
+        float sel_v = 0.0f;
+        int sel_e = 0;
+        for (int j = 0; j < k; ++j) {
+            float wv2 = bv;
+            int we = be;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                const float ov = __shfl_xor_sync(FULL, wv2, off);
+                const int oe = __shfl_xor_sync(FULL, we, off);
+                if (better(ov, oe, wv2, we)) {
+                    wv2 = ov;
+                    we = oe;
+                }
+            }
+            if (lane == j) {
+                sel_v = wv2;
+                sel_e = we;
+            }
+            if ((we & 31) == lane) {
+                taken |= 1u << (we >> 5);
+                rescan();
+            }
+        }
+        const float top = __shfl_sync(FULL, sel_v, 0);
+        const float num = lane < k ? expf(sel_v - top) : 0.0f;
+        float den = 0.0f;
+        if (renorm) {
+            den = num;
+        } else {
+#pragma unroll
+            for (int i = 0; i < NPER; ++i)
+                if (lane + 32 * i < E) den += expf(v[i] - top);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(FULL, den, off);
+        if (lane < k) {
+            ids[(size_t)tt * k + lane] = sel_e;
+            weights[(size_t)tt * k + lane] = num / den;
+            s_ids[tt * k + lane] = sel_e;
+        }
+    }
+    for (int i = tid; i < E * 9; i += blockDim.x) cursor[i] = 0;  // cursor and wcnt
+    __syncthreads();
+    // histogram, exclusive scan (4 entries per thread), stable scatter
+    for (int p = tid; p < P; p += blockDim.x) atomicAdd(&cursor[s_ids[p]], 1);
+    __syncthreads();
+    __shared__ int warp_tot[8];
+    int c4[4], run = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int ee = 4 * tid + q;
+        c4[q] = ee < E ? cursor[ee] : 0;
+        run += c4[q];
+    }
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(FULL, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w2 = 0; w2 < warp; ++w2) before += warp_tot[w2];
+    int ex = incl - run + before;
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int ee = 4 * tid + q;
+        if (ee < E) {
+            offsets[ee] = ex;
+            cursor[ee] = ex;
+        }
+        ex += c4[q];
+    }
+    if (tid == 0) offsets[E] = P;
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base0 = 0; base0 < P; base0 += 256) {
+        const int p = base0 + tid;
+        const bool valid = p < P;
+        const int ee = valid ? s_ids[p] : -1;
+        const unsigned peers = __match_any_sync(FULL, ee);
+        const int rank = __popc(peers & lt);
+        const bool leader = (__ffs(peers) - 1) == lane;
+        if (valid && leader) wcnt[warp * E + ee] = __popc(peers);
+        __syncthreads();
+        if (valid) {
+            int pre = 0;
+            for (int w2 = 0; w2 < warp; ++w2) pre += wcnt[w2 * E + ee];
+            const int pos = cursor[ee] + pre + rank;
+            sorted_pair[pos] = p;
+            pair_to_sorted[p] = pos;
+        }
+        __syncthreads();
+        if (valid && leader) {  // (leaders of several warps may share an expert)
+            atomicAdd(&cursor[ee], __popc(peers));
+            wcnt[warp * E + ee] = 0;
+        }
+        __syncthreads();
+    }
+}
 }  // namespace
 
 moe_status launch_router_logits(const uint16_t* x, const uint16_t* w, const float* bias, float* logits,
@@ -276,6 +482,33 @@ moe_status launch_route_topk(const float* logits, int T, int E, int k, int renor
     cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(threads), 0, s, logits, T, E, k, renorm, ids, weights);
     if (e != cudaSuccess) return cuda_status(e, "moe_route_topk: launch");
     MOE_LAUNCH_CHECK("moe_route_topk: launch");
+    return MOE_OK;
+}
+
+size_t route_fused_smem(int T, int k, int H, int E) {
+    const size_t act = (size_t)H * 2;
+    const size_t tail = sizeof(int32_t) * ((size_t)T * k + (size_t)E * 9);
+    return act > tail ? act : tail;
+}
+
+bool route_fused_ok(int T, int k, int H, int E) {
+    return T >= 1 && T <= 64 && (long long)T * k <= 1024 && E <= 1024 && route_fused_smem(T, k, H, E) <= 48 * 1024;
+}
+
+moe_status launch_route_fused(const uint16_t* x, const uint16_t* w, const float* bias, int T, int H, int E, int k,
+                              int renorm, float* logits, int32_t* ids, float* weights, int32_t* offsets,
+                              int32_t* sorted_pair, int32_t* pair_to_sorted, int* counter, cudaStream_t s) {
+    auto kern = E <= 32    ? route_fused_kernel<1>
+                : E <= 64  ? route_fused_kernel<2>
+                : E <= 128 ? route_fused_kernel<4>
+                : E <= 256 ? route_fused_kernel<8>
+                : E <= 512 ? route_fused_kernel<16>
+                           : route_fused_kernel<32>;
+    dim3 grid((unsigned)((E + 7) / 8), (unsigned)T);
+    cudaError_t e = launch_pdl(kern, grid, dim3(256), route_fused_smem(T, k, H, E), s, x, w, bias, T, H, E, k, renorm,
+                               logits, ids, weights, offsets, sorted_pair, pair_to_sorted, counter);
+    if (e != cudaSuccess) return cuda_status(e, "moe_route: launch");
+    MOE_LAUNCH_CHECK("moe_route: launch");
     return MOE_OK;
 }
 

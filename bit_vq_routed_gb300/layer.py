@@ -1,9 +1,9 @@
 """One routed-expert MoE layer on the device: the buffers it needs and the
 sequence of library calls of one forward pass.
 
-    logits = router(x)                  moe_router_logits
-    ids, w = top-k softmax(logits)      moe_route_topk
-    permutation by expert               moe_permute
+    logits = router(x)                  moe_router_logits  \
+    ids, w = top-k softmax(logits)      moe_route_topk      > moe_route (one kernel
+    permutation by expert               moe_permute        /  for small batches)
     y per (token, expert) pair          moe_vq2_expert_ffn (per-pair mode)
     out = sum_j w * y                   moe_combine
 
@@ -18,8 +18,8 @@ import numpy as np
 import torch
 
 from . import (MOE_FMT_FP4, MOE_FMT_VQ2, MOE_FUSED_SCATTER, MOE_PER_PAIR, SlotTable, moe_combine,
-               moe_fp4_pack, moe_permute, moe_route_topk, moe_router_logits, moe_vq2_expert_ffn,
-               moe_vq2_expert_ffn_workspace_size)
+               moe_fp4_pack, moe_permute, moe_route, moe_route_topk, moe_route_workspace_size, moe_router_logits,
+               moe_vq2_expert_ffn, moe_vq2_expert_ffn_workspace_size)
 
 
 def _dev(a, dtype=None, device="cuda"):
@@ -74,6 +74,8 @@ class MoELayer:
         self.out = torch.empty(T_max, H, dtype=f32, device=device)
         self.ws = torch.empty(moe_vq2_expert_ffn_workspace_size(T_max, k, E, H, I), dtype=torch.uint8,
                               device=device)
+        # (zero-filled once; moe_route leaves its counter at zero)
+        self.route_ws = torch.zeros(moe_route_workspace_size(T_max, k, E), dtype=torch.uint8, device=device)
 
     def set_expert(self, e: int, fmt: int, packed_codes, packed_scales, stream=None):
         self.table.set(e, fmt, packed_codes, packed_scales, stream)
@@ -82,6 +84,13 @@ class MoELayer:
         self.table.evict(e, stream)
 
     def route(self, x, stream=None):
+        T = x.shape[0]
+        moe_route(x, self.w_router, self.bias, self.k, self.renormalize, self.logits[:T], self.ids[:T],
+                  self.weights[:T], self.offsets, self.sorted_pair[:T * self.k], self.pair_to_sorted[:T * self.k],
+                  self.route_ws, stream)
+
+    def route_stepwise(self, x, stream=None):
+        """The same routing as route() through the three separate calls."""
         T = x.shape[0]
         moe_router_logits(x, self.w_router, self.bias, self.logits[:T], stream)
         moe_route_topk(self.logits[:T], self.k, self.renormalize, self.ids[:T], self.weights[:T], stream)

@@ -168,6 +168,22 @@ moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_
                        int32_t* sorted_pair, int32_t* pair_to_sorted, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
 
+/* The whole routing in one call: moe_router_logits, moe_route_topk and
+ * moe_permute of the same arguments, with the same outputs bit for bit
+ * (logits, ids, weights, expert_offsets, sorted_pair, pair_to_sorted).  For
+ * small batches (T <= 64, T*k <= 1024, E <= 1024) it is one kernel launch:
+ * the CTA that finishes its share of the logits last does the top-k and the
+ * permutation (fewer kernel boundaries per layer at decode); otherwise it
+ * enqueues the three steps.
+ * ws: moe_route_workspace_size() bytes of device memory holding a counter;
+ * zero-fill it once before the first call (each call leaves it at zero).
+ * Calls that share a workspace must not overlap on the GPU. */
+size_t moe_route_workspace_size(int T, int k, int E);
+moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E,
+                     int k, int renormalize, float* logits, int32_t* ids, float* weights,
+                     int32_t* expert_offsets, int32_t* sorted_pair, int32_t* pair_to_sorted, void* ws,
+                     size_t ws_bytes, cudaStream_t stream);
+
 /* Expert FFN over the resident experts (Tandem-vLLM page, "How it works";
  * vLLM-Moet page, "Qwen3.8": silu*up fused into the MoE GEMV): for every
  * pair p routed to a resident expert e,

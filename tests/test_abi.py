@@ -107,3 +107,21 @@ def test_launch_count_ignores_rejected_calls(lib):
     assert lib.moe_route_topk(P(16), 4, 8, 0, 1, P(16), P(16), None) == bv.MOE_ERR_INVALID_ARG
     assert lib.moe_router_logits(None, None, None, None, 0, 256, 8, None) == bv.MOE_OK
     assert bv.moe_launch_count() == before
+
+
+def test_route_rejects_bad_args(lib):
+    P = ctypes.c_void_p
+    assert lib.moe_route_workspace_size(1, 8, 256) >= 4
+    args = [P(16), P(16), None, 1, 256, 8, 2, 1, P(16), P(16), P(16), P(16), P(16), P(16), P(16), 256, None]
+    bad_k = list(args)
+    bad_k[6] = 0
+    assert lib.moe_route(*bad_k) == bv.MOE_ERR_INVALID_ARG
+    bad_h = list(args)
+    bad_h[4] = 100
+    assert lib.moe_route(*bad_h) == bv.MOE_ERR_UNSUPPORTED
+    no_ws = list(args)
+    no_ws[14], no_ws[15] = None, 0
+    assert lib.moe_route(*no_ws) == bv.MOE_ERR_WORKSPACE
+    null_x = list(args)
+    null_x[0] = None
+    assert lib.moe_route(*null_x) == bv.MOE_ERR_INVALID_ARG
