@@ -379,7 +379,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16*f16->f32 (bf16 activations)",
         "data": "synthetic (seeded; random weights, no trained checkpoint)", "config": config,
-        "roofline": {"bound": "hbm", "kernel": "moe_vq2_expert_ffn (schedule + FC1 + FC2 launches)",
+        "roofline": {"bound": "hbm", "kernel": "moe_vq2_expert_ffn (its kernels: the two table kernels at one token)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)", "traffic": None,
                      "algorithmic_bytes_per_launch": bytes_avg, "avg_launch_ms": ffn_avg_ms},

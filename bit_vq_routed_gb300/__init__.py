@@ -53,7 +53,7 @@ EXPORTED = [
     "moe_slot_table_set", "moe_slot_table_evict", "moe_slot_table_destroy", "moe_router_logits",
     "moe_route_topk", "moe_permute_workspace_size", "moe_permute",
     "moe_vq2_expert_ffn_workspace_size", "moe_vq2_expert_ffn", "moe_vq2_expert_ffn_noalloc", "moe_combine",
-    "moe_launch_count", "moe_route_workspace_size", "moe_route",
+    "moe_launch_count", "moe_route_workspace_size", "moe_route", "moe_vq2_expert_ffn_combine",
 ]
 
 
@@ -90,6 +90,7 @@ def load(path: Optional[str] = None, build_if_stale: bool = True):
         "moe_launch_count": ([], ctypes.c_uint64),
         "moe_route_workspace_size": ([I, I, I], Z),
         "moe_route": ([P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, Z, P], I),
+        "moe_vq2_expert_ffn_combine": ([P, P, P, P, P, P, I, I, P, P, P, P, P, Z, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -262,6 +263,18 @@ def moe_route(x, w_router, bias, k: int, renormalize: int, logits, ids, weights,
     _check(load().moe_route(_ptr(x), _ptr(w_router), _ptr(bias), T, H, E, k, renormalize, _ptr(logits), _ptr(ids),
                             _ptr(weights), _ptr(expert_offsets), _ptr(sorted_pair), _ptr(pair_to_sorted), _ptr(ws),
                             ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
+
+
+def moe_vq2_expert_ffn_combine(table: "SlotTable", x, expert_offsets, sorted_pair, pair_to_sorted, weights, k: int,
+                               ypair, pair_status, out_f32=None, out_bf16=None, ws=None, stream=None):
+    """moe_vq2_expert_ffn (per-pair mode) and then moe_combine in one call
+    (for single-token calls the combine runs inside the expert kernels)."""
+    T = x.shape[0]
+    _check(load().moe_vq2_expert_ffn_combine(table.handle, _ptr(x), _ptr(expert_offsets), _ptr(sorted_pair),
+                                             _ptr(pair_to_sorted), _ptr(weights), T, k, _ptr(ypair),
+                                             _ptr(pair_status), _ptr(out_f32), _ptr(out_bf16), _ptr(ws),
+                                             ws.numel() * ws.element_size() if ws is not None else 0,
+                                             _stream(stream)))
 
 
 from .layer import GraphedForward, MoELayer, upload_layer  # noqa: E402  (the layer helper uses the functions above)

@@ -270,6 +270,32 @@ moe_status moe_vq2_expert_ffn(const moe_slot_table* table, const uint16_t* x,
                              out_or_ypair, pair_status, ws, ws_bytes, stream);
 }
 
+moe_status moe_vq2_expert_ffn_combine(const moe_slot_table* table, const uint16_t* x,
+                                      const int32_t* expert_offsets, const int32_t* sorted_pair,
+                                      const int32_t* pair_to_sorted, const float* weights, int T, int k,
+                                      float* ypair, uint8_t* pair_status, float* out_f32, uint16_t* out_bf16,
+                                      void* ws, size_t ws_bytes, cudaStream_t stream) {
+    MOE_CHECK_ARG(table, "moe_vq2_expert_ffn_combine: null table");
+    MOE_CHECK_ARG(T >= 0 && k >= 1, "moe_vq2_expert_ffn_combine: T=%d k=%d", T, k);
+    long long P = (long long)T * k;
+    MOE_CHECK_SUPPORTED(P <= (1 << 24), "moe_vq2_expert_ffn_combine: T*k=%lld above 2^24", P);
+    MOE_CHECK_SUPPORTED(T <= 65535, "moe_vq2_expert_ffn_combine: T=%d above 65535", T);
+    if (P == 0) return MOE_OK;
+    MOE_CHECK_ARG(x && expert_offsets && sorted_pair && pair_to_sorted && weights && ypair && pair_status,
+                  "moe_vq2_expert_ffn_combine: null pointer");
+    MOE_CHECK_ARG(out_f32 || out_bf16, "moe_vq2_expert_ffn_combine: both outputs are null");
+    MOE_CHECK_SUPPORTED(aligned16(x) && aligned16(ypair) && aligned16(ws) && aligned16(out_f32) &&
+                            aligned16(out_bf16),
+                        "moe_vq2_expert_ffn_combine: x, ypair, outputs and ws must be 16-byte aligned");
+    size_t need = ffn_workspace_size(T, k, table->h.E, table->h.H, table->h.I);
+    if (!ws || ws_bytes < need) {
+        set_error("moe_vq2_expert_ffn_combine: workspace %zu bytes, need %zu", ws_bytes, need);
+        return MOE_ERR_WORKSPACE;
+    }
+    return launch_expert_ffn(&table->h, x, expert_offsets, sorted_pair, weights, T, k, MOE_PER_PAIR, ypair,
+                             pair_status, ws, ws_bytes, stream, pair_to_sorted, out_f32, out_bf16);
+}
+
 moe_status moe_combine(const float* ypair, const int32_t* pair_to_sorted, const float* weights,
                        const uint8_t* pair_status, int T, int k, int H, float* out_f32,
                        uint16_t* out_bf16, cudaStream_t stream) {

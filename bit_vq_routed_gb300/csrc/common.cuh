@@ -274,9 +274,13 @@ moe_status launch_fp4_pack(const uint8_t* codes, const uint8_t* scales, int rows
                            uint8_t* ps, cudaStream_t s);
 moe_status launch_slot_set(SlotDesc* table, int expert_id, SlotDesc d, cudaStream_t s);
 size_t ffn_workspace_size(int T, int k, int E, int H, int I);
+// With comb32 / comb16 (mode MOE_PER_PAIR): then the combine of the pairs into
+// them, as moe_combine does (inside the table kernels for single-token calls).
 moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const int32_t* offsets,
                              const int32_t* sorted_pair, const float* weights, int T, int k, int mode,
-                             float* out, uint8_t* status, void* ws, size_t ws_bytes, cudaStream_t s);
+                             float* out, uint8_t* status, void* ws, size_t ws_bytes, cudaStream_t s,
+                             const int32_t* pair_to_sorted = nullptr, float* comb32 = nullptr,
+                             uint16_t* comb16 = nullptr);
 moe_status launch_combine(const float* ypair, const int32_t* p2s, const float* w, const uint8_t* st,
                           int T, int k, int H, float* out32, uint16_t* out16, cudaStream_t s);
 

@@ -217,8 +217,10 @@ size_t ffn_workspace_size(int T, int k, int E, int H, int I) { return ws_layout(
 
 moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const int32_t* offsets,
                              const int32_t* sorted_pair, const float* weights, int T, int k, int mode,
-                             float* out, uint8_t* status, void* ws, size_t ws_bytes, cudaStream_t s) {
+                             float* out, uint8_t* status, void* ws, size_t ws_bytes, cudaStream_t s,
+                             const int32_t* pair_to_sorted, float* comb32, uint16_t* comb16) {
     (void)ws_bytes;
+    const bool comb = comb32 != nullptr || comb16 != nullptr;
     const int E = t->E, H = t->H, I = t->I;
     const int P = T * k;
     if (num_sms() >= MAX_LUT_CTAS) {
@@ -250,7 +252,8 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
         if ((st = launch_lut_fc(true, true, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s)) !=
             MOE_OK)
             return st;
-        return launch_lut_fc(false, true, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s);
+        return launch_lut_fc(false, true, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s,
+                             pair_to_sorted, comb32, comb16);
     }
     cudaError_t e = launch_pdl(schedule_kernel, dim3(1), dim3(1024), 0, s, (const SlotDesc*)t->d_desc, E, offsets,
                                sorted_pair, P, k, status, header, chunks, recs, grp_start, use_lut,
@@ -269,6 +272,7 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
         return st;
     if (mma && (st = launch_mma_fc(false, t, sorted_pair, weights, k, mode, out, w, L, s)) != MOE_OK) return st;
     if (use_umma && (st = launch_umma(false, t, sorted_pair, weights, k, P, mode, out, w, L, s)) != MOE_OK) return st;
+    if (comb) return launch_combine(out, pair_to_sorted, weights, status, T, k, H, comb32, comb16, s);
     return MOE_OK;
 }
 

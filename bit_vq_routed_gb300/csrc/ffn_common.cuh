@@ -43,7 +43,7 @@ enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NU
 // tensor-core paths read x16s (fp16 activations gathered by sorted position)
 // and a16 (fp16 silu(g)*u by sorted position).
 struct WsLayout {
-    size_t chunks_off, rec_off, grp_start_off, p1_off, p2_off, cnt_off, range_off;
+    size_t chunks_off, rec_off, grp_start_off, p1_off, p2_off, cnt_off, cnt2_off, range_off;
     size_t uchunks_off, x16s_off, a16_off, total;
     int max_chunks, max_lut, max_uchunks;
 };
@@ -79,6 +79,8 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I)
     o = ws_align(o + sizeof(float) * (size_t)L.max_lut * lut_jobs(I) * H);
     L.cnt_off = o;
     o = ws_align(o + sizeof(int32_t) * (size_t)L.max_lut * (H / 16));
+    L.cnt2_off = o;  // single-token calls that combine in the table kernel: one counter per 16 outputs
+    o = ws_align(o + sizeof(int32_t) * (size_t)(H / 16));
     L.range_off = o;
     o = ws_align(o + sizeof(int4) * (size_t)MAX_LUT_CTAS);
     const bool umma = T >= UMMA_MIN;
@@ -93,9 +95,13 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I)
     return L;
 }
 
+// comb32 / comb16 (single-token FC2 only, either may be null): also write the
+// combine of the pairs (moe_combine's arithmetic) using pair_to_sorted.
 moe_status launch_lut_fc(bool fc1, bool self, const SlotTableHost* t, const uint16_t* x, const int32_t* offsets,
                          const int32_t* sorted_pair, const float* weights, int k, int P, int mode, float* out,
-                         uint8_t* status, char* ws, const WsLayout& L, cudaStream_t s);
+                         uint8_t* status, char* ws, const WsLayout& L, cudaStream_t s,
+                         const int32_t* pair_to_sorted = nullptr, float* comb32 = nullptr,
+                         uint16_t* comb16 = nullptr);
 moe_status launch_gather_f16(const uint16_t* x, const int32_t* sorted_pair, int k, int H, int P, uint16_t* x16s,
                              cudaStream_t s);
 moe_status launch_umma(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,

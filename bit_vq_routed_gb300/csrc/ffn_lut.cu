@@ -30,6 +30,8 @@
 // to registers, hands the slot to the next copy and computes from registers,
 // with two units in flight.  Waits on the slots are bounded: a wait that runs
 // out records an error in the workspace header and the CTA stops.
+#include <cuda_bf16.h>
+
 #include "ffn_common.cuh"
 
 namespace moe {
@@ -143,7 +145,8 @@ __global__ void __maxnreg__(MAX_REG)
                    const int32_t* __restrict__ sorted_pair, const float* __restrict__ weights, int k, int H, int I,
                    int* __restrict__ header, const LutRec* __restrict__ recs,
                    const int4* __restrict__ fc1_range, const float* __restrict__ p1, float* __restrict__ pout,
-                   int* __restrict__ cnt, int mode, float* __restrict__ out) {
+                   int* __restrict__ cnt, int mode, float* __restrict__ out, const int32_t* __restrict__ p2s,
+                   float* __restrict__ comb32, uint16_t* __restrict__ comb16, int* __restrict__ cnt2) {
     extern __shared__ __align__(1024) uint8_t dyn[];
     Smem& S = *reinterpret_cast<Smem*>(dyn);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -244,6 +247,7 @@ __global__ void __maxnreg__(MAX_REG)
         if (FC1) {
             const int nc = n_lut * (H / 16);
             for (int i = blockIdx.x * THREADS + tid; i < nc; i += C * THREADS) cnt[i] = 0;
+            for (int i = blockIdx.x * THREADS + tid; i < H / 16; i += C * THREADS) cnt2[i] = 0;
         }
     } else if (FC1) {
         pdl_wait();
@@ -265,6 +269,7 @@ __global__ void __maxnreg__(MAX_REG)
         uniform_range(n_lut * KR, RT);
     }
 
+    const bool comb = !FC1 && SELF && (comb32 != nullptr || comb16 != nullptr);
     const int b = lane_block(lane), m = lane & 3;  // scale block and group phase of this lane
     const uint32_t lb = TAB | (uint32_t)(4 * lane);
     uint32_t phase = 0;                     // parity of the slot's next completion
@@ -502,7 +507,7 @@ __global__ void __maxnreg__(MAX_REG)
                     atomicAdd(out + (size_t)(pr / k) * H + h, weights[pr] * y);
                 }
             };
-            if (FC1 || KR > 1) {
+            if (FC1 || KR > 1 || comb) {
                 if ((lane & 1) == 0) pout[((size_t)(gs + pi) * KR + kr) * R + h] = acc[0];
             } else if ((lane & 1) == 0) {
                 emit(acc[0]);
@@ -544,10 +549,12 @@ __global__ void __maxnreg__(MAX_REG)
             if (pend) mbar_wait_bounded(bar, phase, nullptr, 0);
             pend = false;
         }
-        if (!FC1 && KR > 1) {
+        if (!FC1 && (KR > 1 || comb)) {
             // FC2 partials of this job's row tiles are all stored: one fence per
             // thread, then per row tile one arrival; the last of the KR units of
-            // a row tile adds the partials in K-range order and writes y.
+            // a row tile adds the partials in K-range order and writes y.  With
+            // the combine, the last of the pairs to finish a row tile then
+            // writes its 16 outputs.
             __threadfence();
             __syncthreads();
             const int pr = gs;  // FC2 groups are single pairs
@@ -578,6 +585,34 @@ __global__ void __maxnreg__(MAX_REG)
                         atomicAdd(out + (size_t)(p / k) * H + h, weights[p] * y);
                     }
                 }
+                if (comb) {
+                    // one token: out[h] = sum over pairs j (in order) of w_j y_j,
+                    // as moe_combine computes it
+                    __threadfence();
+                    __syncthreads();
+                    for (int t = tid; t < nt; t += THREADS) {
+                        if (S.lastf[t]) {
+                            int* c = cnt2 + v_first + v_inc * (tb + t);
+                            if (atomicAdd(c, 1) == n_lut - 1) {
+                                S.lastf[t] = 2;
+                                *c = 0;
+                            }
+                        }
+                    }
+                    __threadfence();
+                    __syncthreads();
+                    for (int idx = tid; idx < 16 * nt; idx += THREADS) {
+                        const int t = idx >> 4;
+                        if (S.lastf[t] != 2) continue;
+                        const int h = (v_first + v_inc * (tb + t)) * 16 + (idx & 15);
+                        float a = 0.0f;
+                        for (int j = 0; j < k; ++j)
+                            if (__ldcg(status + j))
+                                a = __fadd_rn(a, __fmul_rn(weights[j], __ldcg(out + (size_t)p2s[j] * H + h)));
+                        if (comb32) comb32[h] = a;
+                        if (comb16) comb16[h] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+                    }
+                }
                 __syncthreads();  // flags are reused by the next chunk
             }
         }
@@ -587,13 +622,20 @@ __global__ void __maxnreg__(MAX_REG)
         pdl_wait();
         pdl_launch_dependents();
     }
+    if (comb && n_lut == 0) {  // no pair computed: the combine is zero
+        for (int h = blockIdx.x * THREADS + tid; h < H; h += C * THREADS) {
+            if (comb32) comb32[h] = 0.0f;
+            if (comb16) comb16[h] = 0;
+        }
+    }
 }
 
 }  // namespace
 
 moe_status launch_lut_fc(bool fc1, bool self, const SlotTableHost* t, const uint16_t* x, const int32_t* offsets,
                          const int32_t* sorted_pair, const float* weights, int k, int P, int mode, float* out,
-                         uint8_t* status, char* ws, const WsLayout& L, cudaStream_t s) {
+                         uint8_t* status, char* ws, const WsLayout& L, cudaStream_t s,
+                         const int32_t* pair_to_sorted, float* comb32, uint16_t* comb16) {
     int* header = reinterpret_cast<int*>(ws);
     const LutRec* recs = reinterpret_cast<const LutRec*>(ws + L.rec_off);
     const int4* fc1_range = reinterpret_cast<const int4*>(ws + L.range_off);
@@ -606,7 +648,7 @@ moe_status launch_lut_fc(bool fc1, bool self, const SlotTableHost* t, const uint
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: table kernel shared memory");
     e = launch_pdl(kern, dim3((unsigned)num_sms()), dim3(THREADS), DYN_SMEM, s, (const SlotDesc*)t->d_desc, offsets,
                    t->E, P, status, t->codebook, x, sorted_pair, weights, k, t->H, t->I, header, recs, fc1_range, p1,
-                   pout, cnt, mode, out);
+                   pout, cnt, mode, out, pair_to_sorted, comb32, comb16, reinterpret_cast<int*>(ws + L.cnt2_off));
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: table kernel launch");
     MOE_LAUNCH_CHECK("moe_vq2_expert_ffn: table kernel launch");
     return MOE_OK;

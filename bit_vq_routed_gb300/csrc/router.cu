@@ -301,17 +301,113 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __rest
         for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(FULL, acc, off));
         if (lane == 0) logits[(size_t)t * E + e] = bias ? __fadd_rn(acc, bias[e]) : acc;
     }
-    // the last CTA to finish goes on
-    __threadfence();
+    // the last CTA to finish goes on (thread 0's fence, after the barrier,
+    // orders the whole CTA's logits before its arrival)
     __syncthreads();
     if (tid == 0) {
         const int n = gridDim.x * gridDim.y;
-        s_last = atomicAdd(counter, 1) == n - 1;
-        if (s_last) *counter = 0;
+        __threadfence();
+        const bool last = atomicAdd(counter, 1) == n - 1;
+        if (last) {
+            *counter = 0;
+            __threadfence();
+        }
+        s_last = last;
     }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
+
+    if (T == 1) {
+        // one token: warp 0 alone (no block barriers): top-k, then the k ids'
+        // ranks give the sorted order, and offsets[e] = #ids below e
+        if (warp != 0) return;
+        const float* l = logits;
+        float v[NPER];
+        uint32_t taken = 0;
+#pragma unroll
+        for (int i = 0; i < NPER; ++i) {
+            const int ee = lane + 32 * i;
+            if (ee < E) {
+                v[i] = __ldcg(l + ee);
+            } else {
+                v[i] = -INFINITY;
+                taken |= 1u << i;
+            }
+        }
+        float bv = -INFINITY;
+        int be = INT_MAX;
+        auto rescan = [&]() {
+            bv = -INFINITY;
+            be = INT_MAX;
+#pragma unroll
+            for (int i = 0; i < NPER; ++i) {
+                const int ee = lane + 32 * i;
+                if (!((taken >> i) & 1) && better(v[i], ee, bv, be)) {
+                    bv = v[i];
+                    be = ee;
+                }
+            }
+        };
+        rescan();
+        float sel_v = 0.0f;
+        int sel_e = 0;
+        for (int j = 0; j < k; ++j) {
+            float wv2 = bv;
+            int we = be;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                const float ov = __shfl_xor_sync(FULL, wv2, off);
+                const int oe = __shfl_xor_sync(FULL, we, off);
+                if (better(ov, oe, wv2, we)) {
+                    wv2 = ov;
+                    we = oe;
+                }
+            }
+            if (lane == j) {
+                sel_v = wv2;
+                sel_e = we;
+            }
+            if ((we & 31) == lane) {
+                taken |= 1u << (we >> 5);
+                rescan();
+            }
+        }
+        const float top = __shfl_sync(FULL, sel_v, 0);
+        const float num = lane < k ? expf(sel_v - top) : 0.0f;
+        float den = 0.0f;
+        if (renorm) {
+            den = num;
+        } else {
+#pragma unroll
+            for (int i = 0; i < NPER; ++i)
+                if (lane + 32 * i < E) den += expf(v[i] - top);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(FULL, den, off);
+        // the k ids are distinct: rank of pair j = #ids below id_j; per e,
+        // offsets[e] = #ids below e
+        int rank = 0;
+        int cnt[NPER];
+#pragma unroll
+        for (int i = 0; i < NPER; ++i) cnt[i] = 0;
+        for (int j = 0; j < k; ++j) {
+            const int idj = __shfl_sync(FULL, sel_e, j);
+            rank += idj < sel_e;
+#pragma unroll
+            for (int i = 0; i < NPER; ++i) cnt[i] += idj < lane + 32 * i;
+        }
+        if (lane < k) {
+            ids[lane] = sel_e;
+            weights[lane] = num / den;
+            sorted_pair[rank] = lane;
+            pair_to_sorted[lane] = rank;
+        }
+#pragma unroll
+        for (int i = 0; i < NPER; ++i)
+            if (lane + 32 * i < E) offsets[lane + 32 * i] = cnt[i];
+        if (lane == 0) offsets[E] = k;
+        return;
+    }
 
     const int P = T * k;
     int32_t* s_ids = reinterpret_cast<int32_t*>(xs);  // (the activations are done with)

@@ -4,8 +4,8 @@ sequence of library calls of one forward pass.
     logits = router(x)                  moe_router_logits  \
     ids, w = top-k softmax(logits)      moe_route_topk      > moe_route (one kernel
     permutation by expert               moe_permute        /  for small batches)
-    y per (token, expert) pair          moe_vq2_expert_ffn (per-pair mode)
-    out = sum_j w * y                   moe_combine
+    y per (token, expert) pair          moe_vq2_expert_ffn (per-pair mode)  \ (or both in one call:
+    out = sum_j w * y                   moe_combine                         /  moe_vq2_expert_ffn_combine)
 
 All five run as library kernels on one stream, with no host synchronisation,
 so a forward pass can be captured in a CUDA graph.
@@ -19,7 +19,7 @@ import torch
 
 from . import (MOE_FMT_FP4, MOE_FMT_VQ2, MOE_FUSED_SCATTER, MOE_PER_PAIR, SlotTable, moe_combine,
                moe_fp4_pack, moe_permute, moe_route, moe_route_topk, moe_route_workspace_size, moe_router_logits,
-               moe_vq2_expert_ffn, moe_vq2_expert_ffn_workspace_size)
+               moe_vq2_expert_ffn, moe_vq2_expert_ffn_combine, moe_vq2_expert_ffn_workspace_size)
 
 
 def _dev(a, dtype=None, device="cuda"):
@@ -103,6 +103,15 @@ class MoELayer:
         dst = self.ypair[:P] if mode == MOE_PER_PAIR else out
         moe_vq2_expert_ffn(self.table, x, self.offsets, self.sorted_pair[:P], self.weights[:T], self.k, mode,
                            dst, self.pair_status[:P], self.ws, stream)
+
+    def experts_combine(self, x, out, out_bf16=None, stream=None):
+        """experts() in per-pair mode and the combine into out (fp32 [T, H])
+        and/or out_bf16, in one call (moe_vq2_expert_ffn_combine)."""
+        T = x.shape[0]
+        P = T * self.k
+        moe_vq2_expert_ffn_combine(self.table, x, self.offsets, self.sorted_pair[:P], self.pair_to_sorted[:P],
+                                   self.weights[:T], self.k, self.ypair[:P], self.pair_status[:P], out, out_bf16,
+                                   self.ws, stream)
 
     def forward(self, x, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         """x: bf16 [T, H] on the device -> fp32 [T, H] (a view of self.out

@@ -243,6 +243,19 @@ moe_status moe_vq2_expert_ffn_noalloc(const moe_slot_table* table, const uint16_
                                       const float* weights, int T, int k, int mode, float* out_or_ypair,
                                       uint8_t* pair_status, cudaStream_t stream);
 
+/* moe_vq2_expert_ffn in per-pair mode followed by moe_combine, in one call:
+ * ypair and pair_status as moe_vq2_expert_ffn writes them, out_f32 /
+ * out_bf16 as moe_combine(ypair, pair_to_sorted, weights, pair_status)
+ * writes them, bit for bit.  For single-token calls whose slot table holds
+ * VQ2 experts only, the combine runs inside the expert kernels (the last of
+ * the pairs to finish 16 outputs writes them: no separate kernel).  Same
+ * workspace as moe_vq2_expert_ffn. */
+moe_status moe_vq2_expert_ffn_combine(const moe_slot_table* table, const uint16_t* x,
+                                      const int32_t* expert_offsets, const int32_t* sorted_pair,
+                                      const int32_t* pair_to_sorted, const float* weights, int T, int k,
+                                      float* ypair, uint8_t* pair_status, float* out_f32, uint16_t* out_bf16,
+                                      void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Deterministic combine: out[t] = sum over j = 0..k-1 (in that order) of
  * pair_status[t*k+j] * weights[t,j] * ypair[pair_to_sorted[t*k+j]].
  * ypair fp32 [P,H] (per-pair mode of moe_vq2_expert_ffn); out_f32 fp32

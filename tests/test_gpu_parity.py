@@ -166,3 +166,36 @@ def test_workspace_too_small_is_rejected(torch):
         bv.moe_vq2_expert_ffn(dev.table, x, dev.offsets, dev.sorted_pair[:8], dev.weights[:4], 2,
                               bv.MOE_PER_PAIR, dev.ypair[:8], dev.pair_status[:8], small)
     assert ei.value.status == bv.MOE_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("T,resident_frac,bf16", [(1, 1.0, False), (1, 0.5, True), (1, 0.0, False), (6, 0.7, True)])
+def test_expert_ffn_combine_matches_separate_calls(torch, T, resident_frac, bf16):
+    # moe_vq2_expert_ffn_combine == moe_vq2_expert_ffn (per pair) + moe_combine,
+    # bit for bit (one token: the combine runs inside the expert kernels)
+    import bit_vq_routed_gb300 as bv
+    spec = ms.LayerSpec(H=1024, I=512, E=32, k=8, seed=31 + T)
+    layer = ms.Layer(spec)
+    rng = np.random.default_rng(T)
+    res_ids = np.nonzero(rng.random(32) < resident_frac)[0] if resident_frac < 1 else None
+    dev, keep = device_layer(layer, T, res_ids)
+    x = torch.from_numpy(ms.tokens(T, 1024, seed=T)).view(torch.bfloat16).cuda()
+    P = T * 8
+    dev.route(x)
+    dev.experts(x, bv.MOE_PER_PAIR)
+    ref32 = torch.empty(T, 1024, dtype=torch.float32, device="cuda")
+    ref16 = torch.empty(T, 1024, dtype=torch.bfloat16, device="cuda")
+    bv.moe_combine(dev.ypair[:P], dev.pair_to_sorted[:P], dev.weights[:T], dev.pair_status[:P], 8, ref32,
+                   ref16.view(torch.int16) if bf16 else None)
+    y_ref = dev.ypair[:P].clone()
+    st_ref = dev.pair_status[:P].clone()
+    out32 = torch.full((T, 1024), float("nan"), dtype=torch.float32, device="cuda")
+    out16 = torch.zeros(T, 1024, dtype=torch.bfloat16, device="cuda")
+    dev.experts_combine(x, out32, out16.view(torch.int16) if bf16 else None)
+    torch.cuda.synchronize()
+    assert torch.equal(dev.pair_status[:P], st_ref)
+    done = st_ref.bool()
+    assert torch.equal(dev.ypair[:P][done].view(torch.int32), y_ref[done].view(torch.int32))
+    assert torch.equal(out32.view(torch.int32), ref32.view(torch.int32))
+    if bf16:
+        assert torch.equal(out16.view(torch.int16), ref16.view(torch.int16))
+    assert device_error_word(dev) == 0
