@@ -54,6 +54,7 @@ EXPORTED = [
     "moe_route_topk", "moe_permute_workspace_size", "moe_permute",
     "moe_vq2_expert_ffn_workspace_size", "moe_vq2_expert_ffn", "moe_vq2_expert_ffn_noalloc", "moe_combine",
     "moe_launch_count", "moe_route_workspace_size", "moe_route", "moe_vq2_expert_ffn_combine",
+    "moe_selftest",
 ]
 
 
@@ -91,6 +92,7 @@ def load(path: Optional[str] = None, build_if_stale: bool = True):
         "moe_route_workspace_size": ([I, I, I], Z),
         "moe_route": ([P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, Z, P], I),
         "moe_vq2_expert_ffn_combine": ([P, P, P, P, P, P, I, I, P, P, P, P, P, Z, P], I),
+        "moe_selftest": ([P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -247,6 +249,14 @@ def moe_launch_count() -> int:
     """Kernel launches the library has issued since it was loaded (a launch
     inside a stream capture counts once)."""
     return int(load().moe_launch_count())
+
+
+def moe_selftest(stream=None) -> None:
+    """Boot self-check of the library on the current device: runs a tiny
+    layer through every kernel family and compares with stored CPU-reference
+    results.  Synchronises the stream; raises MoeError (status
+    MOE_ERR_MISMATCH for a wrong result) on failure."""
+    _check(load().moe_selftest(_stream(stream)))
 
 
 def moe_route_workspace_size(T: int, k: int, E: int) -> int:

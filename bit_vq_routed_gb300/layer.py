@@ -1,4 +1,4 @@
-"""One routed-expert MoE layer on the device: the buffers it needs and the
+r"""One routed-expert MoE layer on the device: the buffers it needs and the
 sequence of library calls of one forward pass.
 
     logits = router(x)                  moe_router_logits  \

@@ -266,6 +266,26 @@ moe_status moe_combine(const float* ypair, const int32_t* pair_to_sorted, const 
                        const uint8_t* pair_status, int T, int k, int H, float* out_f32,
                        uint16_t* out_bf16, cudaStream_t stream);
 
+/* Boot self-check (Tandem-vLLM page, "New in 0.2.0": each kernel is checked
+ * against a reference at boot).  Runs a tiny layer (hidden 256, intermediate
+ * 128, 8 experts, top-2) through the entry points above on the current
+ * device: the router and top-k step by step and fused, the permutation, the
+ * expert FFN on 1, 4 and 128 tokens (the one-token table kernels, the
+ * small-batch mma.sync kernels and the tcgen05 kernels), an all-VQ2 and a
+ * mixed VQ2/FP4 layer, both output modes, the fused expert-FFN + combine and
+ * a layer with two experts not resident.  The inputs are drawn on the GPU
+ * from a counter-based generator (SplitMix64); the results are compared with
+ * values computed from the same draws by the CPU reference and compiled into
+ * the library: routing (logits bits, ids, offsets, permutation) exactly,
+ * router weights within 1e-6, layer outputs within max |err| <= 2e-2 *
+ * rms(ref) and sum |err| <= 2e-3 * sum |ref|.
+ * Unlike the hot-path calls it allocates and frees device memory (a few MB),
+ * synchronises `stream` and must not be called while the stream is being
+ * captured.  Returns MOE_OK, MOE_ERR_MISMATCH (moe_last_error() names the
+ * first failing case and value), MOE_ERR_NO_MEM, MOE_ERR_CUDA, or the error
+ * of a failing entry point. */
+moe_status moe_selftest(cudaStream_t stream);
+
 /* Number of kernel launches the library has issued on the host since it was
  * loaded, over all devices and threads (atomic).  A launch made while a
  * stream is being captured counts once, as the one kernel node it adds to

@@ -177,3 +177,109 @@ WORKLOADS = {
 def most_popular(layer: Layer, n: int) -> np.ndarray:
     """Ids of the n experts with the lowest popularity rank."""
     return np.nonzero(layer.rank <= n)[0].astype(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# Counter-based inputs of the library's boot self-check.
+#
+# The self-check (Tandem-vLLM page, "New in 0.2.0": each kernel is checked
+# against a reference at boot) draws its inputs on the GPU, so they cannot be
+# handed over from here; the CUDA library draws the same numbers from the
+# same published generator, implemented separately there.
+#
+# Generator: SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom
+# number generators", OOPSLA 2014): the first output of the generator whose
+# state is s, i.e. z = s + 0x9E3779B97F4A7C15, z = (z ^ z>>30) *
+# 0xBF58476D1CE4E5B9, z = (z ^ z>>27) * 0x94D049BB133111EB, z ^ z>>31, all
+# mod 2^64.  Draw i of stream `tag` is the output for s = tag * 2^32 + i.
+#
+# Values (each exactly representable, so that rounding cannot differ):
+#   g(v)   = sum of the 6-bit fields v>>0, v>>8, v>>16, v>>24 (& 63) - 126,
+#            an integer in [-126, 126] with a bell-shaped law, std 36.9;
+#   tokens     bf16  g / 32            (std 1.15; the N(0,1) activations)
+#   router     bf16  g / 2048          (std 0.018; the N(0,0.02) router)
+#   codebook   fp16  g / 32            (std 1.15; the N(0,1) codebook)
+#   VQ2 codes  uint8 v & 255           (uniform codes)
+#   VQ2 scales fp16  (40 + v mod 124) / 8192   (0.0049 .. 0.0199)
+#   FP4 codes  uint8 v & 255           (two uniform e2m1 nibbles)
+#   FP4 scales uint8 118 + v mod 3     (2^-9 .. 2^-7)
+# Arrays are drawn in row-major order of their logical layout; token row t
+# uses draws of row t mod 4, so larger batches repeat the four tokens.
+# ---------------------------------------------------------------------------
+SELFTEST_H, SELFTEST_I, SELFTEST_E, SELFTEST_K, SELFTEST_T = 256, 128, 8, 2, 4
+ST_TAG_TOKENS, ST_TAG_ROUTER, ST_TAG_CODEBOOK = 1, 2, 3
+ST_TAG_VQ2_CODES, ST_TAG_VQ2_SCALES = 16, 48      # + 4*expert + matrix
+ST_TAG_FP4_CODES, ST_TAG_FP4_SCALES = 80, 112     # + 4*expert + matrix
+SELFTEST_FP4_EXPERTS = (1, 3, 5, 7)               # FP4 in the mixed-format layer
+
+_SM_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_SM_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_SM_M2 = np.uint64(0x94D049BB133111EB)
+
+
+def splitmix64(state: np.ndarray) -> np.ndarray:
+    """First SplitMix64 output for each uint64 state (wrapping arithmetic)."""
+    z = np.asarray(state, dtype=np.uint64) + _SM_GAMMA
+    z = (z ^ (z >> np.uint64(30))) * _SM_M1
+    z = (z ^ (z >> np.uint64(27))) * _SM_M2
+    return z ^ (z >> np.uint64(31))
+
+
+def st_draw(tag: int, n: int, period: Optional[int] = None) -> np.ndarray:
+    i = np.arange(n, dtype=np.uint64)
+    if period is not None:
+        i = i % np.uint64(period)
+    return splitmix64((np.uint64(tag) << np.uint64(32)) | i)
+
+
+def st_bell(v: np.ndarray) -> np.ndarray:
+    f = np.zeros(v.shape, dtype=np.int64)
+    for sh in (0, 8, 16, 24):
+        f += ((v >> np.uint64(sh)) & np.uint64(63)).astype(np.int64)
+    return f - 126
+
+
+class SelftestLayer:
+    """The self-check's layer (hidden 256, intermediate 128, 8 experts,
+    top-2, no router bias), VQ2 everywhere or, with ``mixed``, FP4 for the
+    experts in SELFTEST_FP4_EXPERTS; same interface as :class:`Layer`."""
+
+    def __init__(self, mixed: bool = False):
+        H, I, E, k = SELFTEST_H, SELFTEST_I, SELFTEST_E, SELFTEST_K
+        self.spec = LayerSpec(H=H, I=I, E=E, k=k, seed=0)
+        self.w_router = bf16_bits((st_bell(st_draw(ST_TAG_ROUTER, E * H)) / 2048.0)
+                                  .astype(np.float32)).reshape(E, H)
+        self.codebook = fp16_bits(st_bell(st_draw(ST_TAG_CODEBOOK, 512)) / 32.0).reshape(128, 4)
+        self.bias = None
+        self.formats = np.full(E, FMT_VQ2, dtype=np.int32)
+        if mixed:
+            self.formats[list(SELFTEST_FP4_EXPERTS)] = FMT_FP4
+
+    def expert(self, e: int, cache: bool = True) -> ExpertWeights:
+        H, I = SELFTEST_H, SELFTEST_I
+        fmt = int(self.formats[e])
+        codes, scales = [], []
+        for m, (rows, K) in enumerate([(I, H), (I, H), (H, I)]):
+            if fmt == FMT_VQ2:
+                c = st_draw(ST_TAG_VQ2_CODES + 4 * e + m, rows * K // 4)
+                s = st_draw(ST_TAG_VQ2_SCALES + 4 * e + m, rows * K // 128)
+                codes.append((c & np.uint64(255)).astype(np.uint8).reshape(rows, K // 4))
+                scales.append(fp16_bits((40 + (s % np.uint64(124)).astype(np.int64)) / 8192.0)
+                              .reshape(rows, K // 128))
+            else:
+                c = st_draw(ST_TAG_FP4_CODES + 4 * e + m, rows * K // 2)
+                s = st_draw(ST_TAG_FP4_SCALES + 4 * e + m, rows * K // 32)
+                codes.append((c & np.uint64(255)).astype(np.uint8).reshape(rows, K // 2))
+                scales.append((118 + (s % np.uint64(3)).astype(np.int64)).astype(np.uint8)
+                              .reshape(rows, K // 32))
+        return ExpertWeights(fmt, codes, scales)
+
+    def drop_cache(self):
+        pass
+
+
+def selftest_tokens(T: int = SELFTEST_T) -> np.ndarray:
+    """bf16 bits [T, 256]: row t is the self-check's token t mod 4."""
+    H = SELFTEST_H
+    v = st_draw(ST_TAG_TOKENS, T * H, period=SELFTEST_T * H)
+    return bf16_bits((st_bell(v) / 32.0).astype(np.float32)).reshape(T, H)
