@@ -16,7 +16,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       float* __restrict__ out32,
                                                       uint16_t* __restrict__ out16) {
     pdl_wait();
-    pdl_launch_dependents();  // dependents may start their prologues now
+    // dependents may start their prologues now, unless they may read out16
+    // as their activations (then they start when this kernel has finished)
+    if (out16 == nullptr) pdl_launch_dependents();
     const int t = blockIdx.y, lane = threadIdx.x & 31;
     const int h = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
     int row = -1;

@@ -196,11 +196,14 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
 // Launch with programmatic dependent launch allowed: the kernel may start
 // while its predecessor on the stream still runs.  Every kernel of the library
 // calls pdl_wait() before it touches memory an earlier kernel may write or
-// read, and pdl_launch_dependents() right after it.  So when a kernel starts,
-// its predecessor has at least passed its own wait, i.e. everything two
-// launches back is complete; the code before the wait (shared-memory set-up,
-// constant weights, and reads of results two launches back) overlaps the
-// predecessor's run.
+// read, and pdl_launch_dependents() right after it -- except a kernel that
+// writes a bf16 activation output (the combine's out_bf16), which lets its
+// dependents start only when it has finished.  So when a kernel starts, its
+// predecessor has at least passed its own wait, i.e. everything two launches
+// back is complete, and so are the bf16 activations the caller passes in (x):
+// no library kernel that may still be running writes them.  The code before
+// the wait (shared-memory set-up, constant weights, x, and reads of results
+// two launches back) overlaps the predecessor's run.
 //
 // Host-side count of kernel launches the library has issued (a launch made
 // inside a stream capture counts once: it becomes one graph node).

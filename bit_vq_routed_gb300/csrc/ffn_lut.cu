@@ -24,12 +24,13 @@
 // warp that completes a row tile last (one counter per row tile) adds them in
 // K-range order and writes y, so every result is independent of timing.
 //
-// Code tiles are streamed by the copy engine (bulk copies, one per 512-byte
-// tile) into two shared-memory slots per warp, so the code stream never sits
-// in the load/store queue in front of the table reads; a warp copies a slot
-// to registers, hands the slot to the next copy and computes from registers,
-// with two units in flight.  Waits on the slots are bounded: a wait that runs
-// out records an error in the workspace header and the CTA stops.
+// Code tiles are streamed by the copy engine into one shared-memory slot per
+// warp (a unit = 16 rows x 1024 inputs: three bulk copies, codes and scales),
+// so the code stream never sits in the load/store queue in front of the table
+// reads; a warp copies its slot to registers, hands the slot to the copy of
+// its next unit, asks L2 for the unit after that, and computes from
+// registers.  Waits on the slots are bounded: a wait that runs out records an
+// error in the workspace header and the CTA stops.
 #include <cuda_bf16.h>
 
 #include "ffn_common.cuh"
@@ -53,6 +54,7 @@ constexpr uint32_t SCALE_OFF = HALF_OFF + 4 * 512;
 constexpr uint32_t SLOT_BYTES = SCALE_OFF + 8 * 32;
 constexpr int NSLOT = LW;
 constexpr int LOW_SLOTS = 12;            // slots below the table; the rest above it
+static_assert(LOW_SLOTS * SLOT_BYTES >= 4 * (1024 + 1), "the expert offsets (E <= 1024) fit in the low slots");
 // scale block of lane l (the 4 lanes 4q .. 4q+3 share one): blocks b and b + 4
 // for the two lane quads of each quarter-warp
 __host__ __device__ constexpr int lane_block(int l) { return (((l >> 2) & 1) << 2) | (l >> 3); }
@@ -207,15 +209,79 @@ __global__ void __maxnreg__(MAX_REG)
             u1 = (int)((long long)U * (blockIdx.x + 1) / C);
         }
     };
+    // Table of one K-range from S.xs: a thread takes a quad of words (the 4
+    // lanes 4 lq .. 4 lq + 3 of scale block bq, in group-slot pair (j0, j0 + 1),
+    // j0 = 4p + 2jj: the 8 consecutive groups 32 bq + 4 j0 + 0..7) and every
+    // LW-th code.
+    auto build_table = [&](int nkb) {
+        const int q = tid & 31, lq = q & 7, jj = (q >> 3) & 1, p = q >> 4, bq = lane_block(4 * lq);
+        if (bq < nkb) {
+            const int g0 = 32 * bq + 4 * (4 * p + 2 * jj);
+            // xp[m][i] = (x[4(g0+m)+i], x[4(g0+4+m)+i]): the low / high half of word m
+            float2 xp[4][4];
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+                const float4 lo = *reinterpret_cast<const float4*>(&S.xs[xs_at(4 * (g0 + mm))]);
+                const float4 hi = *reinterpret_cast<const float4*>(&S.xs[xs_at(4 * (g0 + 4 + mm))]);
+                xp[mm][0] = make_float2(lo.x, hi.x);
+                xp[mm][1] = make_float2(lo.y, hi.y);
+                xp[mm][2] = make_float2(lo.z, hi.z);
+                xp[mm][3] = make_float2(lo.w, hi.w);
+            }
+            const uint32_t a0 = TAB + (uint32_t)p * PLANE + 128u * jj + 16u * lq;
+#pragma unroll
+            for (int it = 0; it < 128 / LW; ++it) {
+                const int c0 = warp + it * LW;
+                const float4 e = *reinterpret_cast<const float4*>(&S.cb[4 * c0]);
+                const float2 ex = make_float2(e.x, e.x), ey = make_float2(e.y, e.y);
+                const float2 ez = make_float2(e.z, e.z), ew = make_float2(e.w, e.w);
+                uint32_t wv[4];
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm) {
+                    float2 v2 = __fmul2_rn(ex, xp[mm][0]);
+                    v2 = __ffma2_rn(ey, xp[mm][1], v2);
+                    v2 = __ffma2_rn(ez, xp[mm][2], v2);
+                    v2 = __ffma2_rn(ew, xp[mm][3], v2);
+                    const __half2 hv = __floats2half2_rn(v2.x, v2.y);
+                    wv[mm] = *reinterpret_cast<const uint32_t*>(&hv);
+                }
+                const uint32_t a = a0 + 256u * (uint32_t)c0;
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wv[0]), "r"(wv[1]),
+                             "r"(wv[2]), "r"(wv[3]));
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + 128u * 256u),
+                             "r"(wv[0] ^ 0x80008000u), "r"(wv[1] ^ 0x80008000u), "r"(wv[2] ^ 0x80008000u),
+                             "r"(wv[3] ^ 0x80008000u));
+            }
+        }
+    };
+    // The token's activations of a K-range into S.xs (as fp32).
+    auto load_x = [&](int t, int kr, int nin) {
+        for (int i = tid; i < nin; i += THREADS)
+            S.xs[xs_at(i)] = __uint_as_float((uint32_t)x[(size_t)t * H + KR_IN * kr + i] << 16);
+    };
+    // SELF FC1: the CTA's K-range follows from the grid alone (KR jobs of
+    // equal size, see uniform_range), so the activations and the table are
+    // built before the wait, while the routing kernel before this one still
+    // runs (x is complete at launch: no library kernel still running writes
+    // bf16 activations).
+    int pre_kr = -1;
+    if (SELF && FC1 && KR <= C) {
+        pre_kr = (int)(((long long)(blockIdx.x + 1) * KR - 1) / C);
+        const int nkb = min(LUT_KB, KB - LUT_KB * pre_kr);
+        load_x(0, pre_kr, 128 * nkb);
+        __syncthreads();
+        build_table(nkb);
+    }
     if (SELF) {
         // FC1: the offsets come from the kernel just before (wait first); FC2:
         // they are two kernels back (complete), so FC2 lists its pairs first.
         if (FC1) {
             pdl_wait();
-            pdl_launch_dependents();
+            pdl_launch_dependents();  // (FC1 writes no bf16 activations)
             if (blockIdx.x == 0 && tid == 0) *err = 0;  // this call's error word
         }
-        int* s_off = reinterpret_cast<int*>(S.xs);  // (the inputs are built later)
+        // the offsets are staged in the (still unused) code slots below the table
+        int* s_off = reinterpret_cast<int*>(dyn + (low_base - base));
         for (int i = tid; i <= E; i += THREADS) s_off[i] = FC1 ? offsets[i] : __ldcg(offsets + i);
         if (tid < MAX_GROUP) S.e_of_s[tid] = -1;
         __syncthreads();
@@ -241,6 +307,9 @@ __global__ void __maxnreg__(MAX_REG)
             if (FC1 && blockIdx.x == 0 && lane < P) status[sorted_pair[lane]] = res ? 1 : 0;
             if (lane == 0) S.n_self = __popc(mask);
         }
+        // the slots were written through the generic proxy; the copies that
+        // fill them later are async-proxy writes
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         n_lut = S.n_self;
         uniform_range(FC1 ? KR : n_lut * KR, FC1 ? n_lut * RT : RT);
@@ -305,11 +374,8 @@ __global__ void __maxnreg__(MAX_REG)
                 S.ys[tid] = r.sorted;
             }
         }
-        if (FC1) {  // the token's activations of this K-range
-            const int t = SELF ? 0 : r0.token;
-            for (int i = tid; i < nin; i += THREADS)
-                S.xs[xs_at(i)] = __uint_as_float((uint32_t)x[(size_t)t * H + KR_IN * kr + i] << 16);
-        }
+        const bool prebuilt = SELF && FC1 && kr == pre_kr;  // table built before the wait
+        if (FC1 && !prebuilt) load_x(SELF ? 0 : r0.token, kr, nin);  // the token's activations
         __syncthreads();
 
         // unit v of the job <-> (pair pi of the group, row tile rt); cursors
@@ -375,8 +441,10 @@ __global__ void __maxnreg__(MAX_REG)
 
         if (!waited) {
             pdl_wait();
-            // everything a dependent kernel may touch before its own wait is complete
-            pdl_launch_dependents();
+            // everything a dependent kernel may touch before its own wait is
+            // complete; with a bf16 combine output the dependents start only
+            // when this kernel has finished (they may read it as activations)
+            if (comb16 == nullptr) pdl_launch_dependents();
             waited = true;
         }
         if (!FC1) {
@@ -415,50 +483,7 @@ __global__ void __maxnreg__(MAX_REG)
             __syncthreads();
         }
 
-        // Table: a thread takes a quad of words (the 4 lanes 4 lq .. 4 lq + 3 of
-        // scale block bq, in group-slot pair (j0, j0 + 1), j0 = 4p + 2jj: the
-        // 8 consecutive groups 32 bq + 4 j0 + 0..7) and every LW-th code.
-        {
-            const int q = tid & 31, lq = q & 7, jj = (q >> 3) & 1, p = q >> 4, bq = lane_block(4 * lq);
-            if (bq < nkb) {
-                const int g0 = 32 * bq + 4 * (4 * p + 2 * jj);
-                // xp[m][i] = (x[4(g0+m)+i], x[4(g0+4+m)+i]): the low / high half of word m
-                float2 xp[4][4];
-#pragma unroll
-                for (int mm = 0; mm < 4; ++mm) {
-                    const float4 lo = *reinterpret_cast<const float4*>(&S.xs[xs_at(4 * (g0 + mm))]);
-                    const float4 hi = *reinterpret_cast<const float4*>(&S.xs[xs_at(4 * (g0 + 4 + mm))]);
-                    xp[mm][0] = make_float2(lo.x, hi.x);
-                    xp[mm][1] = make_float2(lo.y, hi.y);
-                    xp[mm][2] = make_float2(lo.z, hi.z);
-                    xp[mm][3] = make_float2(lo.w, hi.w);
-                }
-                const uint32_t a0 = TAB + (uint32_t)p * PLANE + 128u * jj + 16u * lq;
-#pragma unroll
-                for (int it = 0; it < 128 / LW; ++it) {
-                    const int c0 = warp + it * LW;
-                    const float4 e = *reinterpret_cast<const float4*>(&S.cb[4 * c0]);
-                    const float2 ex = make_float2(e.x, e.x), ey = make_float2(e.y, e.y);
-                    const float2 ez = make_float2(e.z, e.z), ew = make_float2(e.w, e.w);
-                    uint32_t wv[4];
-#pragma unroll
-                    for (int mm = 0; mm < 4; ++mm) {
-                        float2 v2 = __fmul2_rn(ex, xp[mm][0]);
-                        v2 = __ffma2_rn(ey, xp[mm][1], v2);
-                        v2 = __ffma2_rn(ez, xp[mm][2], v2);
-                        v2 = __ffma2_rn(ew, xp[mm][3], v2);
-                        const __half2 hv = __floats2half2_rn(v2.x, v2.y);
-                        wv[mm] = *reinterpret_cast<const uint32_t*>(&hv);
-                    }
-                    const uint32_t a = a0 + 256u * (uint32_t)c0;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wv[0]), "r"(wv[1]),
-                                 "r"(wv[2]), "r"(wv[3]));
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + 128u * 256u),
-                                 "r"(wv[0] ^ 0x80008000u), "r"(wv[1] ^ 0x80008000u), "r"(wv[2] ^ 0x80008000u),
-                                 "r"(wv[3] ^ 0x80008000u));
-                }
-            }
-        }
+        if (!prebuilt) build_table(nkb);
         __syncthreads();
 
         auto compute_store = [&](const UnitRegs& r, Cur cu) {
@@ -620,7 +645,7 @@ __global__ void __maxnreg__(MAX_REG)
     }
     if (!waited) {  // a CTA without units still waits for FC1 before it leaves
         pdl_wait();
-        pdl_launch_dependents();
+        if (comb16 == nullptr) pdl_launch_dependents();
     }
     if (comb && n_lut == 0) {  // no pair computed: the combine is zero
         for (int h = blockIdx.x * THREADS + tid; h < H; h += C * THREADS) {
@@ -646,7 +671,11 @@ moe_status launch_lut_fc(bool fc1, bool self, const SlotTableHost* t, const uint
                      : (fc1 ? ffn_lut_kernel<true, false> : ffn_lut_kernel<false, false>);
     cudaError_t e = ensure_smem_attr(kern, (int)DYN_SMEM);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: table kernel shared memory");
-    e = launch_pdl(kern, dim3((unsigned)num_sms()), dim3(THREADS), DYN_SMEM, s, (const SlotDesc*)t->d_desc, offsets,
+    // One CTA per SM; the single-token FC1 leaves one SM free, so that all of
+    // its CTAs are resident (building their tables) while the routing
+    // kernel's last CTA still runs.
+    const int grid = (self && fc1 && num_sms() > 1) ? num_sms() - 1 : num_sms();
+    e = launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), DYN_SMEM, s, (const SlotDesc*)t->d_desc, offsets,
                    t->E, P, status, t->codebook, x, sorted_pair, weights, k, t->H, t->I, header, recs, fc1_range, p1,
                    pout, cnt, mode, out, pair_to_sorted, comb32, comb16, reinterpret_cast<int*>(ws + L.cnt2_off));
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: table kernel launch");

@@ -274,9 +274,11 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __rest
 #pragma unroll
     for (int u = 0; u < U; ++u)
         if (u < per) wv[u] = __ldg(wr + lane + 32 * u);
+    // the activations are complete at launch (no library kernel still running
+    // writes them), so they are read before the wait too
+    for (int i = tid; i < nch; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(x + (size_t)t * H)[i];
     pdl_wait();
     pdl_launch_dependents();  // dependents may start their prologues now
-    for (int i = tid; i < nch; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(x + (size_t)t * H)[i];
     __syncthreads();
     if (e < E) {
         float acc = 0.0f;
