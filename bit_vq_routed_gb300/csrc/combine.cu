@@ -23,11 +23,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     const int h = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
     int row = -1;
     float wj = 0.0f;
-    if (lane < k) {
+    if (lane < k) {  // (the three loads in one round trip)
         const int p = t * k + lane;
-        if (st[p]) {
-            row = p2s[p];
-            wj = w[p];
+        const uint8_t sv = st[p];
+        const int rv = p2s[p];
+        const float wv = w[p];
+        if (sv) {
+            row = rv;
+            wj = wv;
         }
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -264,6 +264,18 @@ __global__ void __maxnreg__(MAX_REG)
     // built before the wait, while the routing kernel before this one still
     // runs (x is complete at launch: no library kernel still running writes
     // bf16 activations).
+    // With two FC2 K-ranges and per-pair output, FC2 adds its two partial
+    // sums straight into the zeroed output row (fp32 addition is commutative,
+    // so 0 + p0 + p1 does not depend on the order) instead of a finishing
+    // step; FC1 zeroes the rows of the table pairs.
+    const bool fc2_adds = mode == MOE_PER_PAIR && lut_jobs(I) == 2;
+    auto zero_rows = [&](auto row_of) {
+        const int n4 = H / 4;  // (n_lut <= E <= 1024 table pairs)
+        for (int i = blockIdx.x * THREADS + tid; i < n_lut * n4; i += C * THREADS) {
+            const int p = i / n4;
+            reinterpret_cast<float4*>(out + (size_t)row_of(p) * H)[i - p * n4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
     int pre_kr = -1;
     if (SELF && FC1 && KR <= C) {
         pre_kr = (int)(((long long)(blockIdx.x + 1) * KR - 1) / C);
@@ -317,6 +329,7 @@ __global__ void __maxnreg__(MAX_REG)
             const int nc = n_lut * (H / 16);
             for (int i = blockIdx.x * THREADS + tid; i < nc; i += C * THREADS) cnt[i] = 0;
             for (int i = blockIdx.x * THREADS + tid; i < H / 16; i += C * THREADS) cnt2[i] = 0;
+            if (fc2_adds) zero_rows([&](int p) { return S.all_ys[p]; });
         }
     } else if (FC1) {
         pdl_wait();
@@ -331,6 +344,7 @@ __global__ void __maxnreg__(MAX_REG)
         // FC2's arrival counters start at zero
         const int nc = n_lut * (H / 16);
         for (int i = blockIdx.x * THREADS + tid; i < nc; i += C * THREADS) cnt[i] = 0;
+        if (fc2_adds) zero_rows([&](int p) { return recs[p].sorted; });
     } else {
         // The schedule is two kernels back, so complete: this CTA's units and
         // their code bytes are known before FC1 completes.
@@ -339,6 +353,7 @@ __global__ void __maxnreg__(MAX_REG)
     }
 
     const bool comb = !FC1 && SELF && (comb32 != nullptr || comb16 != nullptr);
+    const bool adds = !FC1 && fc2_adds && !comb;  // (then KR == 2)
     const int b = lane_block(lane), m = lane & 3;  // scale block and group phase of this lane
     const uint32_t lb = TAB | (uint32_t)(4 * lane);
     uint32_t phase = 0;                     // parity of the slot's next completion
@@ -532,7 +547,9 @@ __global__ void __maxnreg__(MAX_REG)
                     atomicAdd(out + (size_t)(pr / k) * H + h, weights[pr] * y);
                 }
             };
-            if (FC1 || KR > 1 || comb) {
+            if (adds) {
+                if ((lane & 1) == 0) atomicAdd(out + (size_t)S.ys[pi] * H + h, acc[0]);
+            } else if (FC1 || KR > 1 || comb) {
                 if ((lane & 1) == 0) pout[((size_t)(gs + pi) * KR + kr) * R + h] = acc[0];
             } else if ((lane & 1) == 0) {
                 emit(acc[0]);
@@ -574,7 +591,7 @@ __global__ void __maxnreg__(MAX_REG)
             if (pend) mbar_wait_bounded(bar, phase, nullptr, 0);
             pend = false;
         }
-        if (!FC1 && (KR > 1 || comb)) {
+        if (!FC1 && (KR > 1 || comb) && !adds) {
             // FC2 partials of this job's row tiles are all stored: one fence per
             // thread, then per row tile one arrival; the last of the KR units of
             // a row tile adds the partials in K-range order and writes y.  With
