@@ -171,7 +171,7 @@ moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_
 /* The whole routing in one call: moe_router_logits, moe_route_topk and
  * moe_permute of the same arguments, with the same outputs bit for bit
  * (logits, ids, weights, expert_offsets, sorted_pair, pair_to_sorted).  For
- * small batches (T <= 64, T*k <= 1024, E <= 1024) it is one kernel launch:
+ * small batches (T <= 8, E <= 1024) it is one kernel launch:
  * the CTA that finishes its share of the logits last does the top-k and the
  * permutation (fewer kernel boundaries per layer at decode); otherwise it
  * enqueues the three steps.

@@ -20,6 +20,7 @@ def torch():
     (64, 1024, 1024, 32, 0, True), (7, 512, 48, 5, 0, False), (16, 2048, 128, 1, 1, True),
     (64, 256, 8, 8, 1, False),  # 512 pairs (two 256-pair chunks), every expert in every warp
     (40, 512, 32, 16, 0, True), (64, 4096, 256, 16, 1, True),  # 640 and 1024 pairs
+    (8, 512, 64, 32, 1, True),  # the one-kernel limit: 8 tokens, 256 pairs
     (100, 512, 64, 4, 1, True),  # above the one-kernel limit: the three-step fallback
 ])
 def test_route_matches_stepwise(torch, T, H, E, k, renorm, with_bias):
