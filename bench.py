@@ -41,6 +41,28 @@ VQ2_EXPERT_BYTES = 6_684_672     # codes + scales, gate + up + down, H=4096 I=20
 FP4_EXPERT_BYTES = 13_369_344
 L2_BYTES = 129 * 2 ** 20
 
+# DRAM bytes (read + write) of one expert-FFN call, from one ncu capture of its
+# kernels (profiles/ffn_lut_decode_b1.md: FC1 35,719,424 + 512, FC2 18,543,360
+# at decode batch 1).  Reported only while the kernel sources hash to the ones
+# the counters were taken on.
+TRAFFIC = {"decode_b1": {"bytes": 54_263_296, "profile": "profiles/ffn_lut_decode_b1.md",
+                         "sources": ["ffn_lut.cu", "ffn_common.cuh", "common.cuh"],
+                         "sha256": "533db05d51dc6f602d207de215af8a5545f2b3cf08e3b7ec0aca9220ae501337"}}
+
+
+def measured_traffic(name):
+    t = TRAFFIC.get(name)
+    if t is None:
+        return None, "no ncu capture of this workload's kernels"
+    import hashlib
+    h = hashlib.sha256()
+    for f in t["sources"]:
+        with open(os.path.join(ROOT, "bit_vq_routed_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != t["sha256"]:
+        return None, "kernel sources changed since the ncu capture"
+    return t["bytes"], t["profile"]
+
 WORKLOADS = {
     "decode_b1": dict(T=1, layers=4, zipf=None, fp4_top=0, pool=64,
                       desc="decode batch 1: H4096 I2048 E256 top-8 softmax, all 256 experts resident, "
@@ -363,6 +385,9 @@ def main():
     if rank != 0:
         return
     hbm, bf16, peak_src = measured_peaks()
+    traffic, traffic_src = measured_traffic(args.workload)  # (per expert-FFN call, like achieved)
+    kernels = ("the two self-scheduling table kernels (FC1, FC2)" if T == 1 else
+               "schedule, gather, table, mma.sync and tcgen05 kernels for FC1 and FC2")
     ms_step = r["ms_total"] / args.steps
     value = T * nL * world / (ms_step / 1000.0)
     ffn_avg_ms = float(np.mean(r["ffn_ms"]))
@@ -379,9 +404,10 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16*f16->f32 (bf16 activations)",
         "data": "synthetic (seeded; random weights, no trained checkpoint)", "config": config,
-        "roofline": {"bound": "hbm", "kernel": "moe_vq2_expert_ffn (its kernels: the two table kernels at one token)",
+        "roofline": {"bound": "hbm", "kernel": f"moe_vq2_expert_ffn: {kernels}",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)", "traffic": None,
+                     "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy, burst: the call is timed alone)",
+                     "traffic": traffic, "traffic_source": traffic_src,
                      "algorithmic_bytes_per_launch": bytes_avg, "avg_launch_ms": ffn_avg_ms},
         "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * 4096 * 2 * nL,
