@@ -39,6 +39,9 @@ METRIC = "MoE-layer tokens/s and achieved HBM GB/s of VQ2 code reads vs ~8 TB/s 
 UNIT = "layer-tokens/s"
 VQ2_EXPERT_BYTES = 6_684_672     # codes + scales, gate + up + down, H=4096 I=2048
 FP4_EXPERT_BYTES = 13_369_344
+VQ2_EXPERT_CODE_BYTES = 6_291_456  # codes only
+FP4_EXPERT_CODE_BYTES = 12_582_912
+FFN_FLOP_PER_PAIR = 2 * 3 * 4096 * 2048  # gate, up and down matvecs of one (token, expert) pair
 L2_BYTES = 129 * 2 ** 20
 
 # DRAM bytes (read + write) of one expert-FFN call, from one ncu capture of its
@@ -137,6 +140,18 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return f"{platform.machine()} ({os.cpu_count()} cores)"
 
 
 def dist_env():
@@ -304,9 +319,11 @@ def run_gpu(args, wl, world, rank, local):
             dev.route(pools[L][sl])
             ids = np.unique(dev.ids[:T].cpu().numpy())
             fmts = layers[L].formats[ids]
-            per_slot[(sl, L)] = (int((fmts == ms.FMT_VQ2).sum()) * VQ2_EXPERT_BYTES
-                                 + int((fmts == ms.FMT_FP4).sum()) * FP4_EXPERT_BYTES)
-    code_bytes = [per_slot[(sl, L)] for sl in ffn_slots for L in range(nL)]
+            nv, nf = int((fmts == ms.FMT_VQ2).sum()), int((fmts == ms.FMT_FP4).sum())
+            per_slot[(sl, L)] = (nv * VQ2_EXPERT_BYTES + nf * FP4_EXPERT_BYTES,
+                                 nv * VQ2_EXPERT_CODE_BYTES + nf * FP4_EXPERT_CODE_BYTES)
+    code_bytes = [per_slot[(sl, L)][0] for sl in ffn_slots for L in range(nL)]
+    codes_only = [per_slot[(sl, L)][1] for sl in ffn_slots for L in range(nL)]
     if world > 1:
         t = torch.tensor([ms_total], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -338,7 +355,8 @@ def run_gpu(args, wl, world, rank, local):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(t.item())
         torch.distributed.destroy_process_group()
-    return dict(ms_total=ms_total, ffn_ms=ffn_ms, code_bytes=code_bytes, clocks=clk, e2e_ms=e2e_ms,
+    return dict(ms_total=ms_total, ffn_ms=ffn_ms, code_bytes=code_bytes, codes_only=codes_only, clocks=clk,
+                e2e_ms=e2e_ms,
                 e2e_steps=e2e_steps, launches=launches)
 
 
@@ -376,7 +394,8 @@ def main():
                 "steps": done, "warmup": 0, "ms_per_step": 1000 * el / max(done, 1),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic (seeded; random weights, no trained checkpoint)", "config": config,
-                "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what},
+                "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what,
+                                 "cpu": cpu_model()},
                 "e2e": {"value": tps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -393,6 +412,25 @@ def main():
     ffn_avg_ms = float(np.mean(r["ffn_ms"]))
     bytes_avg = float(np.mean(r["code_bytes"]))
     achieved = bytes_avg / (ffn_avg_ms / 1000.0) / 1e9
+    codes_gbs = float(np.mean(r["codes_only"])) / (ffn_avg_ms / 1000.0) / 1e9
+    # the prefill chunk is a dense contraction: its roofline is the tensor pipe
+    # (fp16 operands; the measured bf16 GEMM rate, fp16 being the same nominal
+    # dense rate on this part)
+    flop = T * 8 * FFN_FLOP_PER_PAIR
+    tensor = T > 64
+    if tensor:
+        hbm_line = {"achieved_gbs": achieved, "peak_gbs": hbm, "algorithmic_bytes_per_launch": bytes_avg}
+        roof = {"bound": "tensor", "achieved": flop / (ffn_avg_ms / 1000.0) / 1e12, "peak": bf16,
+                "unit": "TFLOP/s", "frac": flop / (ffn_avg_ms / 1000.0) / 1e12 / bf16,
+                "peak_source": f"{peak_src} bf16_tflops (cuBLAS bf16 GEMM, burst: the call is timed alone; "
+                               "fp16 has the same nominal dense rate)",
+                "algorithmic_flop_per_launch": flop, "hbm": hbm_line}
+    else:
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy, burst: the call is timed alone)",
+                "algorithmic_bytes_per_launch": bytes_avg}
+    roof.update({"kernel": f"moe_vq2_expert_ffn: {kernels}", "traffic": traffic, "traffic_source": traffic_src,
+                 "avg_launch_ms": ffn_avg_ms, "codes_only_gbs": codes_gbs})
     e2e_value = T * nL * world / (r["e2e_ms"] / r["e2e_steps"] / 1000.0)
     if args.no_cpu:
         tps, cores, what = None, None, "skipped (--no-cpu)"
@@ -404,12 +442,11 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16*f16->f32 (bf16 activations)",
         "data": "synthetic (seeded; random weights, no trained checkpoint)", "config": config,
-        "roofline": {"bound": "hbm", "kernel": f"moe_vq2_expert_ffn: {kernels}",
-                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy, burst: the call is timed alone)",
-                     "traffic": traffic, "traffic_source": traffic_src,
-                     "algorithmic_bytes_per_launch": bytes_avg, "avg_launch_ms": ffn_avg_ms},
-        "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what},
+        "roofline": roof,
+        "other_bytes_per_layer": {"router_weights": 256 * 4096 * 2, "activations": T * 4096 * 2,
+                                  "per_pair_outputs": T * 8 * 4096 * 4 * 2, "outputs": T * 4096 * 4},
+        "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what,
+                         "cpu": cpu_model()},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * 4096 * 2 * nL,
                 "d2h_bytes_per_step": T * 4096 * 4 * nL},
         "gpu_launches": r["launches"],
