@@ -207,6 +207,9 @@ moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* b
     MOE_CHECK_SUPPORTED(H % 256 == 0, "moe_route: H=%d must be a multiple of 256", H);
     MOE_CHECK_SUPPORTED(aligned16(x) && aligned16(w_router) && aligned16(logits) && aligned16(bias),
                         "moe_route: pointers must be 16-byte aligned");
+    if (route_cluster_ok(T, H, E))
+        return launch_route_cluster(x, w_router, bias, H, E, k, renormalize, logits, ids, weights, expert_offsets,
+                                    sorted_pair, pair_to_sorted, stream);
     if (route_fused_ok(T, k, H, E)) {
         if (!ws || ws_bytes < moe_route_workspace_size(T, k, E)) {
             set_error("moe_route: workspace of %zu bytes, %zu required", ws_bytes, moe_route_workspace_size(T, k, E));

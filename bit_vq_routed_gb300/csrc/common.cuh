@@ -265,6 +265,11 @@ moe_status launch_router_logits(const uint16_t* x, const uint16_t* w, const floa
                                 int T, int H, int E, cudaStream_t s);
 moe_status launch_route_topk(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
                              float* weights, cudaStream_t s);
+// One token: the routing over a thread-block cluster (router.cu).
+bool route_cluster_ok(int T, int H, int E);
+moe_status launch_route_cluster(const uint16_t* x, const uint16_t* w, const float* bias, int H, int E, int k,
+                                int renorm, float* logits, int32_t* ids, float* weights, int32_t* offsets,
+                                int32_t* sorted_pair, int32_t* pair_to_sorted, cudaStream_t s);
 bool route_fused_ok(int T, int k, int H, int E);
 moe_status launch_route_fused(const uint16_t* x, const uint16_t* w, const float* bias, int T, int H, int E, int k,
                               int renorm, float* logits, int32_t* ids, float* weights, int32_t* offsets,

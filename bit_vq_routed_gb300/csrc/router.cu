@@ -2,6 +2,8 @@
 #include <float.h>
 #include <limits.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -244,6 +246,102 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 }
 
 
+// Routing of one token by warp 0 of a CTA: top-k of the E logits (read
+// through logit_of), softmax weights, and -- the k ids being distinct -- the
+// sorted order of the k pairs from the ranks of the ids (offsets[e] = number
+// of ids below e).  Bit for bit what route_topk_kernel and permute_kernel give.
+template <int NPER, typename LogitOf>
+__device__ __forceinline__ void route_one_token(LogitOf logit_of, int E, int k, int renorm, int32_t* __restrict__ ids,
+                                                float* __restrict__ weights, int32_t* __restrict__ offsets,
+                                                int32_t* __restrict__ sorted_pair,
+                                                int32_t* __restrict__ pair_to_sorted) {
+    const int lane = threadIdx.x & 31;
+    float v[NPER];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+        const int ee = lane + 32 * i;
+        if (ee < E) {
+            v[i] = logit_of(ee);
+        } else {
+            v[i] = -INFINITY;
+            taken |= 1u << i;
+        }
+    }
+    float bv = -INFINITY;
+    int be = INT_MAX;
+    auto rescan = [&]() {
+        bv = -INFINITY;
+        be = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < NPER; ++i) {
+            const int ee = lane + 32 * i;
+            if (!((taken >> i) & 1) && better(v[i], ee, bv, be)) {
+                bv = v[i];
+                be = ee;
+            }
+        }
+    };
+    rescan();
+    float sel_v = 0.0f;
+    int sel_e = 0;
+    for (int j = 0; j < k; ++j) {
+        float wv2 = bv;
+        int we = be;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const float ov = __shfl_xor_sync(FULL, wv2, off);
+            const int oe = __shfl_xor_sync(FULL, we, off);
+            if (better(ov, oe, wv2, we)) {
+                wv2 = ov;
+                we = oe;
+            }
+        }
+        if (lane == j) {
+            sel_v = wv2;
+            sel_e = we;
+        }
+        if ((we & 31) == lane) {
+            taken |= 1u << (we >> 5);
+            rescan();
+        }
+    }
+    const float top = __shfl_sync(FULL, sel_v, 0);
+    const float num = lane < k ? expf(sel_v - top) : 0.0f;
+    float den = 0.0f;
+    if (renorm) {
+        den = num;
+    } else {
+#pragma unroll
+        for (int i = 0; i < NPER; ++i)
+            if (lane + 32 * i < E) den += expf(v[i] - top);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(FULL, den, off);
+    // the k ids are distinct: rank of pair j = #ids below id_j; per e,
+    // offsets[e] = #ids below e
+    int rank = 0;
+    int cnt[NPER];
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) cnt[i] = 0;
+    for (int j = 0; j < k; ++j) {
+        const int idj = __shfl_sync(FULL, sel_e, j);
+        rank += idj < sel_e;
+#pragma unroll
+        for (int i = 0; i < NPER; ++i) cnt[i] += idj < lane + 32 * i;
+    }
+    if (lane < k) {
+        ids[lane] = sel_e;
+        weights[lane] = num / den;
+        sorted_pair[rank] = lane;
+        pair_to_sorted[lane] = rank;
+    }
+#pragma unroll
+    for (int i = 0; i < NPER; ++i)
+        if (lane + 32 * i < E) offsets[lane + 32 * i] = cnt[i];
+    if (lane == 0) offsets[E] = k;
+}
+
 // Whole routing of a small batch in one launch (the three steps above,
 // bit for bit): CTA (e8, t) computes the logits of token t for 8 experts as
 // router_logits_small_kernel does; the CTA that finishes last (a counter in
@@ -320,94 +418,10 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __rest
     if (!s_last) return;
 
     if (T == 1) {
-        // one token: warp 0 alone (no block barriers): top-k, then the k ids'
-        // ranks give the sorted order, and offsets[e] = #ids below e
+        // one token: warp 0 alone (no block barriers)
         if (warp != 0) return;
-        const float* l = logits;
-        float v[NPER];
-        uint32_t taken = 0;
-#pragma unroll
-        for (int i = 0; i < NPER; ++i) {
-            const int ee = lane + 32 * i;
-            if (ee < E) {
-                v[i] = __ldcg(l + ee);
-            } else {
-                v[i] = -INFINITY;
-                taken |= 1u << i;
-            }
-        }
-        float bv = -INFINITY;
-        int be = INT_MAX;
-        auto rescan = [&]() {
-            bv = -INFINITY;
-            be = INT_MAX;
-#pragma unroll
-            for (int i = 0; i < NPER; ++i) {
-                const int ee = lane + 32 * i;
-                if (!((taken >> i) & 1) && better(v[i], ee, bv, be)) {
-                    bv = v[i];
-                    be = ee;
-                }
-            }
-        };
-        rescan();
-        float sel_v = 0.0f;
-        int sel_e = 0;
-        for (int j = 0; j < k; ++j) {
-            float wv2 = bv;
-            int we = be;
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                const float ov = __shfl_xor_sync(FULL, wv2, off);
-                const int oe = __shfl_xor_sync(FULL, we, off);
-                if (better(ov, oe, wv2, we)) {
-                    wv2 = ov;
-                    we = oe;
-                }
-            }
-            if (lane == j) {
-                sel_v = wv2;
-                sel_e = we;
-            }
-            if ((we & 31) == lane) {
-                taken |= 1u << (we >> 5);
-                rescan();
-            }
-        }
-        const float top = __shfl_sync(FULL, sel_v, 0);
-        const float num = lane < k ? expf(sel_v - top) : 0.0f;
-        float den = 0.0f;
-        if (renorm) {
-            den = num;
-        } else {
-#pragma unroll
-            for (int i = 0; i < NPER; ++i)
-                if (lane + 32 * i < E) den += expf(v[i] - top);
-        }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(FULL, den, off);
-        // the k ids are distinct: rank of pair j = #ids below id_j; per e,
-        // offsets[e] = #ids below e
-        int rank = 0;
-        int cnt[NPER];
-#pragma unroll
-        for (int i = 0; i < NPER; ++i) cnt[i] = 0;
-        for (int j = 0; j < k; ++j) {
-            const int idj = __shfl_sync(FULL, sel_e, j);
-            rank += idj < sel_e;
-#pragma unroll
-            for (int i = 0; i < NPER; ++i) cnt[i] += idj < lane + 32 * i;
-        }
-        if (lane < k) {
-            ids[lane] = sel_e;
-            weights[lane] = num / den;
-            sorted_pair[rank] = lane;
-            pair_to_sorted[lane] = rank;
-        }
-#pragma unroll
-        for (int i = 0; i < NPER; ++i)
-            if (lane + 32 * i < E) offsets[lane + 32 * i] = cnt[i];
-        if (lane == 0) offsets[E] = k;
+        route_one_token<NPER>([&](int ee) { return __ldcg(logits + ee); }, E, k, renorm, ids, weights, offsets,
+                              sorted_pair, pair_to_sorted);
         return;
     }
 
@@ -547,6 +561,91 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __rest
         __syncthreads();
     }
 }
+
+// One token over a thread-block cluster: CTA r of the cluster computes the
+// logits of experts e = 16 r + warp + 16 C i (C CTAs; one expert per warp at
+// a time, as router_logits_small_kernel does), writes them to logits (the
+// call's output) and into the shared memory of CTA 0; the cluster barrier
+// publishes them, and warp 0 of CTA 0 routes the token from shared memory (no
+// global counter, fence or read-back of the logits).
+constexpr int RC_WARPS = 16;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void st_cta0_f32(uint32_t local_addr, float v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(remote) : "r"(local_addr));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int NPER>
+__global__ void __launch_bounds__(32 * RC_WARPS) route_cluster_kernel(const uint16_t* __restrict__ x,
+                                                                      const uint16_t* __restrict__ w,
+                                                                      const float* __restrict__ bias, int H, int E,
+                                                                      int k, int renorm, float* __restrict__ logits,
+                                                                      int32_t* __restrict__ ids,
+                                                                      float* __restrict__ weights,
+                                                                      int32_t* __restrict__ offsets,
+                                                                      int32_t* __restrict__ sorted_pair,
+                                                                      int32_t* __restrict__ pair_to_sorted) {
+    extern __shared__ __align__(16) uint4 xs[];
+    __shared__ float lg[1024];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nch = H / 8;
+    const int per = H / 256;
+    const int stride = gridDim.x * RC_WARPS;
+    constexpr int U = 16;
+    int e = blockIdx.x * RC_WARPS + warp;
+    uint4 wv[U];
+    auto load_w = [&](int ee, int m0) {
+        const uint4* wr = reinterpret_cast<const uint4*>(w + (size_t)min(ee, E - 1) * H);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (m0 + u < per) wv[u] = __ldg(wr + lane + 32 * (m0 + u));
+    };
+    load_w(e, 0);
+    // the activations are complete at launch (no library kernel still running
+    // writes them), so they are read before the wait too
+    for (int i = tid; i < nch; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(x)[i];
+    pdl_wait();
+    pdl_launch_dependents();  // dependents may start their prologues now
+    __syncthreads();
+    for (; e < E; e += stride) {
+        float acc = 0.0f;
+        for (int m0 = 0; m0 < per; m0 += U) {
+            if (m0 > 0) load_w(e, m0);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (m0 + u < per) {
+                    float xf[8], wf[8];
+                    unpack_bf16x8(xs[lane + 32 * (m0 + u)], xf);
+                    unpack_bf16x8(wv[u], wf);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, __fmul_rn(xf[i], wf[i]));
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(FULL, acc, off));
+        if (lane == 0) {
+            const float v = bias ? __fadd_rn(acc, bias[e]) : acc;
+            logits[e] = v;
+            st_cta0_f32((uint32_t)__cvta_generic_to_shared(&lg[e]), v);
+        }
+        if (e + stride < E) load_w(e + stride, 0);
+    }
+    cluster_barrier();  // every CTA's logits are in CTA 0's shared memory
+    if (cluster_rank() != 0 || warp != 0) return;
+    route_one_token<NPER>([&](int ee) { return lg[ee]; }, E, k, renorm, ids, weights, offsets, sorted_pair,
+                          pair_to_sorted);
+}
+
 }  // namespace
 
 moe_status launch_router_logits(const uint16_t* x, const uint16_t* w, const float* bias, float* logits,
@@ -610,6 +709,109 @@ moe_status launch_route_fused(const uint16_t* x, const uint16_t* w, const float*
                                logits, ids, weights, offsets, sorted_pair, pair_to_sorted, counter);
     if (e != cudaSuccess) return cuda_status(e, "moe_route: launch");
     MOE_LAUNCH_CHECK("moe_route: launch");
+    return MOE_OK;
+}
+
+
+// Allows a kernel's clusters above the portable size once per (kernel,
+// device), so that calls inside a stream capture make no attribute call.
+template <typename F>
+static cudaError_t ensure_cluster_attr(F* kern) {
+    constexpr int kMaxDev = 64;
+    static const void* done[8][kMaxDev];
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    int slot = -1;
+    for (int i = 0; i < 8; ++i) {
+        if (done[i][dev] == (const void*)kern) return cudaSuccess;
+        if (slot < 0 && done[i][dev] == nullptr) slot = i;
+    }
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess && slot >= 0) done[slot][dev] = (const void*)kern;
+    return e;
+}
+
+// CTAs of the one-token cluster: 16 where the device can run clusters of that
+// size, else 8, else 0 (no cluster routing).  Checked once per device; the
+// first call of a process is expected outside stream capture.
+static int route_cluster_size() {
+    constexpr int kMaxDev = 64;
+    static int cached[kMaxDev];
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    if (cached[dev] != 0) return cached[dev] > 0 ? cached[dev] : 0;
+    int found = -1;
+    auto kern = route_cluster_kernel<8>;
+    for (int cl : {16, 8}) {
+        if (cl > 8 && ensure_cluster_attr(kern) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)cl);
+        cfg.blockDim = dim3(32 * RC_WARPS);
+        cfg.dynamicSmemBytes = 8192;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)cl;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1) {
+            found = cl;
+            break;
+        }
+        cudaGetLastError();
+    }
+    cached[dev] = found;
+    return found > 0 ? found : 0;
+}
+
+bool route_cluster_ok(int T, int H, int E) {
+    return T == 1 && E <= 1024 && (size_t)H * 2 <= 48 * 1024 && route_cluster_size() > 0;
+}
+
+moe_status launch_route_cluster(const uint16_t* x, const uint16_t* w, const float* bias, int H, int E, int k,
+                                int renorm, float* logits, int32_t* ids, float* weights, int32_t* offsets,
+                                int32_t* sorted_pair, int32_t* pair_to_sorted, cudaStream_t s) {
+    auto kern = E <= 32    ? route_cluster_kernel<1>
+                : E <= 64  ? route_cluster_kernel<2>
+                : E <= 128 ? route_cluster_kernel<4>
+                : E <= 256 ? route_cluster_kernel<8>
+                : E <= 512 ? route_cluster_kernel<16>
+                           : route_cluster_kernel<32>;
+    const int cl = route_cluster_size();
+    if (cl > 8) {
+        cudaError_t e = ensure_cluster_attr(kern);
+        if (e != cudaSuccess) return cuda_status(e, "moe_route: cluster attribute");
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cl);
+    cfg.blockDim = dim3(32 * RC_WARPS);
+    cfg.dynamicSmemBytes = (size_t)H * 2;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    count_launch();
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, x, w, bias, H, E, k, renorm, logits, ids, weights, offsets,
+                                       sorted_pair, pair_to_sorted);
+    if (e != cudaSuccess) return cuda_status(e, "moe_route: cluster launch");
+    MOE_LAUNCH_CHECK("moe_route: cluster launch");
     return MOE_OK;
 }
 

@@ -171,10 +171,12 @@ moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_
 /* The whole routing in one call: moe_router_logits, moe_route_topk and
  * moe_permute of the same arguments, with the same outputs bit for bit
  * (logits, ids, weights, expert_offsets, sorted_pair, pair_to_sorted).  For
- * small batches (T <= 8, E <= 1024) it is one kernel launch:
- * the CTA that finishes its share of the logits last does the top-k and the
- * permutation (fewer kernel boundaries per layer at decode); otherwise it
- * enqueues the three steps.
+ * small batches (T <= 8, E <= 1024) it is one kernel launch (fewer kernel
+ * boundaries per layer at decode): for one token a thread-block cluster
+ * computes the logits, gathers them in one CTA's shared memory and that CTA
+ * routes the token; for 2..8 tokens the CTA that finishes its share of the
+ * logits last does the top-k and the permutation.  Otherwise it enqueues the
+ * three steps.
  * ws: moe_route_workspace_size() bytes of device memory holding a counter;
  * zero-fill it once before the first call (each call leaves it at zero).
  * Calls that share a workspace must not overlap on the GPU. */
