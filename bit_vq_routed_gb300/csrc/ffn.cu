@@ -43,9 +43,13 @@ __device__ unsigned long long block_scan64(unsigned long long v, unsigned long l
 }
 
 constexpr int SP_SMEM = 4096;  // sorted_pair entries staged in shared memory
+constexpr int MAX_TP = LUT_MAX_M * 1024;  // table pairs at most (E <= 1024)
+constexpr size_t SCHED_SMEM = sizeof(int) * (1025 + (MAX_TP + 1) + 4 * MAX_TP + SP_SMEM) + 1024;
 
 // One CTA of 1024 threads.  Expert e with m_e pairs, if resident:
-//   VQ2 with m_e == 1 (and use_lut) -> one activation-table pair;
+//   VQ2 with m_e <= LUT_MAX_M (and use_lut) -> m_e activation-table pairs
+//     (one per token: the expert's codes are streamed once per token, which
+//     costs less than the mma.sync decode at such counts);
 //   VQ2 with m_e >= UMMA_MIN (and use_umma) -> ceil(m_e / UMMA_NT) tcgen05 chunks;
 //   otherwise -> ceil(m_e / MMA_NT) mma.sync chunks.
 // Table pairs are listed sorted by (token, expert) and grouped by token, so
@@ -61,14 +65,15 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
                                                         Chunk* __restrict__ uchunks, int use_umma, int H, int I,
                                                         int C, int4* __restrict__ fc1_range) {
     __shared__ unsigned long long warp_tot[33];
-    __shared__ int s_off[1025];
-    __shared__ __align__(16) int s_tok[1024];  // token of each table pair, by expert (INT_MAX otherwise)
-    __shared__ int s_sorted_tok[1024];
-    __shared__ int s_gs[1025];
-    __shared__ uint8_t s_res[1024];
-    __shared__ int s_sp[SP_SMEM];
-    __shared__ int s_lut_e[1024];  // table pairs in expert order
-    __shared__ int s_rank[1024];   // (token, expert) rank of each table pair, by expert
+    extern __shared__ __align__(16) int sched_smem[];
+    int* s_off = sched_smem;                       // [1025]
+    int* s_gs = s_off + 1025;                      // [MAX_TP + 1] first table pair of each token group
+    int* s_ptok = s_gs + MAX_TP + 1;               // [MAX_TP] token of each table pair (expert order)
+    int* s_pe = s_ptok + MAX_TP;                   // [MAX_TP] expert of each table pair
+    int* s_sorted_tok = s_pe + MAX_TP;             // [MAX_TP] token of each table pair, (token, expert) order
+    int* s_rank = s_sorted_tok + MAX_TP;           // [MAX_TP] (token, expert) rank of each table pair
+    int* s_sp = s_rank + MAX_TP;                   // [SP_SMEM]
+    uint8_t* s_res = reinterpret_cast<uint8_t*>(s_sp + SP_SMEM);  // [1024]
     pdl_wait();
     pdl_launch_dependents();  // dependents may start their prologues now
     const int tid = threadIdx.x;
@@ -86,17 +91,16 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
 
     const int m = tid < E ? s_off[tid + 1] - s_off[tid] : 0;
     const bool res = tid < E && d.resident != 0 && m > 0;
-    const bool lut = res && use_lut && m == 1 && d.format == MOE_FMT_VQ2;
+    const bool lut = res && use_lut && m <= LUT_MAX_M && d.format == MOE_FMT_VQ2;
+    const int nl = lut ? m : 0;  // this expert's table pairs
     const bool um = res && use_umma && m >= UMMA_MIN && d.format == MOE_FMT_VQ2;
     const int n = (res && !lut && !um) ? (m + MMA_NT - 1) / MMA_NT : 0;
     const int nu = um ? (m + UMMA_NT - 1) / UMMA_NT : 0;
-    const int tok = lut ? sp_at(s_off[tid]) / k : 0x7fffffff;
-    s_tok[tid] = tok;
-    // one scan for the three counts (fields of 21 bits: n, nu, table pair)
+    // one scan for the three counts (fields of 21 bits: n, nu, table pairs)
     unsigned long long tot;
     const unsigned long long ex =
-        block_scan64((unsigned long long)n | ((unsigned long long)nu << 21) | ((unsigned long long)lut << 42),
-                     warp_tot, &tot);  // (its barriers also publish s_tok)
+        block_scan64((unsigned long long)n | ((unsigned long long)nu << 21) | ((unsigned long long)nl << 42),
+                     warp_tot, &tot);
     const int cbase = (int)(ex & 0x1fffff), ubase = (int)((ex >> 21) & 0x1fffff);
     const int n_chunks = (int)(tot & 0x1fffff), n_umma = (int)((tot >> 21) & 0x1fffff), n_lut = (int)(tot >> 42);
     for (int c = 0; c < n; ++c) {
@@ -115,44 +119,57 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
         ch.fmt = d.format;
         uchunks[ubase + c] = ch;
     }
+    // the table pairs of this expert (its tokens, in sorted order)
+    const int lbase = (int)(ex >> 42);
+    for (int q = 0; q < nl; ++q) {
+        s_ptok[lbase + q] = sp_at(s_off[tid] + q) / k;
+        s_pe[lbase + q] = tid;
+    }
+    __syncthreads();
     // rank of each table pair in (token, expert) order, one warp per pair:
     // the pairs with a smaller token, or the same token and a smaller expert
-    if (lut) s_lut_e[(int)(ex >> 42)] = tid;
-    __syncthreads();
+    // (an expert has at most one pair per token)
     {
         const int warp = tid >> 5, lane = tid & 31;
         for (int i = warp; i < n_lut; i += 32) {
-            const int e = s_lut_e[i], te = s_tok[e];
+            const int te = s_ptok[i], e = s_pe[i];
             int c = 0;
-            for (int e2 = lane; e2 < E; e2 += 32) c += (s_tok[e2] < te) || (s_tok[e2] == te && e2 < e);
+            for (int j2 = lane; j2 < n_lut; j2 += 32) c += (s_ptok[j2] < te) || (s_ptok[j2] == te && s_pe[j2] < e);
             c = __reduce_add_sync(0xffffffffu, c);
             if (lane == 0) {
-                s_rank[e] = c;
+                s_rank[i] = c;
                 s_sorted_tok[c] = te;
             }
         }
     }
     __syncthreads();
-    const int rank = lut ? s_rank[tid] : 0;
-    const bool first = tid < n_lut && (tid == 0 || s_sorted_tok[tid] != s_sorted_tok[tid - 1]);
+    // token groups over the sorted table pairs, two per thread
+    const int q0 = 2 * tid, q1 = 2 * tid + 1;
+    const int f0 = (q0 < n_lut && (q0 == 0 || s_sorted_tok[q0] != s_sorted_tok[q0 - 1])) ? 1 : 0;
+    const int f1 = (q1 < n_lut && s_sorted_tok[q1] != s_sorted_tok[q1 - 1]) ? 1 : 0;
     unsigned long long n_groups64;
-    const int gid = (int)block_scan64(first ? 1ull : 0ull, warp_tot, &n_groups64);
+    const int gid = (int)block_scan64((unsigned long long)(f0 + f1), warp_tot, &n_groups64);
     const int n_groups = (int)n_groups64;
-    if (first) {
-        grp_start[gid] = tid;
-        s_gs[gid] = tid;
+    if (f0) {
+        grp_start[gid] = q0;
+        s_gs[gid] = q0;
+    }
+    if (f1) {
+        grp_start[gid + f0] = q1;
+        s_gs[gid + f0] = q1;
     }
     if (tid == 0) s_gs[n_groups] = n_lut;
     __syncthreads();
-    if (lut) {
-        // the expert's own thread writes its record at its rank
+    // the expert's own thread writes the records of its table pairs at their ranks
+    for (int q = 0; q < nl; ++q) {
+        const int rank = s_rank[lbase + q];
         LutRec r;
         for (int mtx = 0; mtx < 3; ++mtx) {
             r.codes[mtx] = d.codes[mtx];
             r.scales[mtx] = d.scales[mtx];
         }
-        r.sorted = s_off[tid];
-        r.token = tok;
+        r.sorted = s_off[tid] + q;
+        r.token = s_ptok[lbase + q];
         // the token group of sorted table pair 'rank': the last group start <= rank
         int lo = 0, hi = n_groups;
         while (hi - lo > 1) {
@@ -172,7 +189,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
             const int gs = s_gs[g], gc = g < n_groups ? s_gs[g + 1] - gs : 0;
             return (gs * KR1 + kr * gc) * RT1;
         };
-        int* s_a = s_lut_e;  // (free after the ranking; C + 1 <= 1024 entries)
+        int* s_a = s_pe;  // (free after the ranking; C + 1 <= MAX_TP entries)
         __syncthreads();
         bool ok = J > 0 && J <= C;
         if (ok && tid <= J) s_a[tid] = tid == J ? C : lut_cta_of(start(tid), C, U);
@@ -255,7 +272,9 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
         return launch_lut_fc(false, true, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s,
                              pair_to_sorted, comb32, comb16);
     }
-    cudaError_t e = launch_pdl(schedule_kernel, dim3(1), dim3(1024), 0, s, (const SlotDesc*)t->d_desc, E, offsets,
+    cudaError_t e = ensure_smem_attr(schedule_kernel, (int)SCHED_SMEM);
+    if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule shared memory");
+    e = launch_pdl(schedule_kernel, dim3(1), dim3(1024), SCHED_SMEM, s, (const SlotDesc*)t->d_desc, E, offsets,
                                sorted_pair, P, k, status, header, chunks, recs, grp_start, use_lut,
                                uchunks, use_umma, H, I, num_sms(), reinterpret_cast<int4*>(w + L.range_off));
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule launch");

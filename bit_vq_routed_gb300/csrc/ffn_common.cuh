@@ -13,6 +13,7 @@ constexpr int LUT_KB = 8;      // scale blocks (x 128 inputs) per activation-tab
 constexpr int UMMA_MIN = 32;   // tokens from which an expert takes the tcgen05 path
 constexpr int UMMA_NT = 128;   // tokens per tcgen05 chunk
 constexpr int MAX_LUT_CTAS = 1024;  // grid of the activation-table kernels (one CTA per SM) at most
+constexpr int LUT_MAX_M = 2;   // VQ2 experts with up to this many tokens take the activation-table path
 
 // A run of sorted positions of one expert (tensor-core paths).
 struct Chunk {
@@ -65,7 +66,7 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I)
     WsLayout L;
     long long P = (long long)T * k;
     L.max_chunks = (int)(P / MMA_NT + E);
-    L.max_lut = (int)(P < E ? P : E);  // single-token experts: at most one per expert
+    L.max_lut = (int)(P < (long long)LUT_MAX_M * E ? P : (long long)LUT_MAX_M * E);  // table pairs
     size_t o = 256;
     L.chunks_off = o;
     o = ws_align(o + sizeof(Chunk) * (size_t)L.max_chunks);
