@@ -143,21 +143,24 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
         }
     }
     __syncthreads();
-    // token groups over the sorted table pairs, two per thread
-    const int q0 = 2 * tid, q1 = 2 * tid + 1;
-    const int f0 = (q0 < n_lut && (q0 == 0 || s_sorted_tok[q0] != s_sorted_tok[q0 - 1])) ? 1 : 0;
-    const int f1 = (q1 < n_lut && s_sorted_tok[q1] != s_sorted_tok[q1 - 1]) ? 1 : 0;
+    // token groups over the sorted table pairs, LUT_MAX_M per thread
+    int fl[LUT_MAX_M], nf = 0;
+#pragma unroll
+    for (int r = 0; r < LUT_MAX_M; ++r) {
+        const int q = LUT_MAX_M * tid + r;
+        fl[r] = (q < n_lut && (q == 0 || s_sorted_tok[q] != s_sorted_tok[q - 1])) ? 1 : 0;
+        nf += fl[r];
+    }
     unsigned long long n_groups64;
-    const int gid = (int)block_scan64((unsigned long long)(f0 + f1), warp_tot, &n_groups64);
+    int gid = (int)block_scan64((unsigned long long)nf, warp_tot, &n_groups64);
     const int n_groups = (int)n_groups64;
-    if (f0) {
-        grp_start[gid] = q0;
-        s_gs[gid] = q0;
-    }
-    if (f1) {
-        grp_start[gid + f0] = q1;
-        s_gs[gid + f0] = q1;
-    }
+#pragma unroll
+    for (int r = 0; r < LUT_MAX_M; ++r)
+        if (fl[r]) {
+            grp_start[gid] = LUT_MAX_M * tid + r;
+            s_gs[gid] = LUT_MAX_M * tid + r;
+            ++gid;
+        }
     if (tid == 0) s_gs[n_groups] = n_lut;
     __syncthreads();
     // the expert's own thread writes the records of its table pairs at their ranks

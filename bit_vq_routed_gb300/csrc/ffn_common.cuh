@@ -13,7 +13,7 @@ constexpr int LUT_KB = 8;      // scale blocks (x 128 inputs) per activation-tab
 constexpr int UMMA_MIN = 32;   // tokens from which an expert takes the tcgen05 path
 constexpr int UMMA_NT = 128;   // tokens per tcgen05 chunk
 constexpr int MAX_LUT_CTAS = 1024;  // grid of the activation-table kernels (one CTA per SM) at most
-constexpr int LUT_MAX_M = 2;   // VQ2 experts with up to this many tokens take the activation-table path
+constexpr int LUT_MAX_M = 3;   // VQ2 experts with up to this many tokens take the activation-table path
 
 // A run of sorted positions of one expert (tensor-core paths).
 struct Chunk {
