@@ -114,34 +114,42 @@ __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
     return v > bv || (v == bv && e < be);
 }
 
-// Small-batch router: one CTA of 8 warps per (token, 8 experts); the token's
-// activations sit in shared memory and each lane first loads all of its
-// router-weight chunks, so a warp needs one memory round trip.  Same fixed
-// summation order as router_logits_tiled_kernel (the order moe_vq2.h states).
+// Small-batch router: one CTA of 8 warps per (RS_TG tokens, 8 experts); the
+// tokens' activations sit in shared memory and each lane first loads all of
+// its router-weight chunks, so a warp needs one memory round trip and uses
+// each weight for RS_TG tokens.  Every (token, expert) sum keeps the fixed
+// order of router_logits_tiled_kernel (the order moe_vq2.h states).
+constexpr int RS_TG = 4;
+
 __global__ void __launch_bounds__(256) router_logits_small_kernel(const uint16_t* __restrict__ x,
                                                                   const uint16_t* __restrict__ w,
                                                                   const float* __restrict__ bias,
                                                                   float* __restrict__ logits, int T, int H,
                                                                   int E) {
     extern __shared__ __align__(16) uint4 xs[];
-    const int t = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.y * RS_TG, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntok = min(RS_TG, T - t0);
     const int e = blockIdx.x * 8 + warp;
     const int nch = H / 8;
     const int per = H / 256;  // chunks per lane
     constexpr int U = 16;
-    // the router weights do not depend on earlier kernels: fetch the first
-    // (for H <= 4096 the only) batch of them before waiting on the predecessor
+    // the router weights do not depend on earlier kernels, and the activations
+    // are complete at launch (no library kernel still running writes them):
+    // both are fetched before waiting on the predecessor
     const uint4* wr = reinterpret_cast<const uint4*>(w + (size_t)min(e, E - 1) * H);
     uint4 wv[U];
 #pragma unroll
     for (int u = 0; u < U; ++u)
         if (u < per) wv[u] = __ldg(wr + lane + 32 * u);
+    for (int i = threadIdx.x; i < ntok * nch; i += blockDim.x)
+        xs[i] = reinterpret_cast<const uint4*>(x + (size_t)t0 * H)[i];
     pdl_wait();
     pdl_launch_dependents();  // dependents may start their prologues now
-    for (int i = threadIdx.x; i < nch; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(x + (size_t)t * H)[i];
     __syncthreads();
     if (e >= E) return;
-    float acc = 0.0f;
+    float acc[RS_TG];
+#pragma unroll
+    for (int tt = 0; tt < RS_TG; ++tt) acc[tt] = 0.0f;
     for (int m0 = 0; m0 < per; m0 += U) {
         if (m0 > 0) {
 #pragma unroll
@@ -151,17 +159,29 @@ __global__ void __launch_bounds__(256) router_logits_small_kernel(const uint16_t
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (m0 + u < per) {
-                float xf[8], wf[8];
-                unpack_bf16x8(xs[lane + 32 * (m0 + u)], xf);
+                float wf[8];
                 unpack_bf16x8(wv[u], wf);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, __fmul_rn(xf[i], wf[i]));
+                for (int tt = 0; tt < RS_TG; ++tt) {
+                    if (tt < ntok) {
+                        float xf[8];
+                        unpack_bf16x8(xs[tt * nch + lane + 32 * (m0 + u)], xf);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[tt] = __fadd_rn(acc[tt], __fmul_rn(xf[i], wf[i]));
+                    }
+                }
             }
         }
     }
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(FULL, acc, off));
-    if (lane == 0) logits[(size_t)t * E + e] = bias ? __fadd_rn(acc, bias[e]) : acc;
+    for (int tt = 0; tt < RS_TG; ++tt) {
+        if (tt < ntok) {
+            float a = acc[tt];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) a = __fadd_rn(a, __shfl_xor_sync(FULL, a, off));
+            if (lane == 0) logits[(size_t)(t0 + tt) * E + e] = bias ? __fadd_rn(a, bias[e]) : a;
+        }
+    }
 }
 
 // One warp per token: lane l holds logits l, l+32, ...; each lane keeps its
@@ -651,9 +671,9 @@ __global__ void __launch_bounds__(32 * RC_WARPS) route_cluster_kernel(const uint
 moe_status launch_router_logits(const uint16_t* x, const uint16_t* w, const float* bias, float* logits,
                                 int T, int H, int E, cudaStream_t s) {
     const int threads = 256;
-    const size_t xs_bytes = (size_t)H * 2;
+    const size_t xs_bytes = (size_t)H * 2 * RS_TG;
     if (T <= 64 && xs_bytes <= 48 * 1024) {
-        dim3 grid((unsigned)((E + 7) / 8), (unsigned)T);
+        dim3 grid((unsigned)((E + 7) / 8), (unsigned)((T + RS_TG - 1) / RS_TG));
         cudaError_t e = launch_pdl(router_logits_small_kernel, grid, dim3(threads), xs_bytes, s, x, w, bias, logits, T,
                                    H, E);
         if (e != cudaSuccess) return cuda_status(e, "moe_router_logits: launch");

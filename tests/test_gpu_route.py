@@ -21,6 +21,8 @@ def torch():
     (64, 256, 8, 8, 1, False),  # 512 pairs (two 256-pair chunks), every expert in every warp
     (40, 512, 32, 16, 0, True), (64, 4096, 256, 16, 1, True),  # 640 and 1024 pairs
     (8, 512, 64, 32, 1, True),  # the one-kernel limit: 8 tokens, 256 pairs
+    (1, 4096, 1024, 32, 0, True), (1, 512, 48, 5, 1, False),  # one token over a cluster: 1024 and 48 experts
+    (1, 8192, 300, 8, 1, True),  # one token, two weight batches per lane (H > 4096), ragged expert count
     (100, 512, 64, 4, 1, True),  # above the one-kernel limit: the three-step fallback
 ])
 def test_route_matches_stepwise(torch, T, H, E, k, renorm, with_bias):
