@@ -154,6 +154,22 @@ def cpu_model() -> str:
     return f"{platform.machine()} ({os.cpu_count()} cores)"
 
 
+def max_over_ranks(v: float, device="cuda") -> float:
+    """The slowest rank's figure (the job's time); v itself without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(v)
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world / (ms / 1000.0)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -324,10 +340,7 @@ def run_gpu(args, wl, world, rank, local):
                                  nv * VQ2_EXPERT_CODE_BYTES + nf * FP4_EXPERT_CODE_BYTES)
     code_bytes = [per_slot[(sl, L)][0] for sl in ffn_slots for L in range(nL)]
     codes_only = [per_slot[(sl, L)][1] for sl in ffn_slots for L in range(nL)]
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total)
 
     # end to end through the public API: pinned host tokens in, outputs out
     host_in = [torch.from_numpy(token_pool(wl, L)).view(torch.bfloat16).pin_memory() for L in range(nL)]
@@ -350,10 +363,8 @@ def run_gpu(args, wl, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = max_over_ranks(e2e_ms)
     if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
         torch.distributed.destroy_process_group()
     return dict(ms_total=ms_total, ffn_ms=ffn_ms, code_bytes=code_bytes, codes_only=codes_only, clocks=clk,
                 e2e_ms=e2e_ms,
@@ -408,7 +419,7 @@ def main():
     kernels = ("the two self-scheduling table kernels (FC1, FC2)" if T == 1 else
                "schedule, gather, table, mma.sync and tcgen05 kernels for FC1 and FC2")
     ms_step = r["ms_total"] / args.steps
-    value = T * nL * world / (ms_step / 1000.0)
+    value = job_rate(T * nL, world, ms_step)
     ffn_avg_ms = float(np.mean(r["ffn_ms"]))
     bytes_avg = float(np.mean(r["code_bytes"]))
     achieved = bytes_avg / (ffn_avg_ms / 1000.0) / 1e9
@@ -431,7 +442,7 @@ def main():
                 "algorithmic_bytes_per_launch": bytes_avg}
     roof.update({"kernel": f"moe_vq2_expert_ffn: {kernels}", "traffic": traffic, "traffic_source": traffic_src,
                  "avg_launch_ms": ffn_avg_ms, "codes_only_gbs": codes_gbs})
-    e2e_value = T * nL * world / (r["e2e_ms"] / r["e2e_steps"] / 1000.0)
+    e2e_value = job_rate(T * nL, world, r["e2e_ms"] / r["e2e_steps"])
     if args.no_cpu:
         tps, cores, what = None, None, "skipped (--no-cpu)"
     else:
