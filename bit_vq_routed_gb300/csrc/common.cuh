@@ -201,9 +201,11 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
 // dependents start only when it has finished.  So when a kernel starts, its
 // predecessor has at least passed its own wait, i.e. everything two launches
 // back is complete, and so are the bf16 activations the caller passes in (x):
-// no library kernel that may still be running writes them.  The code before
-// the wait (shared-memory set-up, constant weights, x, and reads of results
-// two launches back) overlaps the predecessor's run.
+// no library kernel that may still be running writes them.  The slot-table
+// writer is launched without programmatic dependent launch, so no later
+// kernel starts before it has finished.  The code before the wait
+// (shared-memory set-up, constant weights, the slot descriptors, x, and reads
+// of results two launches back) overlaps the predecessor's run.
 //
 // Host-side count of kernel launches the library has issued (a launch made
 // inside a stream capture counts once: it becomes one graph node).

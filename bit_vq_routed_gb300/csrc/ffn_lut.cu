@@ -277,12 +277,40 @@ __global__ void __maxnreg__(MAX_REG)
         }
     };
     int pre_kr = -1;
+    // SELF FC1: the slot descriptors do not depend on the kernel before this one
+    // (only the slot-table writer changes them, and it lets no dependent start
+    // before it has finished), so they are staged in the code slots, after the
+    // expert offsets, before the wait: the pair listing then needs one round
+    // trip to global memory instead of two.
+    // (The descriptor words are loaded into registers first, so that their
+    // round trip overlaps the activations'.)
+    constexpr int DW = 4;  // descriptor words per thread at most
+    const int n_dw = E * (int)(sizeof(SlotDesc) / 8);
+    const size_t off_bytes = ((size_t)4 * (E + 1) + 15) & ~(size_t)15;
+    const bool desc_staged = SELF && FC1 && n_dw <= DW * THREADS &&
+                             off_bytes + sizeof(SlotDesc) * E <= (size_t)LOW_SLOTS * SLOT_BYTES;
+    SlotDesc* s_desc = reinterpret_cast<SlotDesc*>(dyn + (low_base - base) + off_bytes);
+    unsigned long long dv[DW];
+    if (desc_staged) {
+        const unsigned long long* src = reinterpret_cast<const unsigned long long*>(desc);
+#pragma unroll
+        for (int r = 0; r < DW; ++r)
+            if (tid + r * THREADS < n_dw) dv[r] = src[tid + r * THREADS];
+    }
     if (SELF && FC1 && KR <= C) {
         pre_kr = (int)(((long long)(blockIdx.x + 1) * KR - 1) / C);
         const int nkb = min(LUT_KB, KB - LUT_KB * pre_kr);
         load_x(0, pre_kr, 128 * nkb);
+    }
+    if (desc_staged) {
+        unsigned long long* dst = reinterpret_cast<unsigned long long*>(s_desc);
+#pragma unroll
+        for (int r = 0; r < DW; ++r)
+            if (tid + r * THREADS < n_dw) dst[tid + r * THREADS] = dv[r];
+    }
+    if (SELF && FC1 && KR <= C) {
         __syncthreads();
-        build_table(nkb);
+        build_table(min(LUT_KB, KB - LUT_KB * pre_kr));
     }
     if (SELF) {
         // FC1: the offsets come from the kernel just before (wait first); FC2:
@@ -304,7 +332,7 @@ __global__ void __maxnreg__(MAX_REG)
             SlotDesc d;
             d.resident = 0;
             d.format = MOE_FMT_VQ2;
-            if (lane < P && S.e_of_s[lane] >= 0) d = desc[S.e_of_s[lane]];
+            if (lane < P && S.e_of_s[lane] >= 0) d = desc_staged ? s_desc[S.e_of_s[lane]] : desc[S.e_of_s[lane]];
             const bool res = lane < P && d.resident != 0 && d.format == MOE_FMT_VQ2;
             const unsigned mask = __ballot_sync(0xffffffffu, res);
             const int idx = __popc(mask & ((1u << lane) - 1u));
