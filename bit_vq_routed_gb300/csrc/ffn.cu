@@ -2,7 +2,8 @@
 //
 // The schedule kernel sorts each resident expert of the call to one path by
 // its token count m_e:
-//   - VQ2, m_e == 1: the activation-table kernels (ffn_lut.cu);
+//   - VQ2, m_e <= LUT_MAX_M: the activation-table kernels (ffn_lut.cu), one
+//     table pair per token;
 //   - VQ2, m_e >= 32: the tcgen05 kernels (ffn_umma.cu);
 //   - otherwise: the mma.sync kernels (ffn_mma.cu), chunks of <= 32 tokens.
 #include "ffn_common.cuh"

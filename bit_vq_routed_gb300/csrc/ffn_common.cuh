@@ -33,12 +33,12 @@ static_assert(sizeof(LutRec) == 64 && offsetof(LutRec, codes) == 0 && offsetof(L
 // Header words at the start of the workspace.
 enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NUMMA = 4 };
 
-// Activation-table pairs (single-token VQ2 experts) are listed sorted by
-// (token, expert) in lut_rec, grouped by token: grp_start holds the first
-// pair of each token group, then n_lut.  p1 / p2
-// hold their FC1 / FC2 K-range partial sums, lut_cnt one arrival counter per
-// (table pair, FC2 row tile of 16 outputs); range holds each FC1 CTA's unit
-// range, computed by the schedule.
+// Activation-table pairs (VQ2 experts with at most LUT_MAX_M tokens, one pair
+// per token) are listed sorted by (token, expert) in lut_rec, grouped by
+// token: grp_start holds the first pair of each token group, then n_lut.
+// p1 / p2 hold their FC1 / FC2 K-range partial sums, lut_cnt one arrival
+// counter per (table pair, FC2 row tile of 16 outputs); range holds each FC1
+// CTA's unit range, computed by the schedule.
 // Experts with at least UMMA_MIN pairs (possible once T >= UMMA_MIN) take
 // the tcgen05 path (uchunks: chunks of <= UMMA_NT sorted positions); the
 // tensor-core paths read x16s (fp16 activations gathered by sorted position)

@@ -1,6 +1,7 @@
-// Activation-table path of the expert FFN, for VQ2 experts that receive a
-// single token in this call (every expert at decode batch 1, most of them at
-// small batches).
+// Activation-table path of the expert FFN, for VQ2 experts that receive at
+// most LUT_MAX_M tokens in this call (every expert at decode batch 1, most of
+// them at small batches): one table pair per (token, expert), the expert's
+// codes streamed once per token.
 //
 // For one token, every code byte c of group G (inputs 4G .. 4G+3) adds
 //     scale[r, G/32] * sign(c) * dot(codebook[c & 127], x[4G .. 4G+3])

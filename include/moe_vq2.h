@@ -202,7 +202,7 @@ moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* b
  * over the same ids; weights fp32 [T,k] from moe_route_topk.
  * ws: moe_vq2_expert_ffn_workspace_size(T, k, E, H, I) bytes of device
  * memory (scratch: the schedule, the fp32 intermediate a [P, I] and the
- * K-range partial sums of single-token experts).
+ * K-range partial sums of the activation-table pairs).
  * Requires H % 256 == 0, I % 128 == 0, k <= 32, x 16-byte aligned. */
 size_t moe_vq2_expert_ffn_workspace_size(int T, int k, int E, int H, int I);
 moe_status moe_vq2_expert_ffn(const moe_slot_table* table, const uint16_t* x,
