@@ -52,7 +52,8 @@ constexpr size_t SCHED_SMEM = sizeof(int) * (1025 + (MAX_TP + 1) + 4 * MAX_TP + 
 //     (one per token: the expert's codes are streamed once per token, which
 //     costs less than the mma.sync decode at such counts);
 //   VQ2 with m_e >= UMMA_MIN (and use_umma) -> ceil(m_e / UMMA_NT) tcgen05 chunks;
-//   otherwise -> ceil(m_e / MMA_NT) mma.sync chunks.
+//   otherwise -> mma.sync chunks of MMA_NT_VQ2 (VQ2) or MMA_NT_FP4 (FP4)
+//     tokens, the VQ2 chunks listed first.
 // Table pairs are listed sorted by (token, expert) and grouped by token, so
 // the experts of one token share each activation table.  pair_status of every
 // pair from the residency of its expert; the header's error word is cleared.
@@ -95,20 +96,25 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
     const bool lut = res && use_lut && m <= LUT_MAX_M && d.format == MOE_FMT_VQ2;
     const int nl = lut ? m : 0;  // this expert's table pairs
     const bool um = res && use_umma && m >= UMMA_MIN && d.format == MOE_FMT_VQ2;
-    const int n = (res && !lut && !um) ? (m + MMA_NT - 1) / MMA_NT : 0;
+    const bool fp4 = d.format == MOE_FMT_FP4;
+    const int nt_e = fp4 ? MMA_NT_FP4 : MMA_NT_VQ2;  // tokens per mma.sync chunk of this expert
+    const int n = (res && !lut && !um) ? (m + nt_e - 1) / nt_e : 0;
     const int nu = um ? (m + UMMA_NT - 1) / UMMA_NT : 0;
     // one scan for the three counts (fields of 21 bits: n, nu, table pairs)
     unsigned long long tot;
     const unsigned long long ex =
-        block_scan64((unsigned long long)n | ((unsigned long long)nu << 21) | ((unsigned long long)nl << 42),
+        block_scan64((unsigned long long)(fp4 ? 0 : n) | ((unsigned long long)nu << 21) | ((unsigned long long)nl << 42),
                      warp_tot, &tot);
-    const int cbase = (int)(ex & 0x1fffff), ubase = (int)((ex >> 21) & 0x1fffff);
-    const int n_chunks = (int)(tot & 0x1fffff), n_umma = (int)((tot >> 21) & 0x1fffff), n_lut = (int)(tot >> 42);
+    unsigned long long tot4;  // the FP4 chunks, listed after the VQ2 ones
+    const unsigned long long ex4 = block_scan64(fp4 ? (unsigned long long)n : 0ull, warp_tot, &tot4);
+    const int n_vq2 = (int)(tot & 0x1fffff);
+    const int cbase = fp4 ? n_vq2 + (int)ex4 : (int)(ex & 0x1fffff), ubase = (int)((ex >> 21) & 0x1fffff);
+    const int n_chunks = n_vq2 + (int)tot4, n_umma = (int)((tot >> 21) & 0x1fffff), n_lut = (int)(tot >> 42);
     for (int c = 0; c < n; ++c) {
         Chunk ch;
         ch.expert = tid;
-        ch.start = s_off[tid] + c * MMA_NT;
-        ch.count = min(MMA_NT, m - c * MMA_NT);
+        ch.start = s_off[tid] + c * nt_e;
+        ch.count = min(nt_e, m - c * nt_e);
         ch.fmt = d.format;
         chunks[cbase + c] = ch;
     }
@@ -221,6 +227,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
         header[HDR_ERR] = 0;
         header[HDR_NGROUPS] = n_groups;
         header[HDR_NUMMA] = n_umma;
+        header[HDR_NVQ2] = n_vq2;
     }
     for (int s2 = tid; s2 < P; s2 += 1024) {
         int lo = 0, hi = E;  // find e with off[e] <= s2 < off[e+1]

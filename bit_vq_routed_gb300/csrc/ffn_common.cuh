@@ -8,7 +8,8 @@
 
 namespace moe {
 
-constexpr int MMA_NT = 32;     // tokens per mma.sync chunk (four n8 MMA tiles)
+constexpr int MMA_NT_VQ2 = 32; // tokens per mma.sync chunk of a VQ2 expert (four n8 MMA tiles)
+constexpr int MMA_NT_FP4 = 16; // tokens per mma.sync chunk of an FP4 expert (two n8 MMA tiles)
 constexpr int LUT_KB = 8;      // scale blocks (x 128 inputs) per activation-table K-range
 constexpr int UMMA_MIN = 32;   // tokens from which an expert takes the tcgen05 path
 constexpr int UMMA_NT = 128;   // tokens per tcgen05 chunk
@@ -31,7 +32,8 @@ static_assert(sizeof(LutRec) == 64 && offsetof(LutRec, codes) == 0 && offsetof(L
               "table pair record layout");
 
 // Header words at the start of the workspace.
-enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NUMMA = 4 };
+// HDR_NVQ2: the chunks list holds the VQ2 chunks first, then the FP4 ones.
+enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NUMMA = 4, HDR_NVQ2 = 5 };
 
 // Activation-table pairs (VQ2 experts with at most LUT_MAX_M tokens, one pair
 // per token) are listed sorted by (token, expert) in lut_rec, grouped by
@@ -65,7 +67,7 @@ __host__ __device__ inline int lut_cta_of(long long start, int C, int U) { retur
 __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I) {
     WsLayout L;
     long long P = (long long)T * k;
-    L.max_chunks = (int)(P / MMA_NT + E);
+    L.max_chunks = (int)(P / MMA_NT_FP4 + E);
     L.max_lut = (int)(P < (long long)LUT_MAX_M * E ? P : (long long)LUT_MAX_M * E);  // table pairs
     size_t o = 256;
     L.chunks_off = o;

@@ -25,19 +25,29 @@ namespace {
 
 constexpr int WARPS = 8;
 constexpr int THREADS = 32 * WARPS;
-constexpr int NTOK = MMA_NT;        // tokens per chunk (4 n8 tiles)
-constexpr int SLAB = 512;           // inputs per slab (VQ2; FP4 slabs are 256 inputs)
-constexpr int XSTRIDE = 2 * SLAB + 32;  // bytes per token row of a slab (padding: B-fragment banks)
-constexpr int TILE_CODES = 2048;    // one 16-row tile x one slab: 512 VQ2 inputs or 256 FP4 inputs
-constexpr int TILE_SCALES = 128;    // 16 rows x 4 fp16 (VQ2) or x 8 ue8m0 (FP4)
-constexpr int WARP_BYTES = 2 * (TILE_CODES + TILE_SCALES);  // per warp per slab (two tiles)
 constexpr int CB_COPIES = 16;
 
-struct __align__(16) Smem {
-    uint2 cbt[256 * CB_COPIES];
-    uint8_t xs[2][NTOK * XSTRIDE];
-    uint8_t w[2][WARPS][WARP_BYTES];
+// Two configurations.  VQ2 chunks: 32 tokens, 512-input slabs, one CTA per SM
+// (an expert's codes are read once per 32 tokens).  FP4 chunks (the most
+// routed experts, at small batches with few tokens each): 16 tokens, 256-input
+// slabs, two CTAs per SM, whose independent slab barriers hide more latency.
+template <int NTOK_>
+struct MmaCfg {
+    static constexpr int NTOK = NTOK_;                   // tokens per chunk
+    static constexpr int NNT = NTOK / 8;                 // n8 MMA tiles per chunk
+    static constexpr int SLAB = NTOK == 32 ? 512 : 256;  // inputs per slab (VQ2; FP4 slabs are half as many)
+    static constexpr int XSTRIDE = 2 * SLAB + 32;        // bytes per token row of a slab (padding: B-fragment banks)
+    static constexpr int TILE_CODES = 4 * SLAB;          // one 16-row tile x one slab
+    static constexpr int TILE_SCALES = SLAB / 4;         // 16 rows x SLAB/128 fp16 (VQ2) or x SLAB/64 ue8m0 (FP4)
+    static constexpr int WARP_BYTES = 2 * (TILE_CODES + TILE_SCALES);  // per warp per slab (two tiles)
+    static constexpr int MIN_BLOCKS = NTOK == 32 ? 1 : 2;
+    struct __align__(16) Smem {
+        uint2 cbt[256 * CB_COPIES];
+        uint8_t xs[2][NTOK * XSTRIDE];
+        uint8_t w[2][WARPS][WARP_BYTES];
+    };
 };
+static_assert(MMA_NT_VQ2 == 32 && MMA_NT_FP4 == 16, "mma.sync configurations");
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
@@ -53,12 +63,17 @@ __device__ __forceinline__ uint32_t sh_u32(const uint8_t* p) { return *reinterpr
 
 // FC1 = true: A tiles are the gate and up tiles of 16 I-rows, B = x16s (K = H);
 // FC1 = false: A tiles are two down tiles (32 H-rows), B = a16 (K = I).
-template <bool FC1>
-__global__ void __launch_bounds__(THREADS, 1)
+template <bool FC1, int NTOK_>
+__global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_>::MIN_BLOCKS)
     ffn_mma_kernel(const SlotDesc* __restrict__ desc, const uint16_t* __restrict__ codebook,
                    const uint16_t* __restrict__ bsrc, const int32_t* __restrict__ sorted_pair,
                    const float* __restrict__ weights, int k, int H, int I, const int* __restrict__ header,
-                   const Chunk* __restrict__ chunks, uint16_t* __restrict__ a16, float* __restrict__ out, int mode) {
+                   const Chunk* __restrict__ chunks, uint16_t* __restrict__ a16, float* __restrict__ out, int mode,
+                   int fp4_part) {
+    using Cfg = MmaCfg<NTOK_>;
+    using Smem = typename Cfg::Smem;
+    constexpr int NTOK = Cfg::NTOK, NNT = Cfg::NNT, SLAB = Cfg::SLAB, XSTRIDE = Cfg::XSTRIDE;
+    constexpr int TILE_CODES = Cfg::TILE_CODES, TILE_SCALES = Cfg::TILE_SCALES;
     extern __shared__ __align__(16) uint8_t dyn[];
     Smem& S = *reinterpret_cast<Smem*>(dyn);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -70,7 +85,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     pdl_wait();
     pdl_launch_dependents();  // dependents may start their prologues now
-    const int n_chunks = header[HDR_NCHUNKS];
+    // the chunks list holds the VQ2 chunks, then the FP4 ones: this launch's part
+    const int c0 = fp4_part ? header[HDR_NVQ2] : 0;
+    const int n_chunks = (fp4_part ? header[HDR_NCHUNKS] : header[HDR_NVQ2]) - c0;
     const int n_items = n_chunks * n_rg;
     if ((int)blockIdx.x >= n_items) return;
     for (int idx = tid; idx < 256 * CB_COPIES; idx += THREADS) {
@@ -82,7 +99,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint8_t* cbt = reinterpret_cast<const uint8_t*>(&S.cbt[0]) + 8 * (lane & 15);
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const Chunk ch = chunks[item / n_rg];
+        const Chunk ch = chunks[c0 + item / n_rg];
         const int rg = item % n_rg;
         const SlotDesc& d = desc[ch.expert];
         const bool vq2 = ch.fmt == MOE_FMT_VQ2;
@@ -135,11 +152,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             cp_async_commit();
         };
 
-        float acc[2][4][4];
+        float acc[2][NNT][4];
 #pragma unroll
         for (int t = 0; t < 2; ++t)
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
+            for (int nt = 0; nt < NNT; ++nt)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) acc[t][nt][q] = 0.0f;
 
@@ -159,19 +176,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint8_t* wb = &S.w[buf][warp][0];
             if (vq2) {
                 for (int kb = 0; kb < kn / 128; ++kb) {
-                    float tmp[2][4][4];
+                    float tmp[2][NNT][4];
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
 #pragma unroll
-                        for (int nt = 0; nt < 4; ++nt)
+                        for (int nt = 0; nt < NNT; ++nt)
 #pragma unroll
                             for (int q = 0; q < 4; ++q) tmp[t][nt][q] = 0.0f;
 #pragma unroll
                     for (int s = 0; s < 8; ++s) {
                         const int g = 4 * s + j;  // this thread's group in the scale block
-                        uint2 b[4];
+                        uint2 b[NNT];
 #pragma unroll
-                        for (int nt = 0; nt < 4; ++nt)
+                        for (int nt = 0; nt < NNT; ++nt)
                             if (nt < n_nt) b[nt] = sh_u64(xs + (8 * nt + i) * XSTRIDE + 2 * (kb * 128 + 4 * g));
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
@@ -179,7 +196,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             const uint2 lo = sh_u64(cbt + 128u * (pr & 0xffu));
                             const uint2 hi = sh_u64(cbt + 128u * (pr >> 8));
 #pragma unroll
-                            for (int nt = 0; nt < 4; ++nt)
+                            for (int nt = 0; nt < NNT; ++nt)
                                 if (nt < n_nt) mma_16816(tmp[t][nt], lo.x, hi.x, lo.y, hi.y, b[nt].x, b[nt].y);
                         }
                     }
@@ -189,7 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const float s_lo = __half2float(__ushort_as_half((unsigned short)sh_u16(sa + 2 * i)));
                         const float s_hi = __half2float(__ushort_as_half((unsigned short)sh_u16(sa + 2 * (i + 8))));
 #pragma unroll
-                        for (int nt = 0; nt < 4; ++nt) {
+                        for (int nt = 0; nt < NNT; ++nt) {
                             acc[t][nt][0] = fmaf(s_lo, tmp[t][nt][0], acc[t][nt][0]);
                             acc[t][nt][1] = fmaf(s_lo, tmp[t][nt][1], acc[t][nt][1]);
                             acc[t][nt][2] = fmaf(s_hi, tmp[t][nt][2], acc[t][nt][2]);
@@ -201,20 +218,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int kt = 0; kt < kn / 64; ++kt) {
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {  // 32-element scale blocks
-                        float tmp[2][4][4];
+                        float tmp[2][NNT][4];
 #pragma unroll
                         for (int t = 0; t < 2; ++t)
 #pragma unroll
-                            for (int nt = 0; nt < 4; ++nt)
+                            for (int nt = 0; nt < NNT; ++nt)
 #pragma unroll
                                 for (int q = 0; q < 4; ++q) tmp[t][nt][q] = 0.0f;
 #pragma unroll
                         for (int s2 = 0; s2 < 2; ++s2) {
                             const int s = 2 * half + s2;
                             const int e0 = kt * 64 + 16 * s + 2 * j;  // element of k-slot 2j
-                            uint32_t b0[4], b1[4];
+                            uint32_t b0[NNT], b1[NNT];
 #pragma unroll
-                            for (int nt = 0; nt < 4; ++nt)
+                            for (int nt = 0; nt < NNT; ++nt)
                                 if (nt < n_nt) {
                                     b0[nt] = sh_u32(xs + (8 * nt + i) * XSTRIDE + 2 * e0);
                                     b1[nt] = sh_u32(xs + (8 * nt + i) * XSTRIDE + 2 * (e0 + 8));
@@ -225,7 +242,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 uint32_t r0, r1, r2, r3;  // row i lo-k, row i hi-k, row i+8 lo-k, row i+8 hi-k
                                 e2m1x8_to_f16x8(w, r0, r1, r2, r3);
 #pragma unroll
-                                for (int nt = 0; nt < 4; ++nt)
+                                for (int nt = 0; nt < NNT; ++nt)
                                     if (nt < n_nt) mma_16816(tmp[t][nt], r0, r2, r1, r3, b0[nt], b1[nt]);
                             }
                         }
@@ -235,7 +252,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             const uint32_t e_lo = sa[i], e_hi = sa[i + 8];
                             const float s_lo = e8m0_to_float(e_lo), s_hi = e8m0_to_float(e_hi);
 #pragma unroll
-                            for (int nt = 0; nt < 4; ++nt) {
+                            for (int nt = 0; nt < NNT; ++nt) {
                                 acc[t][nt][0] = fmaf(s_lo, tmp[t][nt][0], acc[t][nt][0]);
                                 acc[t][nt][1] = fmaf(s_lo, tmp[t][nt][1], acc[t][nt][1]);
                                 acc[t][nt][2] = fmaf(s_hi, tmp[t][nt][2], acc[t][nt][2]);
@@ -250,7 +267,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
         // epilogue: acc[t][nt] holds (row i | i+8 of tile t, tokens 8nt + 2j | +1)
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
+        for (int nt = 0; nt < NNT; ++nt) {
             if (nt >= n_nt) continue;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -281,22 +298,31 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
-size_t mma_smem_bytes() { return sizeof(Smem); }
 
-moe_status launch_mma_fc(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
-                         int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s) {
+template <int NTOK_>
+static moe_status launch_mma_cfg(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights,
+                                 int k, int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s) {
+    using Smem = typename MmaCfg<NTOK_>::Smem;
     const int* header = reinterpret_cast<const int*>(ws);
     const Chunk* chunks = reinterpret_cast<const Chunk*>(ws + L.chunks_off);
     const uint16_t* x16s = reinterpret_cast<const uint16_t*>(ws + L.x16s_off);
     uint16_t* a16 = reinterpret_cast<uint16_t*>(ws + L.a16_off);
-    auto kern = fc1 ? ffn_mma_kernel<true> : ffn_mma_kernel<false>;
+    auto kern = fc1 ? ffn_mma_kernel<true, NTOK_> : ffn_mma_kernel<false, NTOK_>;
     cudaError_t e = ensure_smem_attr(kern, (int)sizeof(Smem));
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: mma kernel shared memory");
-    e = launch_pdl(kern, dim3((unsigned)num_sms()), dim3(THREADS), sizeof(Smem), s, (const SlotDesc*)t->d_desc,
-                   t->codebook, fc1 ? x16s : (const uint16_t*)a16, sorted_pair, weights, k, t->H, t->I, header,
-                   chunks, a16, out, mode);
+    e = launch_pdl(kern, dim3((unsigned)(MmaCfg<NTOK_>::MIN_BLOCKS * num_sms())), dim3(THREADS), sizeof(Smem), s,
+                   (const SlotDesc*)t->d_desc, t->codebook, fc1 ? x16s : (const uint16_t*)a16, sorted_pair, weights, k,
+                   t->H, t->I, header, chunks, a16, out, mode, NTOK_ == MMA_NT_FP4 ? 1 : 0);
     if (e != cudaSuccess) return cuda_status(e, fc1 ? "moe_vq2_expert_ffn: FC1 launch" : "moe_vq2_expert_ffn: FC2 launch");
     return MOE_OK;
+}
+
+moe_status launch_mma_fc(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
+                         int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s) {
+    moe_status st = launch_mma_cfg<MMA_NT_VQ2>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s);
+    if (st == MOE_OK && t->n_fp4 > 0)
+        st = launch_mma_cfg<MMA_NT_FP4>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s);
+    return st;
 }
 
 }  // namespace moe

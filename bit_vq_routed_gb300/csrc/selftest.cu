@@ -21,11 +21,13 @@
 // Cases, each with the path it reaches:
 //   route4     moe_router_logits + moe_route_topk + moe_permute, 4 tokens;
 //   route4f    moe_route (one fused kernel), 4 tokens;
-//   vq2_t4     per-pair FFN (one-token table kernels, small-batch mma.sync)
-//              + moe_combine;
+//   vq2_t4     per-pair FFN (table kernels: every expert has at most three
+//              tokens) + moe_combine;
 //   vq2_scat   the same in fused-scatter mode;
 //   vq2_t1     moe_route + moe_vq2_expert_ffn_combine on token 0 alone (the
 //              self-scheduling single-token kernels with the combine inside);
+//   vq2_t16    16 tokens (the four repeated): 4 or 8 tokens per routed
+//              expert, the small-batch mma.sync kernels;
 //   vq2_t128   128 tokens (the four repeated): every routed expert has at
 //              least 32 tokens, so the tcgen05 kernels run;
 //   mix_t4 / mix_t128   the mixed-format layer (FP4 experts 1, 3, 5, 7);
@@ -375,6 +377,12 @@ moe_status run_cases(moe_slot_table* vq2, moe_slot_table* mixed, const Buffers& 
     ST_TRY(moe_vq2_expert_ffn_combine(vq2, b.x, b.offsets, b.sorted_pair, b.pair_to_sorted, b.weights, 1, k,
                                       b.ypair, b.status, b.out, nullptr, b.ffn_ws, b.ffn_ws_bytes, s));
     ST_TRY(check_out(b, 1, 0, X::out_vq2, "vq2_t1", s));
+
+    // 16 tokens: 4 or 8 per routed expert (mma.sync)
+    ST_TRY(route(b, 16, s));
+    ST_TRY(check_routing(b, 16, true, "route16", s));
+    ST_TRY(ffn_combine(vq2, b, 16, s));
+    ST_TRY(check_out(b, 16, 0, X::out_vq2, "vq2_t16", s));
 
     // 128 tokens: every routed expert takes at least 32 of them
     ST_TRY(route(b, ST_TMAX, s));

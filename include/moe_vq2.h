@@ -272,7 +272,7 @@ moe_status moe_combine(const float* ypair, const int32_t* pair_to_sorted, const 
  * against a reference at boot).  Runs a tiny layer (hidden 256, intermediate
  * 128, 8 experts, top-2) through the entry points above on the current
  * device: the router and top-k step by step and fused, the permutation, the
- * expert FFN on 1, 4 and 128 tokens (the one-token table kernels, the
+ * expert FFN on 1, 4, 16 and 128 tokens (the table kernels, the
  * small-batch mma.sync kernels and the tcgen05 kernels), an all-VQ2 and a
  * mixed VQ2/FP4 layer, both output modes, the fused expert-FFN + combine and
  * a layer with two experts not resident.  The inputs are drawn on the GPU
