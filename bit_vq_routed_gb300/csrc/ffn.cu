@@ -5,7 +5,8 @@
 //   - VQ2, m_e <= LUT_MAX_M: the activation-table kernels (ffn_lut.cu), one
 //     table pair per token;
 //   - VQ2, m_e >= 32: the tcgen05 kernels (ffn_umma.cu);
-//   - otherwise: the mma.sync kernels (ffn_mma.cu), chunks of <= 32 tokens.
+//   - otherwise: the mma.sync kernels (ffn_mma.cu), chunks of <= 32 (VQ2) or
+//     <= 16 (FP4) tokens.
 #include "ffn_common.cuh"
 
 namespace moe {

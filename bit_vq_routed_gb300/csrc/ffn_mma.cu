@@ -1,5 +1,6 @@
-// Tensor-core mma.sync path of the expert FFN for experts with 2..31 tokens
-// in the call (and FP4 experts with any count below the tcgen05 threshold).
+// Tensor-core mma.sync path of the expert FFN for VQ2 experts with more tokens
+// than the activation-table path takes and fewer than the tcgen05 threshold,
+// and for FP4 experts with any count.
 //
 // mma.sync m16n8k16 (fp16 in, fp32 accumulate) on weights decoded in
 // registers.  A VQ2 code byte indexes a sign-folded codebook (256 entries:
@@ -11,13 +12,13 @@
 // applied in fp32 once per 128-input block.  FP4 (e2m1) bytes become f16x2
 // with cvt and are scaled per 32 inputs.
 //
-// A CTA of 8 warps takes items (chunk of <= 32 tokens of one expert, 8 x 32
-// weight rows); each warp owns two 16-row tiles (FC1: the gate and the up
-// tile of the same rows; FC2: two down tiles), so every activation fragment
-// feeds two tiles.  K is walked in slabs of 512 inputs: the chunk's fp16
-// activations (gathered by sorted position) and each warp's code and scale
-// tiles for the next slab stream into shared memory with cp.async while the
-// current slab is computed.
+// A CTA of 8 warps takes items (chunk of tokens of one expert, 8 x 32 weight
+// rows); each warp owns two 16-row tiles (FC1: the gate and the up tile of the
+// same rows; FC2: two down tiles), so every activation fragment feeds two
+// tiles.  K is walked in slabs: the chunk's fp16 activations (gathered by
+// sorted position) and each warp's code and scale tiles for the next slab
+// stream into shared memory with cp.async while the current slab is computed.
+// Chunk size, slab length and CTAs per SM differ for VQ2 and FP4 (MmaCfg).
 #include "ffn_common.cuh"
 
 namespace moe {
