@@ -54,7 +54,9 @@ EXPORTED = [
     "moe_route_topk", "moe_permute_workspace_size", "moe_permute",
     "moe_vq2_expert_ffn_workspace_size", "moe_vq2_expert_ffn", "moe_vq2_expert_ffn_noalloc", "moe_combine",
     "moe_launch_count", "moe_route_workspace_size", "moe_route", "moe_vq2_expert_ffn_combine",
-    "moe_selftest",
+    "moe_selftest", "moe_expert_cache_slot_bytes", "moe_expert_cache_create", "moe_expert_cache_set_host",
+    "moe_expert_cache_fetch", "moe_expert_cache_slot_of", "moe_expert_cache_stats", "moe_expert_cache_plan",
+    "moe_expert_cache_destroy", "moe_expert_cache_set_host_image",
 ]
 
 
@@ -93,6 +95,15 @@ def load(path: Optional[str] = None, build_if_stale: bool = True):
         "moe_route": ([P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, Z, P], I),
         "moe_vq2_expert_ffn_combine": ([P, P, P, P, P, P, I, I, P, P, P, P, P, Z, P], I),
         "moe_selftest": ([P], I),
+        "moe_expert_cache_slot_bytes": ([I, I, I], Z),
+        "moe_expert_cache_create": ([P, P, Z, Z, ctypes.POINTER(P)], I),
+        "moe_expert_cache_set_host": ([P, I, ctypes.POINTER(_ExpertDesc)], I),
+        "moe_expert_cache_fetch": ([P, P, I, P, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)], I),
+        "moe_expert_cache_slot_of": ([P, I], I),
+        "moe_expert_cache_stats": ([P] + [ctypes.POINTER(ctypes.c_uint64)] * 4, I),
+        "moe_expert_cache_plan": ([I, I, P, P, P, ctypes.c_uint64, P, I, P, P, ctypes.POINTER(I)], I),
+        "moe_expert_cache_destroy": ([P, P], I),
+        "moe_expert_cache_set_host_image": ([P, I, I, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -287,4 +298,114 @@ def moe_vq2_expert_ffn_combine(table: "SlotTable", x, expert_offsets, sorted_pai
                                              _stream(stream)))
 
 
-from .layer import GraphedForward, MoELayer, upload_layer  # noqa: E402  (the layer helper uses the functions above)
+# ------------------------------------------------------------------ expert cache
+
+def moe_expert_cache_slot_bytes(H: int, I: int, fmt: int) -> int:
+    """Bytes of one cache slot for an expert of format fmt."""
+    return int(load().moe_expert_cache_slot_bytes(H, I, fmt))
+
+
+def moe_expert_cache_plan(num_experts: int, slot_expert, counts, last_step, step: int, request):
+    """Host-only planning step of the expert cache.  slot_expert (int32),
+    counts and last_step (uint64) are numpy arrays updated in place; returns
+    (fill_slot, evicted, n_unplaced) for the requests."""
+    import numpy as np
+    for a, dt in ((slot_expert, np.int32), (counts, np.uint64), (last_step, np.uint64)):
+        if not (isinstance(a, np.ndarray) and a.dtype == dt and a.flags.c_contiguous):
+            raise ValueError(f"expected a contiguous numpy {dt.__name__} array")
+    req = np.ascontiguousarray(request, dtype=np.int32)
+    fill = np.empty(req.size, np.int32)
+    ev = np.empty(req.size, np.int32)
+    left = ctypes.c_int(0)
+    vp = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+    _check(load().moe_expert_cache_plan(num_experts, slot_expert.size, vp(slot_expert), vp(counts), vp(last_step),
+                                        step, vp(req), req.size, vp(fill), vp(ev), ctypes.byref(left)))
+    return fill, ev, left.value
+
+
+def _host_ptr(t: torch.Tensor) -> int:
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError("expected a page-locked (pinned) host tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+class ExpertCache:
+    """moe_expert_cache_*: slot-table entries filled on a miss from pinned
+    host copies of the experts' packed buffers, into slots of a device pool
+    (a uint8 CUDA tensor this object keeps).  Keeps references to the host
+    tensors it was given."""
+
+    def __init__(self, table: SlotTable, pool: torch.Tensor, slot_bytes: int):
+        self.lib = load()
+        self.table, self.pool, self.slot_bytes = table, pool, slot_bytes
+        h = ctypes.c_void_p()
+        _check(self.lib.moe_expert_cache_create(table.handle, _ptr(pool), pool.numel() * pool.element_size(),
+                                                slot_bytes, ctypes.byref(h)))
+        self.handle = h
+        self.num_slots = pool.numel() * pool.element_size() // slot_bytes
+        self._host = {}
+
+    def set_host(self, expert_id: int, fmt: int, codes: Sequence[torch.Tensor], scales: Sequence[torch.Tensor]):
+        H, I = self.table.H, self.table.I
+        for m in range(3):  # the packed sizes the fetch copies (the C side trusts them)
+            rows, K = (H, I) if m == 2 else (I, H)
+            want = (rows * K // 4, rows * K // 128 * 2) if fmt == MOE_FMT_VQ2 else (rows * K // 2, rows * K // 32)
+            got = (codes[m].numel() * codes[m].element_size(), scales[m].numel() * scales[m].element_size())
+            if got != want:
+                raise ValueError(f"expert {expert_id} matrix {m}: {got} bytes of codes/scales, expected {want}")
+        d = _ExpertDesc()
+        d.format = fmt
+        for m in range(3):
+            d.codes[m] = _host_ptr(codes[m])
+            d.scales[m] = _host_ptr(scales[m])
+        _check(self.lib.moe_expert_cache_set_host(self.handle, expert_id, ctypes.byref(d)))
+        self._host[expert_id] = (list(codes), list(scales))
+
+    def set_host_image(self, expert_id: int, fmt: int, image: torch.Tensor):
+        """One pinned uint8 block in the slot's layout (host_expert_image):
+        fetched with one copy."""
+        want = moe_expert_cache_slot_bytes(self.table.H, self.table.I, fmt)
+        if image.numel() * image.element_size() != want:
+            raise ValueError(f"expert {expert_id}: image of {image.numel() * image.element_size()} bytes, "
+                             f"expected {want}")
+        _check(self.lib.moe_expert_cache_set_host_image(self.handle, expert_id, fmt, _host_ptr(image)))
+        self._host[expert_id] = image
+
+    def fetch(self, experts, stream=None) -> dict:
+        """One step: makes the named experts resident (see the C header for
+        the eviction rule).  Returns n_fetched, n_unplaced and recapture."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(experts).ravel(), dtype=np.int32)
+        nf, nu, rc = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+        _check(self.lib.moe_expert_cache_fetch(self.handle, ids.ctypes.data_as(ctypes.c_void_p), ids.size,
+                                               _stream(stream), ctypes.byref(nf), ctypes.byref(nu),
+                                               ctypes.byref(rc)))
+        return dict(n_fetched=nf.value, n_unplaced=nu.value, recapture=bool(rc.value))
+
+    def slot_of(self, expert_id: int) -> int:
+        return int(self.lib.moe_expert_cache_slot_of(self.handle, expert_id))
+
+    def stats(self) -> dict:
+        v = [ctypes.c_uint64(0) for _ in range(4)]
+        _check(self.lib.moe_expert_cache_stats(self.handle, *[ctypes.byref(x) for x in v]))
+        return dict(hits=v[0].value, misses=v[1].value, unplaced=v[2].value, bytes_fetched=v[3].value)
+
+    def destroy(self, stream=None):
+        if self.handle is not None:
+            h, self.handle = self.handle, None
+            if self.table.handle is not None:  # (the table's entries die with the table)
+                _check(self.lib.moe_expert_cache_destroy(h, _stream(stream)))
+
+    def __del__(self):
+        try:
+            if self.handle is not None and torch.cuda.is_initialized():
+                self.destroy()
+                torch.cuda.synchronize()
+        except Exception:
+            pass
+
+
+from .layer import (GraphedForward, MissFetchForward, MoELayer, host_expert, host_expert_image,  # noqa: E402,F401
+                    upload_layer)

@@ -1,5 +1,6 @@
 // Logical -> packed weight layouts (see moe_vq2.h), and the slot writer.
 #include "common.cuh"
+#include "slot_batch.cuh"
 
 namespace moe {
 namespace {
@@ -42,6 +43,11 @@ __global__ void fp4_pack_scales(const uint8_t* __restrict__ src, int rows, int K
 
 __global__ void slot_set_kernel(SlotDesc* table, int expert_id, SlotDesc d) { table[expert_id] = d; }
 
+// (distinct ids: the writes of one batch do not depend on their order)
+__global__ void slot_set_many_kernel(SlotDesc* table, SlotBatch b) {
+    if ((int)threadIdx.x < b.n) table[b.ids[threadIdx.x]] = b.d[threadIdx.x];
+}
+
 unsigned grid_for(long n) {
     long b = (n + 255) / 256;
     long cap = (long)num_sms() * 16;
@@ -67,6 +73,14 @@ moe_status launch_fp4_pack(const uint8_t* codes, const uint8_t* scales, int rows
     count_launch();
     fp4_pack_scales<<<grid_for((long)rows * K / 32), 256, 0, s>>>(scales, rows, K, ps);
     MOE_LAUNCH_CHECK("moe_fp4_pack: launch");
+    return MOE_OK;
+}
+
+moe_status launch_slot_set_many(SlotDesc* table, const SlotBatch& b, cudaStream_t s) {
+    if (b.n <= 0) return MOE_OK;
+    count_launch();
+    slot_set_many_kernel<<<1, SLOT_BATCH, 0, s>>>(table, b);
+    MOE_LAUNCH_CHECK("moe_expert_cache_fetch: slot-table launch");
     return MOE_OK;
 }
 

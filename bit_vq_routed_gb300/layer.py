@@ -146,6 +146,117 @@ class GraphedForward:
         return self.out
 
 
+def host_expert(fmt: int, codes: Sequence, scales: Sequence, stream=None, device="cuda"):
+    """Packs one expert on the device (upload_expert) and returns page-locked
+    host copies of the packed buffers (codes[3], scales[3]): the host-resident
+    base that an ExpertCache fetches from."""
+    pc, ps = upload_expert(fmt, codes, scales, stream, device)
+    torch.cuda.synchronize()
+    return [c.cpu().pin_memory() for c in pc], [s.cpu().pin_memory() for s in ps]
+
+
+def slot_layout(H: int, I: int, fmt: int):
+    """(offset, bytes) of the six packed buffers of an expert in a cache slot
+    or host image: codes of gate, up, down, then their scales, each offset
+    rounded up to 256 bytes (the layout moe_expert_cache_set_host_image
+    reads)."""
+    out, off = [], 0
+    for b in range(6):
+        rows, K = (H, I) if b % 3 == 2 else (I, H)
+        n = (rows * K // 4 if b < 3 else rows * K // 128 * 2) if fmt == MOE_FMT_VQ2 else \
+            (rows * K // 2 if b < 3 else rows * K // 32)
+        out.append((off, n))
+        off += (n + 255) // 256 * 256
+    return out, off
+
+
+def host_expert_image(fmt: int, codes: Sequence, scales: Sequence, stream=None, device="cuda"):
+    """Packs one expert on the device straight into a block in the slot's
+    layout and returns a page-locked host copy of it (one uint8 tensor): the
+    host-resident base that an ExpertCache fetches with one copy."""
+    from . import moe_vq2_pack
+    I, H4 = np.asarray(codes[0]).shape
+    H = H4 * (4 if fmt == MOE_FMT_VQ2 else 2)
+    lay, total = slot_layout(H, I, fmt)
+    img = torch.zeros(total, dtype=torch.uint8, device=device)
+    for m in range(3):
+        (oc, nc), (osc, ns) = lay[m], lay[3 + m]
+        c = _dev(codes[m], torch.uint8, device)
+        pc = img[oc:oc + nc].view(c.shape)
+        if fmt == MOE_FMT_VQ2:
+            s = _dev(scales[m], torch.float16, device)
+            moe_vq2_pack(c, s, pc, img[osc:osc + ns].view(torch.float16).view(s.shape), stream)
+        else:
+            s = _dev(scales[m], torch.uint8, device)
+            moe_fp4_pack(c, s, pc, img[osc:osc + ns].view(s.shape), stream)
+    torch.cuda.synchronize()
+    return img.cpu().pin_memory()
+
+
+class MissFetchForward:
+    """The forward of a layer whose experts live in host memory, with the GPU
+    as an expert cache (vLLM-Moet page, "2-bit experts on vLLM v0.24.0",
+    "Experts beyond VRAM": a miss is fetched and the step's graph replayed).
+
+    The step's work is captured as two CUDA graphs, split at the routing:
+    each step replays the routing graph, reads the routed ids back (one
+    device-to-host copy and one wait), names them to the cache (routing
+    counts; misses are copied in) and then replays the expert graph (expert
+    FFN and combine) once, over experts that are all resident when they fit
+    in the cache's slots.  Its output is then bit-identical to a forward with
+    every expert resident.  The expert graph is captured again when a fetch
+    changes whether the table holds FP4 experts (the expert-FFN call picks
+    its kernels by that on the host)."""
+
+    def __init__(self, layer: MoELayer, cache, T: int, device="cuda"):
+        self.layer, self.cache, self.T = layer, cache, T
+        self.x = torch.zeros(T, layer.H, dtype=torch.bfloat16, device=device)
+        self.out = layer.out[:T]
+        self.ids_host = torch.empty(T, layer.k, dtype=torch.int32).pin_memory()
+        layer.forward(self.x)  # first eager call: kernel attributes are set outside capture
+        torch.cuda.synchronize()
+        self.g_route = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_route):
+            layer.route(self.x)
+        self._capture_experts()
+        self.steps = 0
+        self.fetch_steps = 0
+        self.captures = 1
+        self.last = None
+
+    def _capture_experts(self):
+        T, k = self.T, self.layer.k
+        self.g_ffn = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_ffn):
+            self.layer.experts(self.x, MOE_PER_PAIR)
+            moe_combine(self.layer.ypair[:T * k], self.layer.pair_to_sorted[:T * k], self.layer.weights[:T],
+                        self.layer.pair_status[:T * k], k, self.out)
+
+    def step(self, x=None, fetch_events=None) -> torch.Tensor:
+        """x: bf16 [T, H] (copied into the graphs' input), or None when
+        self.x already holds the tokens.  Returns the fp32 [T, H] output.
+        fetch_events: optional pair of CUDA events recorded on the stream
+        around the fetch; self.last holds the fetch's result."""
+        if x is not None:
+            self.x.copy_(x, non_blocking=True)
+        self.g_route.replay()
+        self.ids_host.copy_(self.layer.ids[:self.T], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        if fetch_events is not None:
+            fetch_events[0].record()
+        r = self.cache.fetch(self.ids_host.numpy())
+        if fetch_events is not None:
+            fetch_events[1].record()
+        self.last = r
+        if r["recapture"]:
+            self._capture_experts()
+            self.captures += 1
+        self.g_ffn.replay()
+        self.steps += 1
+        self.fetch_steps += 1 if r["n_fetched"] else 0
+        return self.out
+
+
 def upload_layer(H, I, E, k, T_max, codebook, w_router, bias, experts, renormalize=1, resident=None,
                  stream=None, device="cuda"):
     """Builds a MoELayer and makes resident the experts in ``resident`` (all

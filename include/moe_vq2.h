@@ -132,6 +132,120 @@ moe_status moe_slot_table_evict(moe_slot_table* t, int expert_id, cudaStream_t s
 moe_status moe_slot_table_destroy(moe_slot_table* t);
 
 /* ---------------------------------------------------------------------- */
+/* Expert cache: misses fetched from host memory (vLLM-Moet page, "2-bit    */
+/* experts on vLLM v0.24.0", "Experts beyond VRAM": the base lives in host  */
+/* RAM, the GPU is an expert cache, a miss is fetched and the step's graph  */
+/* replayed, bit-identical to a resident forward; Tandem-vLLM page, "How it */
+/* works": the GPU cache holds the most-used experts)                       */
+/* ---------------------------------------------------------------------- */
+/*
+ * The cache fills the entries of one slot table from page-locked host copies
+ * of the experts' packed buffers, into fixed-size slots carved from a device
+ * pool that the caller owns.  The expert kernels read the table's
+ * descriptors on the device, so a CUDA graph of a forward pass captured once
+ * stays valid while the cache changes which experts are resident: after a
+ * fetch, replaying the same graph computes the newly resident experts.  The
+ * result of a pair does not depend on the slot (the address) its expert's
+ * buffers sit at, nor on which other experts are resident, so a forward
+ * replayed after the fetch of its misses is bit-identical to a forward with
+ * every expert resident.
+ *
+ * Eviction by routing counts: every fetch call is one step; each distinct
+ * expert it names gains one count and is stamped with the step number.  A
+ * named expert that is not resident takes the free slot with the lowest
+ * index, else the slot of the resident expert that this step does not name
+ * with the smallest (count, last step named, expert id).  Experts named in
+ * the step are never evicted by it; when the step names more experts than
+ * there are slots, the ones that find no slot stay non-resident (their pairs
+ * are reported in pair_status, as for any non-resident expert).
+ */
+typedef struct moe_expert_cache moe_expert_cache;
+
+typedef struct moe_host_expert {
+    int format;                /* MOE_FMT_VQ2 or MOE_FMT_FP4                        */
+    const void* codes[3];      /* page-locked HOST copies of the packed codes       */
+    const void* scales[3];     /* and scales of gate [I,H], up [I,H], down [H,I]    */
+} moe_host_expert;
+
+/* Bytes one slot needs for an expert of the given format at hidden H and
+ * intermediate I: the six packed buffers, each starting on a 256-byte
+ * boundary.  Returns 0 for an unknown format or a non-positive shape. */
+size_t moe_expert_cache_slot_bytes(int H, int I, int format);
+
+/* Creates a cache for `table` over the caller's device memory `pool`
+ * (pool_bytes, 256-byte aligned), cut into floor(pool_bytes / slot_bytes)
+ * slots of slot_bytes each (a multiple of 256, at least
+ * moe_expert_cache_slot_bytes(H, I, MOE_FMT_VQ2)).  The pool and the table
+ * must outlive the cache.  Host memory only: allocates and enqueues nothing
+ * on the device. */
+moe_status moe_expert_cache_create(moe_slot_table* table, void* pool, size_t pool_bytes, size_t slot_bytes,
+                                   moe_expert_cache** out);
+
+/* Registers the host copy of expert_id (replacing an earlier one; a resident
+ * copy of the expert is not refreshed).  The buffers are not copied now and
+ * must stay valid and unchanged while the cache may fetch them; they must be
+ * page-locked (cudaHostAlloc / cudaHostRegister), so that the fetch copies
+ * are asynchronous.  The format's buffers must fit in one slot. */
+moe_status moe_expert_cache_set_host(moe_expert_cache* c, int expert_id, const moe_host_expert* h);
+
+/* Registers the host copy of expert_id as one block: `image` holds, in
+ * page-locked host memory of moe_expert_cache_slot_bytes(H, I, format)
+ * bytes, the six packed buffers at their slot offsets (codes of gate, up,
+ * down, then scales of gate, up, down; each at the sum of the sizes before
+ * it, every size rounded up to 256 bytes).  A fetch of such an expert is one
+ * host-to-device copy instead of six. */
+moe_status moe_expert_cache_set_host_image(moe_expert_cache* c, int expert_id, int format, const void* image);
+
+/* One step: makes the experts in `experts` (HOST array of n ids, repeats
+ * allowed) resident, in the order named, by the rule above.  It enqueues on
+ * `stream` the host-to-device copies of every miss into its slot, then one
+ * kernel (per 32 entries) that writes the table: the entries of the experts
+ * replaced cleared, those of the new ones set.  The work that read a
+ * replaced expert must be ordered before `stream`, and nothing may read the
+ * table on another stream while the fetch runs (both hold when the forward
+ * passes run on the same stream).  An expert already set in the table by
+ * the caller is left as it is.  Every named expert must have a host copy,
+ * else nothing is enqueued (MOE_ERR_INVALID_ARG).  After MOE_ERR_CUDA the
+ * cache and the table may disagree: destroy both.
+ * Outputs (each may be NULL): n_fetched = experts copied in, n_unplaced =
+ * named experts left non-resident for lack of a slot, recapture = 1 if the
+ * call changed whether the table holds any FP4 expert (the expert-FFN call
+ * chooses its kernels by that on the host, so a graph captured before must
+ * then be captured again), else 0. */
+moe_status moe_expert_cache_fetch(moe_expert_cache* c, const int32_t* experts, int n, cudaStream_t stream,
+                                  int* n_fetched, int* n_unplaced, int* recapture);
+
+/* Slot index holding expert_id, or -1 (not resident through this cache, or
+ * an out-of-range id).  Host bookkeeping: valid in stream order. */
+int moe_expert_cache_slot_of(const moe_expert_cache* c, int expert_id);
+
+/* Counters since creation: experts named and resident already (hits), named
+ * and fetched (misses), named and left without a slot (unplaced), and the
+ * bytes copied from host to device. */
+moe_status moe_expert_cache_stats(const moe_expert_cache* c, uint64_t* hits, uint64_t* misses,
+                                  uint64_t* unplaced, uint64_t* bytes_fetched);
+
+/* Host-only planning step of moe_expert_cache_fetch, for callers that manage
+ * slots and copies themselves (and testable without a GPU).  State arrays
+ * (read and updated): slot_expert [num_slots] = expert held by each slot or
+ * -1; counts [num_experts] and last_step [num_experts] = routing counts and
+ * the last step each expert was named (0 = never).  `step` numbers this call
+ * (> every last_step).  request: n expert ids.  Outputs, one entry per
+ * request: fill_slot[i] = the slot that request i is copied into, or -1 (a
+ * hit, a repeat of an earlier request of the call, or no slot: see
+ * placed); evicted[i] = the expert that slot held before, or -1.
+ * Returns MOE_ERR_INVALID_ARG for a bad id, a slot_expert entry out of range
+ * or held twice, or a step not above every last_step (nothing is updated). */
+moe_status moe_expert_cache_plan(int num_experts, int num_slots, int32_t* slot_expert, uint64_t* counts,
+                                 uint64_t* last_step, uint64_t step, const int32_t* request, int n,
+                                 int32_t* fill_slot, int32_t* evicted, int* n_unplaced);
+
+/* Enqueues on `stream` the eviction from the table of every expert that the
+ * cache made resident, then frees the host bookkeeping.  The pool may be
+ * reused once that work has run. */
+moe_status moe_expert_cache_destroy(moe_expert_cache* c, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* Hot path                                                                */
 /* ---------------------------------------------------------------------- */
 
