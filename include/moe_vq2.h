@@ -226,8 +226,8 @@ moe_status moe_expert_cache_stats(const moe_expert_cache* c, uint64_t* hits, uin
                                   uint64_t* unplaced, uint64_t* bytes_fetched);
 
 /* Host-only planning step of moe_expert_cache_fetch, for callers that manage
- * slots and copies themselves (and testable without a GPU).  State arrays
- * (read and updated): slot_expert [num_slots] = expert held by each slot or
+ * slots and copies themselves (and testable without a GPU).  Every array
+ * here is a HOST array.  State arrays (read and updated): slot_expert [num_slots] = expert held by each slot or
  * -1; counts [num_experts] and last_step [num_experts] = routing counts and
  * the last step each expert was named (0 = never).  `step` numbers this call
  * (> every last_step).  request: n expert ids.  Outputs, one entry per
