@@ -192,12 +192,13 @@ def token_pool(wl, L):
 
 # --------------------------------------------------------------- CPU oracle arm
 
-def oracle_time(wl, layers, budget_s: float, max_steps: int):
+def oracle_time(wl, layers, budget_s: float, max_steps: int, threads: int = 0):
     """Times the CPU oracle over whole steps (every layer, one batch each)
-    until the budget is spent.  Weights are drawn before the clock starts."""
+    until the budget is spent, on `threads` host threads (0 = every core).
+    Weights are drawn before the clock starts."""
     import oracle
     O = oracle.default
-    cores = O.set_threads(os.cpu_count() or 1)
+    cores = O.set_threads(threads or os.cpu_count() or 1)
     pools = [token_pool(wl, L) for L in range(len(layers))]
     T = wl["T"]
     if T > 64:  # prefill: a bounded token sample of the chunk
@@ -604,6 +605,10 @@ def main():
     else:
         layers = make_layers(wl)
         tps, cores, what, done, el = oracle_time(wl, layers, budget_s=args.cpu_budget, max_steps=4)
+    single = None
+    if not args.no_cpu and T == 1:  # the oracle on one core too, one step
+        s_tps, s_cores, s_what, _, _ = oracle_time(wl, layers[:1], budget_s=1.0, max_steps=1, threads=1)
+        single = {"value": s_tps, "unit": UNIT, "cores": s_cores, "sample": s_what}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -613,7 +618,7 @@ def main():
         "other_bytes_per_layer": {"router_weights": 256 * 4096 * 2, "activations": T * 4096 * 2,
                                   "per_pair_outputs": T * 8 * 4096 * 4 * 2, "outputs": T * 4096 * 4},
         "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what,
-                         "cpu": cpu_model()},
+                         "cpu": cpu_model(), "single_core": single},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * 4096 * 2 * nL,
                 "d2h_bytes_per_step": T * 4096 * 4 * nL},
         "gpu_launches": r["launches"],
