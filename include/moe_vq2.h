@@ -158,6 +158,11 @@ moe_status moe_slot_table_destroy(moe_slot_table* t);
  * the step are never evicted by it; when the step names more experts than
  * there are slots, the ones that find no slot stay non-resident (their pairs
  * are reported in pair_status, as for any non-resident expert).
+ *
+ * A cache is used by one host thread at a time (its calls are not
+ * synchronised with each other).  The caller must not set or evict, through
+ * moe_slot_table_set / _evict, the entries of experts the cache holds; an
+ * entry the caller evicts anyway frees its slot at the next fetch.
  */
 typedef struct moe_expert_cache moe_expert_cache;
 

@@ -125,3 +125,17 @@ def test_route_rejects_bad_args(lib):
     null_x = list(args)
     null_x[0] = None
     assert lib.moe_route(*null_x) == bv.MOE_ERR_INVALID_ARG
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    if gcc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("gcc or the CUDA headers are missing")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "moe_vq2.h"\nint main(void) { return moe_version() > 0 ? 0 : 1; }\n')
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I",
+                        os.path.dirname(HEADER), "-I", cuda_inc, str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
