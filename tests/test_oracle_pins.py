@@ -145,6 +145,24 @@ def test_router_canonical_order_worked_example():
     assert np.float32(float((x.astype(np.float64) * w).sum())) == np.float32(g["expect_exact_fp32"][0][0])
 
 
+def test_router_butterfly_order_worked_example():
+    g = keyed("router_butterfly_order.txt")
+    H = int(g["H"][0][0])
+    x = np.zeros((1, H), np.float32)
+    w = np.zeros((1, H), np.float32)
+    x[0, 0] = float(g["x0"][0][0])
+    w[0, 0] = float(g["w0"][0][0])
+    for h in g["h_ones"][0]:
+        x[0, int(h)] = w[0, int(h)] = 1.0
+    l = O.router_logits(ms.bf16_bits(x), ms.bf16_bits(w))
+    assert l[0, 0] == np.float32(g["expect_canonical"][0][0])
+    assert np.float32(g["expect_canonical"][0][0]) != np.float32(g["expect_xor1_first"][0][0])
+    seq = np.float32(0)
+    for h in range(H):
+        seq = np.float32(seq + np.float32(x[0, h] * w[0, h]))
+    assert seq == np.float32(g["expect_sequential"][0][0])
+
+
 def test_router_logits_vs_fp64_matmul():
     layer = ms.Layer(ms.LayerSpec(H=1024, I=128, E=16, k=4, seed=9, zipf_s=1.1))
     x = ms.tokens(6, 1024, seed=9)

@@ -29,6 +29,18 @@ MISTAKES = {
     "fp4_nibble_order": ("unsigned nib = h ? (v >> 4) : (v & 15);",
                          "unsigned nib = h ? (v & 15) : (v >> 4);"),
     "bias_dropped": ("if (bias) s = s + bias[e];", "(void)bias;"),
+    "permute_not_stable": ("    for (int p = 0; p < P; ++p) {\n        int s = cursor[ids[p]]++;",
+                           "    for (int p = P - 1; p >= 0; --p) {\n        int s = cursor[ids[p]]++;"),
+    "down_scales_from_up": ("decode_matrix(fmt, c_down, s_down, cb, H, I, Wd)",
+                            "decode_matrix(fmt, c_down, s_up, cb, H, I, Wd)"),
+    "fp4_scale_block_64": ("e8m0_value(scales[(size_t)r * KB + col / 32])",
+                           "e8m0_value(scales[(size_t)r * KB + col / 64])"),
+    "renormalize_ignored": ("if (renormalize)", "if (0)"),
+    "fp16_subnormal_exponent": ("ldexp((double)fr, -24)", "ldexp((double)fr, -25)"),
+    "butterfly_order_reversed": ("for (int off = 16; off >= 1; off /= 2)", "for (int off = 1; off <= 16; off *= 2)"),
+    "up_uses_gate_codes": ("decode_matrix(fmt, c_up, s_up, cb, I, H, Wu)",
+                           "decode_matrix(fmt, c_gate, s_up, cb, I, H, Wu)"),
+    "ue8m0_bias_126": ("ldexp(1.0, (int)e - 127)", "ldexp(1.0, (int)e - 126)"),
 }
 
 
