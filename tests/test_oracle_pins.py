@@ -299,6 +299,20 @@ def test_single_expert_top1_is_plain_swiglu_mlp():
     assert np.allclose(r["out"], ref, rtol=1e-12, atol=1e-12)
 
 
+def test_token_sample_is_a_restriction_of_the_full_layer():
+    # the prefill parity test asks the oracle for a sample of the tokens only:
+    # the sampled run must equal the full run's rows for those tokens, exactly
+    spec = ms.LayerSpec(H=256, I=128, E=8, k=2, seed=12, zipf_s=1.1)
+    layer = ms.Layer(spec)
+    x = ms.tokens(9, 256, seed=12)
+    full = O.moe_layer(layer, x)
+    sel = np.array([7, 0, 4])
+    sub = O.moe_layer(layer, x, tokens=sel)
+    assert np.array_equal(sub["tokens"], sel)
+    assert np.array_equal(sub["out"], full["out"][sel])
+    assert np.array_equal(sub["ids"], full["ids"]) and np.array_equal(sub["weights"], full["weights"])
+
+
 def test_residency_partial_plus_remainder_is_full():
     # nothing is skipped or substituted: resident part + remainder = whole layer
     spec = ms.LayerSpec(H=256, I=128, E=16, k=4, seed=11, zipf_s=1.1, fp4_top=4)

@@ -1,7 +1,10 @@
 """Each plausible mistake planted in a copy of the oracle must make at least
 one pin in test_oracle_pins.py fail.  The mistakes are planted in a temporary
-copy of oracle/moe_oracle.c on the CPU; the committed oracle is untouched."""
+copy of oracle/moe_oracle.c (the arithmetic) or of oracle/__init__.py (how
+the layer strings the steps together) on the CPU; the committed oracle is
+untouched."""
 import os
+import shutil
 import subprocess
 import sys
 
@@ -56,4 +59,35 @@ def test_planted_mistake_is_caught(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"planted mistake {name} passed every pin:\n{r.stdout[-2000:]}"
+
+
+# Mistakes in the layer's composition (oracle/__init__.py).
+MISTAKES_PY = {
+    "token_row_of_pair": ("X = xf[[p // k for p in pairs]]", "X = xf[[p % k for p in pairs]]"),
+    "ypair_by_sorted_position": ("pairs = [int(sp[s]) for s in pairs]", "pairs = [int(s) for s in pairs]"),
+    "remainder_is_partial": ("remainder = self.combine(wsel, ysel, 1 - inc_res[sel])",
+                             "remainder = self.combine(wsel, ysel, inc_res[sel])"),
+    "weights_not_selected": ("wsel = w[sel]", "wsel = w[:len(sel)]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MISTAKES_PY))
+def test_planted_composition_mistake_is_caught(name, tmp_path):
+    old, new = MISTAKES_PY[name]
+    pkg = tmp_path / "oracle"
+    pkg.mkdir()
+    shutil.copy(SRC, pkg / "moe_oracle.c")
+    src = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
+    assert src.count(old) == 1, f"pattern for {name} not found exactly once"
+    (pkg / "__init__.py").write_text(src.replace(old, new))
+    env = dict(os.environ, PYTHONPATH=os.pathsep.join([str(tmp_path), ROOT]))
+    env.pop("MOE_ORACLE_LIB", None)
+    # the pins must import the mutant package, not the committed one
+    probe = subprocess.run([sys.executable, "-c", "import oracle; print(oracle.__file__)"], cwd=str(tmp_path),
+                           env=env, capture_output=True, text=True, timeout=120)
+    assert probe.stdout.strip().startswith(str(tmp_path)), probe.stdout + probe.stderr
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "--rootdir", str(tmp_path), os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=str(tmp_path), env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"planted mistake {name} passed every pin:\n{r.stdout[-2000:]}"
