@@ -44,6 +44,13 @@ MISTAKES = {
     "up_uses_gate_codes": ("decode_matrix(fmt, c_up, s_up, cb, I, H, Wu)",
                            "decode_matrix(fmt, c_gate, s_up, cb, I, H, Wu)"),
     "ue8m0_bias_126": ("ldexp(1.0, (int)e - 127)", "ldexp(1.0, (int)e - 126)"),
+    "vq2_index_six_bits": ("int idx = c & 127;", "int idx = c & 63;"),
+    "e2m1_mantissa_quarter": ("ldexp(1.0 + 0.5 * m, ex - 1)", "ldexp(1.0 + 0.25 * m, ex - 1)"),
+    "fp16_normal_exponent": ("ldexp((double)(1024 + fr), ex - 25)", "ldexp((double)(1024 + fr), ex - 24)"),
+    "matvec_drops_last_input": ("for (int c = 0; c < K; ++c) s += w[c] * x[c];",
+                                "for (int c = 0; c < K - 1; ++c) s += w[c] * x[c];"),
+    "silu_sign": ("g[r] = g[r] / (1.0 + exp(-g[r])) * u[r];", "g[r] = g[r] / (1.0 + exp(g[r])) * u[r];"),
+    "topk_excludes_nothing": ("taken[best] = 1;", "(void)taken;"),
 }
 
 
