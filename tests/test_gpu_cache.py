@@ -29,7 +29,9 @@ def _cached(layer, T, slots, fmt_for_slots):
     s = layer.spec
     dev = bv.MoELayer(s.H, s.I, s.E, s.k, T, layer.codebook, layer.w_router, layer.bias, s.renormalize)
     slot_bytes = bv.moe_expert_cache_slot_bytes(s.H, s.I, fmt_for_slots)
-    pool = torch.empty(slots * slot_bytes, dtype=torch.uint8, device="cuda")
+    # poisoned slots: 0xFF bytes are NaN as fp16 scales, so any byte a fetch
+    # failed to overwrite would show in the outputs
+    pool = torch.full((slots * slot_bytes,), 0xFF, dtype=torch.uint8, device="cuda")
     cache = bv.ExpertCache(dev.table, pool, slot_bytes)
     f = experts_fn(layer)
     for e in range(s.E):  # even ids: one host block in the slot's layout; odd ids: six buffers
@@ -139,3 +141,17 @@ def test_caller_set_entries_are_left_alone(torch):
         d.codes[m] = d.scales[m] = pageable.data_ptr()
     assert cache.lib.moe_expert_cache_set_host(cache.handle, 1, ctypes.byref(d)) == bv.MOE_ERR_UNSUPPORTED
     assert "page-locked" in cache.lib.moe_last_error().decode()
+
+
+def test_destroy_evicts_the_cached_entries(torch):
+    import bit_vq_routed_gb300 as bv
+    spec = ms.LayerSpec(H=512, I=256, E=8, k=2, seed=36)
+    layer = ms.Layer(spec)
+    dev, cache, mf = _cached(layer, 1, 4, bv.MOE_FMT_VQ2)
+    x = ms.tokens(1, spec.H, seed=6)
+    mf.step(torch.from_numpy(x).view(torch.bfloat16).cuda())
+    assert (dev.pair_status[:2].cpu().numpy() == 1).all()
+    cache.destroy()
+    g = run(dev, x)  # the table no longer points into the pool
+    assert (g["status"] == 0).all()
+    assert np.array_equal(g["out"], np.zeros_like(g["out"]))

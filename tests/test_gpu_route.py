@@ -69,3 +69,49 @@ def test_route_repeated_calls_stay_consistent(torch):
             g.replay()
             torch.cuda.synchronize()
             assert np.array_equal(dev.sorted_pair[:32].cpu().numpy(), r)
+
+
+@pytest.mark.parametrize("T,E,k,zero_first", [(1, 256, 8, True), (1, 256, 8, False), (1, 48, 5, False),
+                                              (4, 64, 8, True), (40, 64, 8, True), (3, 1024, 32, True)])
+def test_equal_logits_go_to_the_lower_id(torch, T, E, k, zero_first):
+    # Router rows duplicated in pairs give bit-equal logits (one fixed summation
+    # order); all-zero tokens make every logit equal.  Every routing path (one
+    # token over a cluster, the one-kernel path up to 8 tokens, the three steps
+    # above) must pick the lower id of equal logits, as the oracle does.
+    import oracle
+    import bit_vq_routed_gb300 as bv
+    H = 512
+    spec = ms.LayerSpec(H=H, I=128, E=E, k=k, seed=50 + T)
+    layer = ms.Layer(spec)
+    w = layer.w_router.copy()
+    rng = np.random.default_rng(E + T)
+    perm = rng.permutation(E)
+    for a, b in zip(perm[0::2], perm[1::2]):  # expert b gets expert a's router row
+        w[b] = w[a]
+    x = ms.tokens(T, H, seed=60 + T)
+    if zero_first:
+        x[0] = 0  # token 0: every logit equal
+    O = oracle.default
+    lg = O.router_logits(x, w, None)
+    ids_ref, w_ref = O.route_topk(lg, k, 1)
+    if zero_first:
+        assert (ids_ref[0] == np.arange(k)).all()
+    else:  # the duplicated rows do tie inside this token's selection
+        sel = lg[0, ids_ref[0]]
+        assert len(np.unique(sel)) < k
+    off_ref, sp_ref, p2s_ref = O.permute(ids_ref, E)
+    dev = bv.MoELayer(H, 128, E, k, T, layer.codebook, w, None, 1)
+    xd = torch.from_numpy(x).view(torch.bfloat16).cuda()
+    for fused in (False, True):
+        dev.ids.fill_(-7)
+        (dev.route if fused else dev.route_stepwise)(xd)
+        torch.cuda.synchronize()
+        P = T * k
+        assert np.array_equal(dev.logits[:T].cpu().numpy().view(np.uint32), lg.view(np.uint32))
+        assert np.array_equal(dev.ids[:T].cpu().numpy(), ids_ref), f"fused={fused}"
+        assert np.abs(dev.weights[:T].cpu().numpy() - w_ref).max() <= 1e-6
+        assert np.array_equal(dev.offsets.cpu().numpy(), off_ref)
+        assert np.array_equal(dev.sorted_pair[:P].cpu().numpy(), sp_ref)
+        assert np.array_equal(dev.pair_to_sorted[:P].cpu().numpy(), p2s_ref)
+        if zero_first:  # equal logits get equal weights
+            assert np.allclose(dev.weights[0].cpu().numpy(), 1.0 / k, rtol=0, atol=1e-7)
