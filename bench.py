@@ -348,23 +348,26 @@ def run_gpu(args, wl, world, rank, local):
     codes_only = [per_slot[(sl, L)][1] for sl in ffn_slots for L in range(nL)]
     ms_total = max_over_ranks(ms_total)
 
-    # end to end through the public API: pinned host tokens in, outputs out
-    host_in = [torch.from_numpy(token_pool(wl, L)).view(torch.bfloat16).pin_memory() for L in range(nL)]
+    # end to end through the public API: pinned host tokens in, outputs out.
+    # Graphed: one GraphedStep per token batch of the pool (the graph copies
+    # the batch's tokens of every layer in, runs the layers, copies the
+    # outputs out).
+    host_in = torch.from_numpy(np.stack([token_pool(wl, L) for L in range(nL)], axis=1)).view(
+        torch.bfloat16).pin_memory()  # [G, layers, T, H]
     host_out = torch.empty(nL, T, 4096, dtype=torch.float32).pin_memory()
     if args.graph:
-        fwd = [bv.GraphedForward(dev, T) for dev in devs]
+        e2e_graphs = [bv.GraphedStep(devs, host_in[sl], host_out) for sl in range(G)]
     e2e_steps = args.steps
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for s in range(e2e_steps):
+        if args.graph:
+            e2e_graphs[s % G].replay()
+            continue
         for L, dev in enumerate(devs):
-            if args.graph:
-                fwd[L].x.copy_(host_in[L][s % G], non_blocking=True)
-                out = fwd[L].replay()
-            else:
-                xin = host_in[L][s % G].cuda(non_blocking=True)
-                out = dev.forward(xin)
+            xin = host_in[s % G][L].cuda(non_blocking=True)
+            out = dev.forward(xin)
             host_out[L].copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -620,7 +623,10 @@ def main():
         "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what,
                          "cpu": cpu_model(), "single_core": single},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * 4096 * 2 * nL,
-                "d2h_bytes_per_step": T * 4096 * 4 * nL},
+                "d2h_bytes_per_step": T * 4096 * 4 * nL,
+                "how": ("GraphedStep: one CUDA graph per step holding the page-locked host -> device copy of "
+                        "every layer's tokens, the layers, and the device -> host copy of their outputs")
+                if args.graph else "eager calls with a copy in and out per layer"},
         "gpu_launches": r["launches"],
         "launch": ("one CUDA graph per step (every layer's route, expert FFN and combine; programmatic "
                    "dependent launch between kernels); the expert-FFN time is a graph of the step's FFN calls "

@@ -407,5 +407,5 @@ class ExpertCache:
             pass
 
 
-from .layer import (GraphedForward, MissFetchForward, MoELayer, host_expert, host_expert_image,  # noqa: E402,F401
-                    upload_layer)
+from .layer import (GraphedForward, GraphedStep, MissFetchForward, MoELayer, host_expert,  # noqa: E402,F401
+                    host_expert_image, upload_layer)

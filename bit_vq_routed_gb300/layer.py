@@ -146,6 +146,40 @@ class GraphedForward:
         return self.out
 
 
+class GraphedStep:
+    """One step over several layers as one CUDA graph, inputs and outputs
+    included: the graph copies the step's tokens from page-locked host memory
+    (``host_in``: bf16 [L, T, H], one copy), runs every layer's forward on its
+    own slice, and copies the fp32 outputs back (``host_out``: [L, T, H], one
+    copy).  Write the next tokens into ``host_in`` (or capture one
+    GraphedStep per input buffer), call ``replay()``, and read ``host_out``
+    after synchronising the stream."""
+
+    def __init__(self, layers: Sequence[MoELayer], host_in: torch.Tensor, host_out: torch.Tensor, device="cuda"):
+        if not (host_in.is_pinned() and host_out.is_pinned()):
+            raise ValueError("host_in and host_out must be page-locked")
+        L, T, H = host_in.shape
+        if L != len(layers) or tuple(host_out.shape) != (L, T, H):
+            raise ValueError("host_in / host_out must be [layers, T, H]")
+        self.layers, self.host_in, self.host_out = list(layers), host_in, host_out
+        self.x = torch.empty(L, T, H, dtype=torch.bfloat16, device=device)
+        self.out = torch.empty(L, T, H, dtype=torch.float32, device=device)
+        self._run()  # first eager call: kernel attributes are set outside capture
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._run()
+
+    def _run(self):
+        self.x.copy_(self.host_in, non_blocking=True)
+        for i, layer in enumerate(self.layers):
+            layer.forward(self.x[i], out=self.out[i])
+        self.host_out.copy_(self.out, non_blocking=True)
+
+    def replay(self):
+        self.graph.replay()
+
+
 def host_expert(fmt: int, codes: Sequence, scales: Sequence, stream=None, device="cuda"):
     """Packs one expert on the device (upload_expert) and returns page-locked
     host copies of the packed buffers (codes[3], scales[3]): the host-resident
