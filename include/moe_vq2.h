@@ -232,13 +232,15 @@ moe_status moe_expert_cache_stats(const moe_expert_cache* c, uint64_t* hits, uin
 
 /* Host-only planning step of moe_expert_cache_fetch, for callers that manage
  * slots and copies themselves (and testable without a GPU).  Every array
- * here is a HOST array.  State arrays (read and updated): slot_expert [num_slots] = expert held by each slot or
- * -1; counts [num_experts] and last_step [num_experts] = routing counts and
- * the last step each expert was named (0 = never).  `step` numbers this call
- * (> every last_step).  request: n expert ids.  Outputs, one entry per
- * request: fill_slot[i] = the slot that request i is copied into, or -1 (a
- * hit, a repeat of an earlier request of the call, or no slot: see
- * placed); evicted[i] = the expert that slot held before, or -1.
+ * here is a HOST array.  State arrays (read and updated):
+ *   slot_expert [num_slots]: the expert held by each slot, or -1;
+ *   counts [num_experts], last_step [num_experts]: the routing counts and the
+ *     last step each expert was named (0 = never).
+ * `step` numbers this call and must be above every last_step.  request: n
+ * expert ids.  Outputs, one entry per request: fill_slot[i] = the slot that
+ * request i is copied into, or -1 (a hit, a repeat of an earlier request of
+ * the call, or no slot left: those are counted in n_unplaced); evicted[i] =
+ * the expert that slot held before, or -1.
  * Returns MOE_ERR_INVALID_ARG for a bad id, a slot_expert entry out of range
  * or held twice, or a step not above every last_step (nothing is updated). */
 moe_status moe_expert_cache_plan(int num_experts, int num_slots, int32_t* slot_expert, uint64_t* counts,
