@@ -139,3 +139,21 @@ def test_header_compiles_as_plain_c(tmp_path):
     r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I",
                         os.path.dirname(HEADER), "-I", cuda_inc, str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_expert_cache_rejects_bad_args(lib):
+    # host-side checks before any table is touched (no GPU needed)
+    P = ctypes.c_void_p
+    h = P(12345)
+    assert lib.moe_expert_cache_create(None, P(256), 1 << 24, 6_684_672, ctypes.byref(h)) == bv.MOE_ERR_INVALID_ARG
+    assert h.value is None  # the out handle is cleared first
+    assert lib.moe_expert_cache_create(P(16), None, 1 << 24, 6_684_672, ctypes.byref(h)) == bv.MOE_ERR_INVALID_ARG
+    assert lib.moe_expert_cache_create(None, None, 0, 0, None) == bv.MOE_ERR_INVALID_ARG
+    assert lib.moe_expert_cache_set_host(None, 0, None) == bv.MOE_ERR_INVALID_ARG
+    assert lib.moe_expert_cache_set_host_image(None, 0, 0, P(16)) == bv.MOE_ERR_INVALID_ARG
+    nf = ctypes.c_int(-1)
+    assert lib.moe_expert_cache_fetch(None, None, 0, None, ctypes.byref(nf), None, None) == bv.MOE_ERR_INVALID_ARG
+    assert lib.moe_expert_cache_slot_of(None, 0) == -1
+    assert lib.moe_expert_cache_stats(None, None, None, None, None) == bv.MOE_ERR_INVALID_ARG
+    assert "moe_expert_cache_stats" in lib.moe_last_error().decode()
+    assert lib.moe_expert_cache_destroy(None, None) == bv.MOE_OK
