@@ -145,6 +145,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait: gives up after max_iter polls, records code in *err and
 // returns false (callers then skip their work so every loop still ends).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* err, int code) {
+#pragma unroll 1
     for (uint32_t it = 0; it < (1u << 20); ++it)
         if (mbar_try_wait(bar, parity)) return true;
     if (err) atomicExch(err, code);

@@ -3,22 +3,8 @@
 // them at small batches): one table pair per (token, expert), the expert's
 // codes streamed once per token.
 //
-// For one token, every code byte c of group G (inputs 4G .. 4G+3) adds
-//     scale[r, G/32] * sign(c) * dot(codebook[c & 127], x[4G .. 4G+3])
-// to output row r, and the signed dot product depends on (c, G) only.  A CTA
-// first builds the table L[c][G] of those values for a K-range of 1024 inputs
-// (256 codes x 256 groups in fp16, 128 KB; the negated half is stored too, so
-// the sign costs nothing), then streams the code tiles of many rows through
-// it: per code byte one byte permute (the table address), one 2-byte shared
-// load and one mixed-precision add of the fp16 entry into an fp32 sum.
-//
-// Lanes own groups: lane l = 4b + m takes, in scale block b of the K-range,
-// the 8 groups m, m+4, ..., m+28 (one 16-byte load each, so each load
-// instruction of the warp reads whole 64-byte runs), and its 8 values of a
-// row share one scale.  The table puts every entry a lane reads in bank l,
-// whatever the code, so the 32 table reads of a warp never conflict, and the
-// group slot becomes the load's immediate offset.  The 16 row sums of a tile
-// are reduced across the warp by a reduce-scatter.
+// The table, the lane layout and the per-unit lookups are the shared core in
+// lut_core.cuh.
 //
 // K-range partial sums go to the workspace: FC2's table build adds FC1's
 // partials in a fixed order and applies silu(g) * u; of FC2's partials, the
@@ -35,40 +21,22 @@
 #include <cuda_bf16.h>
 
 #include "ffn_common.cuh"
+#include "lut_core.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int LW = 16;                   // warps
-constexpr int THREADS = 32 * LW;
-constexpr int KR_IN = 128 * LUT_KB;      // inputs per K-range: 32 lanes x 8 groups x 4
-constexpr uint32_t TAB = 0x10000;        // table: [0x10000, 0x30000) of the shared window
-constexpr uint32_t PLANE = 0x10000;      // group slots 0-3 | 4-7
-constexpr uint32_t DYN_SMEM = 227 * 1024;  // dynamic shared memory requested (the maximum)
+using namespace lut;
+
 constexpr int MAX_GROUP = 32;            // table pairs of one token (<= k <= 32)
-// One code slot per warp, filled by three bulk copies: tiles 0-3 of the unit
-// (2 KB), tiles 4-7 after 64 bytes of skew, then the 8 tiles' row scales (32
-// bytes each).  The lanes of a quarter-warp take scale blocks b and b + 4, so
-// their 16-byte reads of one group slot hit 8 distinct bank groups.
-constexpr uint32_t HALF_OFF = 4 * 512 + 64;
-constexpr uint32_t SCALE_OFF = HALF_OFF + 4 * 512;
-constexpr uint32_t SLOT_BYTES = SCALE_OFF + 8 * 32;
-constexpr int NSLOT = LW;
+constexpr int NSLOT = LW;                // one code slot per warp
 constexpr int LOW_SLOTS = 12;            // slots below the table; the rest above it
 static_assert(LOW_SLOTS * SLOT_BYTES >= 4 * (1024 + 1), "the expert offsets (E <= 1024) fit in the low slots");
-// scale block of lane l (the 4 lanes 4q .. 4q+3 share one): blocks b and b + 4
-// for the two lane quads of each quarter-warp
-__host__ __device__ constexpr int lane_block(int l) { return (((l >> 2) & 1) << 2) | (l >> 3); }
-constexpr uint32_t HIGH_BASE = TAB + 2 * PLANE;
-
-// Inputs of the K-range in shared memory: float i at xs_at(i), a float4 of
-// padding after every 32 groups (one scale block), so the table build's
-// 16-byte reads of one group in each of the 8 blocks spread over all banks.
-__device__ __forceinline__ int xs_at(int i) { return i + 4 * (i >> 7); }
+constexpr uint32_t HIGH_BASE = TAB_END;
 
 struct __align__(16) Smem {
     unsigned long long full[NSLOT];        // slot mbarriers (one arrival + the copied bytes)
-    alignas(16) float xs[KR_IN + KR_IN / 32];  // (read as float4)
+    alignas(16) float xs[XS_FLOATS];       // (read as float4)
     alignas(16) float cb[128 * 4];         // (read as float4)
     const void* pa[MAX_GROUP];  // per pair of the current group: FC1 gate / FC2 down codes
     const void* pb[MAX_GROUP];  // FC1 up codes
@@ -88,54 +56,6 @@ static_assert(offsetof(Smem, xs) % 16 == 0 && offsetof(Smem, cb) % 16 == 0, "flo
 static_assert(0x400 + ((sizeof(Smem) + 127) / 128 * 128) + LOW_SLOTS * SLOT_BYTES <= TAB &&
                   HIGH_BASE + (NSLOT - LOW_SLOTS) * SLOT_BYTES <= 0x400 + DYN_SMEM && NSLOT >= LOW_SLOTS,
               "shared layout");
-
-// Table entry of lane l, group slot j, code c sits at shared-window byte
-//     TAB + (j/4)*PLANE + c*256 + 128*((j/2)&1) + 4*l + 2*(j&1):
-// the code fills bits 8-15 (one byte permute), the slot is an immediate.
-template <int J>
-__device__ __forceinline__ float tab_add(uint32_t addr, float t) {
-    constexpr int IMM = (J >> 2) * (int)PLANE + 128 * ((J >> 1) & 1) + 2 * (J & 1);
-    uint16_t v;
-    asm volatile("ld.shared.b16 %0, [%1+%2];" : "=h"(v) : "r"(addr), "n"(IMM));
-    float d;
-    asm("add.rn.f32.f16 %0, %1, %2;" : "=f"(d) : "h"(v), "f"(t));
-    return d;
-}
-
-template <uint32_t SEL>
-__device__ __forceinline__ uint32_t prmt_i(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "n"(SEL));
-    return d;
-}
-
-struct UnitRegs {
-    uint4 cw[8];  // group slot j: the 16 code bytes (rows) of group 4j + m
-    uint4 sc[2];  // the 16 row scales of this lane's scale block
-};
-
-// Sum over the lane's 8 groups of row byte RB (row (RB >> 1) + 8 (RB & 1)).
-template <int RB>
-__device__ __forceinline__ float row_sum(const UnitRegs& u, uint32_t lb) {
-    constexpr uint32_t SEL = 0x7604u | ((uint32_t)(RB & 3) << 4);
-    float t = 0.0f;
-    t = tab_add<0>(prmt_i<SEL>((&u.cw[0].x)[RB >> 2], lb), t);
-    t = tab_add<1>(prmt_i<SEL>((&u.cw[1].x)[RB >> 2], lb), t);
-    t = tab_add<2>(prmt_i<SEL>((&u.cw[2].x)[RB >> 2], lb), t);
-    t = tab_add<3>(prmt_i<SEL>((&u.cw[3].x)[RB >> 2], lb), t);
-    t = tab_add<4>(prmt_i<SEL>((&u.cw[4].x)[RB >> 2], lb), t);
-    t = tab_add<5>(prmt_i<SEL>((&u.cw[5].x)[RB >> 2], lb), t);
-    t = tab_add<6>(prmt_i<SEL>((&u.cw[6].x)[RB >> 2], lb), t);
-    t = tab_add<7>(prmt_i<SEL>((&u.cw[7].x)[RB >> 2], lb), t);
-    constexpr int ROW = (RB >> 1) + 8 * (RB & 1);
-    const uint32_t s2 = (&u.sc[ROW >> 3].x)[(ROW & 7) >> 1];
-    const __half2 h = *reinterpret_cast<const __half2*>(&s2);
-    return t * ((ROW & 1) ? __high2float(h) : __low2float(h));
-}
-
-// Register cap: each of the SM's four schedulers holds 16384 registers for
-// its share of the CTA's warps (ceil(LW / 4) warps).
-constexpr int MAX_REG = 16384 / (32 * ((LW + 3) / 4)) > 255 ? 255 : 16384 / (32 * ((LW + 3) / 4)) / 8 * 8;
 
 // SELF: a single-token call whose experts are all VQ2 (no schedule kernel):
 // the kernel lists the call's pairs itself from the expert offsets and the
@@ -210,51 +130,7 @@ __global__ void __maxnreg__(MAX_REG)
             u1 = (int)((long long)U * (blockIdx.x + 1) / C);
         }
     };
-    // Table of one K-range from S.xs: a thread takes a quad of words (the 4
-    // lanes 4 lq .. 4 lq + 3 of scale block bq, in group-slot pair (j0, j0 + 1),
-    // j0 = 4p + 2jj: the 8 consecutive groups 32 bq + 4 j0 + 0..7) and every
-    // LW-th code.
-    auto build_table = [&](int nkb) {
-        const int q = tid & 31, lq = q & 7, jj = (q >> 3) & 1, p = q >> 4, bq = lane_block(4 * lq);
-        if (bq < nkb) {
-            const int g0 = 32 * bq + 4 * (4 * p + 2 * jj);
-            // xp[m][i] = (x[4(g0+m)+i], x[4(g0+4+m)+i]): the low / high half of word m
-            float2 xp[4][4];
-#pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-                const float4 lo = *reinterpret_cast<const float4*>(&S.xs[xs_at(4 * (g0 + mm))]);
-                const float4 hi = *reinterpret_cast<const float4*>(&S.xs[xs_at(4 * (g0 + 4 + mm))]);
-                xp[mm][0] = make_float2(lo.x, hi.x);
-                xp[mm][1] = make_float2(lo.y, hi.y);
-                xp[mm][2] = make_float2(lo.z, hi.z);
-                xp[mm][3] = make_float2(lo.w, hi.w);
-            }
-            const uint32_t a0 = TAB + (uint32_t)p * PLANE + 128u * jj + 16u * lq;
-#pragma unroll
-            for (int it = 0; it < 128 / LW; ++it) {
-                const int c0 = warp + it * LW;
-                const float4 e = *reinterpret_cast<const float4*>(&S.cb[4 * c0]);
-                const float2 ex = make_float2(e.x, e.x), ey = make_float2(e.y, e.y);
-                const float2 ez = make_float2(e.z, e.z), ew = make_float2(e.w, e.w);
-                uint32_t wv[4];
-#pragma unroll
-                for (int mm = 0; mm < 4; ++mm) {
-                    float2 v2 = __fmul2_rn(ex, xp[mm][0]);
-                    v2 = __ffma2_rn(ey, xp[mm][1], v2);
-                    v2 = __ffma2_rn(ez, xp[mm][2], v2);
-                    v2 = __ffma2_rn(ew, xp[mm][3], v2);
-                    const __half2 hv = __floats2half2_rn(v2.x, v2.y);
-                    wv[mm] = *reinterpret_cast<const uint32_t*>(&hv);
-                }
-                const uint32_t a = a0 + 256u * (uint32_t)c0;
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wv[0]), "r"(wv[1]),
-                             "r"(wv[2]), "r"(wv[3]));
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + 128u * 256u),
-                             "r"(wv[0] ^ 0x80008000u), "r"(wv[1] ^ 0x80008000u), "r"(wv[2] ^ 0x80008000u),
-                             "r"(wv[3] ^ 0x80008000u));
-            }
-        }
-    };
+    auto build_table = [&](int nkb) { lut::build_table(S.xs, S.cb, nkb, tid); };
     // The token's activations of a K-range into S.xs (as fp32).
     auto load_x = [&](int t, int kr, int nin) {
         for (int i = tid; i < nin; i += THREADS)
@@ -383,7 +259,7 @@ __global__ void __maxnreg__(MAX_REG)
 
     const bool comb = !FC1 && SELF && (comb32 != nullptr || comb16 != nullptr);
     const bool adds = !FC1 && fc2_adds && !comb;  // (then KR == 2)
-    const int b = lane_block(lane), m = lane & 3;  // scale block and group phase of this lane
+    const int b = lane_block(lane);  // scale block of this lane
     const uint32_t lb = TAB | (uint32_t)(4 * lane);
     uint32_t phase = 0;                     // parity of the slot's next completion
     bool pend = false;                      // the slot has a copy in flight
@@ -457,19 +333,13 @@ __global__ void __maxnreg__(MAX_REG)
             c = static_cast<const uint8_t*>(second ? S.pb[cu.pi] : S.pa[cu.pi]) + tile * 512;
             sp = static_cast<const uint16_t*>(second ? S.sb[cu.pi] : S.sa[cu.pi]) + tile * 16;
         };
-        // Unit at cursor cu into the warp's slot: lane 0 arms the barrier
-        // with the byte count, lanes < nkb copy one tile each, lane 31 the
-        // scales.
+        // Unit at cursor cu into the warp's slot.
         auto issue = [&](Cur cu) {
             pend = true;
             const uint8_t* c;
             const uint16_t* sp;
             unit_ptrs(cu, c, sp);
-            if (lane == 0) mbar_arrive_expect_tx(bar, 544u * nkb);
-            __syncwarp();
-            if (lane == 0) bulk_g2s(slot, c, 512u * min(nkb, 4), bar);
-            if (lane == 1 && nkb > 4) bulk_g2s(slot + HALF_OFF, c + 2048, 512u * (nkb - 4), bar);
-            if (lane == 2) bulk_g2s(slot + SCALE_OFF, sp, 32u * nkb, bar);
+            issue_unit(slot, bar, c, sp, nkb, lane);
         };
         auto prefetch = [&](Cur cu) {  // ask L2 for the unit at cu
             if (lane == 0) {
@@ -532,41 +402,9 @@ __global__ void __maxnreg__(MAX_REG)
 
         auto compute_store = [&](const UnitRegs& r, Cur cu) {
             const int pi = cu.pi, rt = cu.rt;
-            // Reduce-scatter over the warp (lanes 2p and 2p+1 end with byte
-            // position p); its first step (lanes 16 apart) runs as each pair
-            // of row sums (i, i + 8) is ready, so only 8 sums stay live.
-            float acc[8];
-            const bool up16 = lane & 16;
-#define MOE_LUT_PAIR(I)                                                                  \
-    {                                                                                    \
-        const float lo = active ? row_sum<I>(r, lb) : 0.0f;                              \
-        const float hi = active ? row_sum<I + 8>(r, lb) : 0.0f;                          \
-        acc[I] = (up16 ? hi : lo) + __shfl_xor_sync(0xffffffffu, up16 ? lo : hi, 16);   \
-    }
-            MOE_LUT_PAIR(0)
-            MOE_LUT_PAIR(1)
-            MOE_LUT_PAIR(2)
-            MOE_LUT_PAIR(3)
-            MOE_LUT_PAIR(4)
-            MOE_LUT_PAIR(5)
-            MOE_LUT_PAIR(6)
-            MOE_LUT_PAIR(7)
-#undef MOE_LUT_PAIR
-#pragma unroll
-            for (int o = 8, n8 = 4; o >= 2; o >>= 1, n8 >>= 1) {
-                const bool upo = lane & o;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (i < n8) {
-                        const float send = upo ? acc[i] : acc[i + n8];
-                        const float keep = upo ? acc[i + n8] : acc[i];
-                        acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                    }
-                }
-            }
-            acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
-            const int pp = lane >> 1;
-            const int h = rt * 16 + (pp >> 1) + 8 * (pp & 1);  // output row of this lane pair
+            float acc[1];
+            acc[0] = unit_rows(r, lb, active, lane);
+            const int h = rt * 16 + unit_row(lane);  // output row of this lane pair
             auto emit = [&](float y) {  // FC2: the finished y of row h
                 const int s = S.ys[pi];
                 if (mode == MOE_PER_PAIR) {
@@ -596,13 +434,7 @@ __global__ void __maxnreg__(MAX_REG)
             phase ^= 1u;
             pend = false;
             UnitRegs r;
-            if (active) {
-                const uint32_t tb = slot + (b < 4 ? 512u * b : HALF_OFF + 512u * (b - 4)) + 16u * m;
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) r.cw[jj] = lds_u128(tb + 64 * jj);
-                r.sc[0] = lds_u128(slot + SCALE_OFF + 32 * b);
-                r.sc[1] = lds_u128(slot + SCALE_OFF + 32 * b + 16);
-            }
+            load_unit(r, slot, lane, active);
             __syncwarp();
             // the generic-proxy reads of the slot come before the next copy's writes
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -1,8 +1,8 @@
 // moe_vq2_expert_ffn_noalloc: the expert FFN for callers that must not
 // allocate device memory (see the declaration in moe_vq2.h).  Its scratch is
-// one file-scope device array, created when the library is loaded on a
-// device and held until the process exits; no call here allocates or frees
-// device memory.
+// one file-scope device array, reserved when the library's device code is
+// loaded on a device (under lazy loading: at the first call here) and held
+// until the process exits; no call here allocates or frees device memory.
 #include <mutex>
 
 #include "common.cuh"
@@ -34,7 +34,10 @@ moe_status scratch_address(void** out) {
     if (!g_scratch_addr[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_ffn_scratch);
-        if (e != cudaSuccess) return moe::cuda_status(e, "moe_vq2_expert_ffn_noalloc: cudaGetSymbolAddress");
+        if (e != cudaSuccess)
+            return moe::cuda_status(e, "moe_vq2_expert_ffn_noalloc: cudaGetSymbolAddress (loading the library's "
+                                       "device code reserves its 64 MiB scratch; an out-of-memory here means the "
+                                       "device had no room left for it)");
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];

@@ -323,7 +323,10 @@ moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* b
  * over the same ids; weights fp32 [T,k] from moe_route_topk.
  * ws: moe_vq2_expert_ffn_workspace_size(T, k, E, H, I) bytes of device
  * memory (scratch: the schedule, the fp32 intermediate a [P, I] and the
- * K-range partial sums of the activation-table pairs).
+ * K-range partial sums of the activation-table pairs).  Its contents need
+ * no initialisation.  A bounded device-side wait that ran out is recorded in
+ * the int32 word at byte 8 of ws (0 = none).  Calls that share a workspace
+ * must not overlap on the GPU.
  * Requires H % 256 == 0, I % 128 == 0, k <= 32, x 16-byte aligned. */
 size_t moe_vq2_expert_ffn_workspace_size(int T, int k, int E, int H, int I);
 moe_status moe_vq2_expert_ffn(const moe_slot_table* table, const uint16_t* x,
@@ -343,9 +346,12 @@ moe_status moe_vq2_expert_ffn(const moe_slot_table* table, const uint16_t* x,
  * not allowed.  This call takes no workspace: it computes exactly what
  * moe_vq2_expert_ffn computes (same arguments and outputs) using a scratch
  * area of MOE_NOALLOC_SCRATCH_BYTES that is a static device array of the
- * library, reserved on every GPU that loads the library and held until the
- * process exits.  It never calls cudaMalloc, cudaFree or an allocating
- * library routine.
+ * library, held until the process exits.  Under CUDA's lazy module loading
+ * (the default) the array is reserved on a device only when the library's
+ * device code is first loaded there, which the first call of this entry
+ * point forces; a caller that sizes its own arena from the free device
+ * memory should make one call first, so that the 64 MiB are already taken.
+ * It never calls cudaMalloc, cudaFree or an allocating library routine.
  *
  * Limits and rules:
  *   - the call fails with MOE_ERR_UNSUPPORTED, and enqueues nothing, when
@@ -353,8 +359,11 @@ moe_status moe_vq2_expert_ffn(const moe_slot_table* table, const uint16_t* x,
  *     MOE_NOALLOC_SCRATCH_BYTES (64 MiB: at H = 4096, I = 2048 this covers
  *     decode batches of up to 32 tokens at top-8, and more);
  *   - the first call on each device looks up the device address of the
- *     static array (cudaGetSymbolAddress, with that device current); make
- *     that first call before any stream capture on the device;
+ *     static array (cudaGetSymbolAddress, with that device current) and
+ *     keeps it for the life of the process; make that first call before any
+ *     stream capture on the device.  The address belongs to the device's
+ *     context: after cudaDeviceReset on a device, do not call this entry
+ *     point on it again in the same process;
  *   - every call on a device shares the one array, which keeps the contents
  *     of the last call (no part of it needs to start at zero: each call
  *     writes what it reads).  Calls whose work overlaps on the GPU (on

@@ -53,6 +53,22 @@ def test_noalloc_matches_workspace_entry_point_twice(torch, mode_name):
         assert_close(got, ref, f"noalloc call {call}")
 
 
+def test_noalloc_single_token_vq2_only_twice(torch):
+    """One token on a table of VQ2 experts only: the path without a schedule
+    kernel, whose table kernels keep their counters, K-range partial sums
+    and error word in the scratch."""
+    import bit_vq_routed_gb300 as bv
+    spec = ms.LayerSpec(H=4096, I=2048, E=16, k=4, seed=37, fp4_top=0)
+    layer = ms.Layer(spec)
+    dev, keep = device_layer(layer, 1)
+    for call in range(2):
+        x = ms.tokens(1, spec.H, seed=37, stream=call)
+        ref, got, st_ref, st_got = _both(torch, dev, x, bv.MOE_PER_PAIR)
+        assert np.array_equal(st_ref, st_got)
+        assert st_got.all()
+        assert_close(got, ref, f"single-token noalloc call {call}")
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(torch):
     import bit_vq_routed_gb300 as bv
     spec = ms.LayerSpec(H=256, I=2048, E=8, k=8, seed=1)
