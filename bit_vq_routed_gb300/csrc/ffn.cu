@@ -267,7 +267,6 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     LutRec* recs = reinterpret_cast<LutRec*>(w + L.rec_off);
     int32_t* grp_start = reinterpret_cast<int32_t*>(w + L.grp_start_off);
     Chunk* uchunks = reinterpret_cast<Chunk*>(w + L.uchunks_off);
-    uint16_t* x16s = reinterpret_cast<uint16_t*>(w + L.x16s_off);
     const int use_lut = 1;
     const int use_umma = T >= UMMA_MIN ? 1 : 0;  // an expert gets at most T of the pairs
     // With one token no expert gets two pairs, so the mma.sync kernels only
@@ -290,13 +289,14 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
                                sorted_pair, P, k, status, header, chunks, recs, grp_start, use_lut,
                                uchunks, use_umma, H, I, num_sms(), reinterpret_cast<int4*>(w + L.range_off));
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule launch");
-    if ((mma || use_umma) && (st = launch_gather_f16(x, sorted_pair, k, H, P, x16s, s)) != MOE_OK) return st;
+    if ((mma || use_umma) && (st = launch_gather_f16(x, sorted_pair, k, H, P, w, L, s)) != MOE_OK) return st;
     if (use_lut &&
         (st = launch_lut_fc(true, false, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s)) !=
             MOE_OK)
         return st;
     if (mma && (st = launch_mma_fc(true, t, sorted_pair, weights, k, mode, out, w, L, s)) != MOE_OK) return st;
     if (use_umma && (st = launch_umma(true, t, sorted_pair, weights, k, P, mode, out, w, L, s)) != MOE_OK) return st;
+    if ((mma || use_umma) && (st = launch_a_to_f16(P, I, w, L, s)) != MOE_OK) return st;
     if (use_lut &&
         (st = launch_lut_fc(false, false, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s)) !=
             MOE_OK)

@@ -45,9 +45,14 @@ enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NU
 // the tcgen05 path (uchunks: chunks of <= UMMA_NT sorted positions); the
 // tensor-core paths read x16s (fp16 activations gathered by sorted position)
 // and a16 (fp16 silu(g)*u by sorted position).
+// Range: x16s[s] holds x / xsc[s] and a16[s] holds a / asc[s], with xsc and
+// asc powers of two that bring the row's largest magnitude to at most 2^14,
+// so neither overflows fp16 whatever the range of the activations; the FC1
+// epilogues write a in fp32 (a32) with its largest magnitude per sorted
+// position (amax, float bits), from which the conversion kernel makes a16.
 struct WsLayout {
     size_t chunks_off, rec_off, grp_start_off, p1_off, p2_off, cnt_off, cnt2_off, range_off;
-    size_t uchunks_off, x16s_off, a16_off, total;
+    size_t uchunks_off, x16s_off, a16_off, xsc_off, asc_off, amax_off, a32_off, total;
     int max_chunks, max_lut, max_uchunks;
 };
 
@@ -94,6 +99,14 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I)
     o = ws_align(o + sizeof(uint16_t) * (size_t)P * H);
     L.a16_off = o;
     o = ws_align(o + sizeof(uint16_t) * (size_t)P * I);
+    L.xsc_off = o;
+    o = ws_align(o + sizeof(float) * (size_t)P);
+    L.asc_off = o;
+    o = ws_align(o + sizeof(float) * (size_t)P);
+    L.amax_off = o;
+    o = ws_align(o + sizeof(uint32_t) * (size_t)P);
+    L.a32_off = o;
+    o = ws_align(o + sizeof(float) * (size_t)P * I);
     L.total = o;
     return L;
 }
@@ -105,8 +118,23 @@ moe_status launch_lut_fc(bool fc1, bool self, const SlotTableHost* t, const uint
                          uint8_t* status, char* ws, const WsLayout& L, cudaStream_t s,
                          const int32_t* pair_to_sorted = nullptr, float* comb32 = nullptr,
                          uint16_t* comb16 = nullptr);
-moe_status launch_gather_f16(const uint16_t* x, const int32_t* sorted_pair, int k, int H, int P, uint16_t* x16s,
-                             cudaStream_t s);
+// x16s, xsc (and amax zeroed) for every sorted position.
+moe_status launch_gather_f16(const uint16_t* x, const int32_t* sorted_pair, int k, int H, int P, char* ws,
+                             const WsLayout& L, cudaStream_t s);
+// a16, asc from a32, amax (the sorted positions the tensor-core FC1 wrote).
+moe_status launch_a_to_f16(int P, int I, char* ws, const WsLayout& L, cudaStream_t s);
+// 2^e as fp32 for |e| <= 126, and the exponent e (clamped to [-120, 120])
+// of the power of two that brings a magnitude m to at most 2^top.
+__host__ __device__ inline float exp2_i(int e) {
+    union { uint32_t u; float f; } v;
+    v.u = (uint32_t)(e + 127) << 23;
+    return v.f;
+}
+__device__ __forceinline__ int range_exponent(float m, int top) {
+    int ex = 0;
+    frexpf(m, &ex);  // m < 2^ex
+    return min(max(ex - top, -120), 120);
+}
 moe_status launch_umma(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
                        int P, int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s);
 moe_status launch_mma_fc(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,

@@ -49,6 +49,7 @@ struct __align__(16) Smem {
     int all_ys[MAX_GROUP];
     int e_of_s[MAX_GROUP];
     uint8_t lastf[256];         // FC2: the row tiles whose partials this CTA adds up
+    unsigned red[2 * LW];       // table-scale reduction
     int n_self;
     int failed;
 };
@@ -130,7 +131,14 @@ __global__ void __maxnreg__(MAX_REG)
             u1 = (int)((long long)U * (blockIdx.x + 1) / C);
         }
     };
-    auto build_table = [&](int nkb) { lut::build_table(S.xs, S.cb, nkb, tid); };
+    // The table of the K-range whose inputs are in S.xs, with its scale
+    // exponent (block-wide); tab_s = 2^e multiplies each unit's sums back.
+    float tab_s = 1.0f;
+    auto build_table = [&](int nkb) {
+        const int e = table_exponent(S.xs, 128 * nkb, S.cb, S.red, tid);
+        tab_s = exp2_int(e);
+        lut::build_table(S.xs, S.cb, nkb, e, tid);
+    };
     // The token's activations of a K-range into S.xs (as fp32).
     auto load_x = [&](int t, int kr, int nin) {
         for (int i = tid; i < nin; i += THREADS)
@@ -403,7 +411,7 @@ __global__ void __maxnreg__(MAX_REG)
         auto compute_store = [&](const UnitRegs& r, Cur cu) {
             const int pi = cu.pi, rt = cu.rt;
             float acc[1];
-            acc[0] = unit_rows(r, lb, active, lane);
+            acc[0] = unit_rows(r, lb, active, lane) * tab_s;
             const int h = rt * 16 + unit_row(lane);  // output row of this lane pair
             auto emit = [&](float y) {  // FC2: the finished y of row h
                 const int s = S.ys[pi];

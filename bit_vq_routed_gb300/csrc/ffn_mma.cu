@@ -64,12 +64,16 @@ __device__ __forceinline__ uint32_t sh_u32(const uint8_t* p) { return *reinterpr
 
 // FC1 = true: A tiles are the gate and up tiles of 16 I-rows, B = x16s (K = H);
 // FC1 = false: A tiles are two down tiles (32 H-rows), B = a16 (K = I).
+// The B rows are scaled by powers of two (x16s = x / xsc, a16 = a / asc, per
+// sorted position); the epilogues multiply the scale back in fp32.  FC1
+// writes a in fp32 (a32) and the largest |a| of each sorted position (amax).
 template <bool FC1, int NTOK_>
 __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_>::MIN_BLOCKS)
     ffn_mma_kernel(const SlotDesc* __restrict__ desc, const uint16_t* __restrict__ codebook,
                    const uint16_t* __restrict__ bsrc, const int32_t* __restrict__ sorted_pair,
                    const float* __restrict__ weights, int k, int H, int I, const int* __restrict__ header,
-                   const Chunk* __restrict__ chunks, uint16_t* __restrict__ a16, float* __restrict__ out, int mode,
+                   const Chunk* __restrict__ chunks, const float* __restrict__ xsc, const float* __restrict__ asc,
+                   float* __restrict__ a32, uint32_t* __restrict__ amax, float* __restrict__ out, int mode,
                    int fp4_part) {
     using Cfg = MmaCfg<NTOK_>;
     using Smem = typename Cfg::Smem;
@@ -266,31 +270,48 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_>::MIN_BLOCKS)
             __syncthreads();  // buffer buf is free for the copies of slab sl + 2
         }
 
-        // epilogue: acc[t][nt] holds (row i | i+8 of tile t, tokens 8nt + 2j | +1)
+        // epilogue: acc[t][nt] holds (row i | i+8 of tile t, tokens 8nt + 2j | +1):
+        // acc[t][nt][b + 2 hi] is token 8 nt + 2 j + b, row i + 8 hi
 #pragma unroll
         for (int nt = 0; nt < NNT; ++nt) {
             if (nt >= n_nt) continue;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int tok = 8 * nt + 2 * j + (q & 1);
-                if (tok >= ch.count) continue;
-                const int spos = ch.start + tok;
-                const int r16 = i + ((q & 2) ? 8 : 0);
+            for (int b = 0; b < 2; ++b) {
+                const int tok = 8 * nt + 2 * j + b;
+                const bool valid = tok < ch.count;
+                const int spos = ch.start + (valid ? tok : 0);
+                const float sc = valid ? (FC1 ? xsc[spos] : asc[spos]) : 0.0f;
                 if (FC1) {
-                    const int row = rtt[0] * 16 + r16;
-                    const float g = acc[0][nt][q], u = acc[1][nt][q];
-                    a16[(size_t)spos * I + row] = __half_as_ushort(__float2half_rn(g / (1.0f + expf(-g)) * u));
-                } else {
+                    float am = 0.0f;
 #pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        const int row = rtt[t] * 16 + r16;
-                        if (mode == MOE_PER_PAIR) {
-                            out[(size_t)spos * H + row] = acc[t][nt][q];
-                        } else {
-                            const int p = sorted_pair[spos];
-                            atomicAdd(out + (size_t)(p / k) * H + row, weights[p] * acc[t][nt][q]);
-                        }
+                    for (int hi = 0; hi < 2; ++hi) {
+                        const float g = acc[0][nt][b + 2 * hi] * sc, u = acc[1][nt][b + 2 * hi] * sc;
+                        const float av = g / (1.0f + expf(-g)) * u;
+                        if (valid) a32[(size_t)spos * I + rtt[0] * 16 + i + 8 * hi] = av;
+                        am = fmaxf(am, fabsf(av));
                     }
+                    // largest |a| of this token over the warp's 16 rows (the 8 lanes
+                    // of this j; non-negative floats order as their bits), at least
+                    // 1 so that the conversion sees the position as written
+                    uint32_t mb = __float_as_uint(am);
+                    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+                    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+                    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+                    if (valid && i == 0) atomicMax(amax + spos, max(mb, 1u));
+                } else if (valid) {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int hi = 0; hi < 2; ++hi) {
+                            const int row = rtt[t] * 16 + i + 8 * hi;
+                            const float y = acc[t][nt][b + 2 * hi] * sc;
+                            if (mode == MOE_PER_PAIR) {
+                                out[(size_t)spos * H + row] = y;
+                            } else {
+                                const int p = sorted_pair[spos];
+                                atomicAdd(out + (size_t)(p / k) * H + row, weights[p] * y);
+                            }
+                        }
                 }
             }
         }
@@ -307,13 +328,15 @@ static moe_status launch_mma_cfg(bool fc1, const SlotTableHost* t, const int32_t
     const int* header = reinterpret_cast<const int*>(ws);
     const Chunk* chunks = reinterpret_cast<const Chunk*>(ws + L.chunks_off);
     const uint16_t* x16s = reinterpret_cast<const uint16_t*>(ws + L.x16s_off);
-    uint16_t* a16 = reinterpret_cast<uint16_t*>(ws + L.a16_off);
+    const uint16_t* a16 = reinterpret_cast<const uint16_t*>(ws + L.a16_off);
     auto kern = fc1 ? ffn_mma_kernel<true, NTOK_> : ffn_mma_kernel<false, NTOK_>;
     cudaError_t e = ensure_smem_attr(kern, (int)sizeof(Smem));
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: mma kernel shared memory");
     e = launch_pdl(kern, dim3((unsigned)(MmaCfg<NTOK_>::MIN_BLOCKS * num_sms())), dim3(THREADS), sizeof(Smem), s,
-                   (const SlotDesc*)t->d_desc, t->codebook, fc1 ? x16s : (const uint16_t*)a16, sorted_pair, weights, k,
-                   t->H, t->I, header, chunks, a16, out, mode, NTOK_ == MMA_NT_FP4 ? 1 : 0);
+                   (const SlotDesc*)t->d_desc, t->codebook, fc1 ? x16s : a16, sorted_pair, weights, k, t->H, t->I,
+                   header, chunks, reinterpret_cast<const float*>(ws + L.xsc_off),
+                   reinterpret_cast<const float*>(ws + L.asc_off), reinterpret_cast<float*>(ws + L.a32_off),
+                   reinterpret_cast<uint32_t*>(ws + L.amax_off), out, mode, NTOK_ == MMA_NT_FP4 ? 1 : 0);
     if (e != cudaSuccess) return cuda_status(e, fc1 ? "moe_vq2_expert_ffn: FC1 launch" : "moe_vq2_expert_ffn: FC2 launch");
     return MOE_OK;
 }

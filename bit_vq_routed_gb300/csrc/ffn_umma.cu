@@ -17,8 +17,9 @@
 //     and tcgen05.commit frees each stage when the tensor core is done;
 //   - 4 epilogue warps read the accumulators back with tcgen05.ld (each warp
 //     owns one quarter of the TMEM lanes = weight rows) and store FC1's
-//     a = silu(g) * u as fp16 (the FC2 B operand) or FC2's y per pair / w*y
-//     into the token's output.
+//     a = silu(g) * u in fp32 with its largest magnitude per token (a
+//     conversion kernel then makes the fp16 FC2 B operand), or FC2's y per
+//     pair / w*y into the token's output.
 // The accumulators are double-buffered in TMEM, so the epilogue of one item
 // overlaps the main loop of the next.  Every wait is bounded: a wait that
 // gives up records an error word and the CTA runs on to its end without
@@ -101,13 +102,16 @@ struct DecRegs {
 
 // FC1 (FC1 = true): items = (chunk, 128-row tile of I), A = gate and up tiles.
 // FC2: items = (chunk, 256-row tile of H), A = two 128-row down tiles.
+// The B rows are scaled by powers of two (x16s = x / xsc, a16 = a / asc, per
+// sorted position); the epilogue multiplies the scale back in fp32.  FC1
+// writes a in fp32 (a32) and the largest |a| of each sorted position (amax).
 template <bool FC1>
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_umma_kernel(const __grid_constant__ CUtensorMap bmap, const SlotDesc* __restrict__ desc,
                     const uint16_t* __restrict__ codebook, const int32_t* __restrict__ sorted_pair,
                     const float* __restrict__ weights, int k, int H, int I, int* __restrict__ header,
-                    const Chunk* __restrict__ uchunks, uint16_t* __restrict__ a16, float* __restrict__ out,
-                    int mode) {
+                    const Chunk* __restrict__ uchunks, const float* __restrict__ xsc, const float* __restrict__ asc,
+                    float* __restrict__ a32, uint32_t* __restrict__ amax, float* __restrict__ out, int mode) {
     extern __shared__ __align__(1024) uint8_t dyn[];
     // the swizzled operand tiles need 1024-byte alignment in the shared window
     Smem& S = *reinterpret_cast<Smem*>(dyn + ((1024u - (smem_u32(dyn) & 1023u)) & 1023u));
@@ -317,10 +321,17 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
                         const int tok = c0 + q;
-                        if (tok < ch.count) {
-                            const float gv = v[q];
-                            a16[(size_t)(ch.start + tok) * I + irow] =
-                                __half_as_ushort(__float2half_rn(gv / (1.0f + expf(-gv)) * u[q]));
+                        if (tok < ch.count) {  // (the same for every lane)
+                            const int spos = ch.start + tok;
+                            const float sc = xsc[spos];
+                            const float gv = v[q] * sc, uv = u[q] * sc;
+                            const float av = gv / (1.0f + expf(-gv)) * uv;
+                            a32[(size_t)spos * I + irow] = av;
+                            // largest |a| of the token over the warp's 32 rows
+                            // (non-negative floats order as their bits), at least
+                            // 1 so that the conversion sees the position as written
+                            const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(av)));
+                            if (lane == 0) atomicMax(amax + spos, max(mb, 1u));
                         }
                     }
                 } else {
@@ -333,11 +344,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                             const int tok = c0 + q;
                             if (tok < ch.count) {
                                 const int spos = ch.start + tok;
+                                const float y = v[q] * asc[spos];
                                 if (mode == MOE_PER_PAIR) {
-                                    out[(size_t)spos * H + h] = v[q];
+                                    out[(size_t)spos * H + h] = y;
                                 } else {
                                     const int p = sorted_pair[spos];
-                                    atomicAdd(out + (size_t)(p / k) * H + h, weights[p] * v[q]);
+                                    atomicAdd(out + (size_t)(p / k) * H + h, weights[p] * y);
                                 }
                             }
                         }
@@ -353,28 +365,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == MMA_WARP) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
-    }
-}
-
-// x16s[s, :] = fp16(x[token of sorted position s, :]) for the tensor-core B operand
-__global__ void __launch_bounds__(256) gather_f16_kernel(const uint16_t* __restrict__ x,
-                                                         const int32_t* __restrict__ sorted_pair, int k, int H,
-                                                         int P, uint16_t* __restrict__ x16s) {
-    pdl_wait();
-    pdl_launch_dependents();  // dependents may start their prologues now
-    const long long n = (long long)P * (H / 8);
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-        const int s = (int)(i / (H / 8)), c = (int)(i % (H / 8));
-        const int t = sorted_pair[s] / k;
-        const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + 8 * c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const __half2 h = __floats2half2_rn(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
-            o[q] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        *reinterpret_cast<uint4*>(x16s + (size_t)s * H + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -410,16 +400,6 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int cols) {
 
 size_t umma_smem_bytes() { return sizeof(Smem) + 1024; }
 
-moe_status launch_gather_f16(const uint16_t* x, const int32_t* sorted_pair, int k, int H, int P, uint16_t* x16s,
-                             cudaStream_t s) {
-    long long n = (long long)P * (H / 8);
-    long long blocks = (n + 255) / 256, cap = (long long)num_sms() * 8;
-    cudaError_t e = launch_pdl(gather_f16_kernel, dim3((unsigned)(blocks < cap ? blocks : cap)), dim3(256), 0, s, x,
-                               sorted_pair, k, H, P, x16s);
-    if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: gather launch");
-    return MOE_OK;
-}
-
 moe_status launch_umma(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
                        int P, int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s) {
     int* header = reinterpret_cast<int*>(ws);
@@ -437,7 +417,9 @@ moe_status launch_umma(bool fc1, const SlotTableHost* t, const int32_t* sorted_p
     cudaError_t e = ensure_smem_attr(kern, smem);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: tensor-core kernel shared memory");
     e = launch_pdl(kern, dim3((unsigned)num_sms()), dim3(THREADS), (size_t)smem, s, map, (const SlotDesc*)t->d_desc,
-                   t->codebook, sorted_pair, weights, k, H, I, header, uchunks, a16, out, mode);
+                   t->codebook, sorted_pair, weights, k, H, I, header, uchunks,
+                   reinterpret_cast<const float*>(ws + L.xsc_off), reinterpret_cast<const float*>(ws + L.asc_off),
+                   reinterpret_cast<float*>(ws + L.a32_off), reinterpret_cast<uint32_t*>(ws + L.amax_off), out, mode);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: tensor-core launch");
     return MOE_OK;
 }

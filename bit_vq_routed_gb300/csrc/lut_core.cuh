@@ -143,26 +143,61 @@ __device__ __forceinline__ int unit_row(int lane) {
     return (pp >> 1) + 8 * (pp & 1);
 }
 
+// The table's power-of-two scale.  Every entry |dot(cb[c], x_G)| is at most
+// m = max |x| over the K-range times the largest L1 norm of a codebook row;
+// the table holds fp16(entry / s) with s = 2^e, m / s <= 2^15 (e clamped to
+// [-120, 120]), and each unit's sums are multiplied back by s.  Both scalings
+// are exact, so the fp16 entries cannot overflow whatever the range of the
+// inputs, and for inputs in the normal range the results equal those of
+// unscaled entries bit for bit.  Block-wide (every thread calls it, after the
+// inputs are in xs); red: 2 * LW words of shared scratch, which the caller
+// must not pass to another call before a CTA barrier.  Returns e.
+__device__ __forceinline__ int table_exponent(const float* xs, int nin, const float* cb, unsigned* red, int tid) {
+    float xm = 0.0f, c1 = 0.0f;
+    for (int i = tid; i < nin; i += THREADS) xm = fmaxf(xm, fabsf(xs[xs_at(i)]));
+    if (tid < 128) c1 = fabsf(cb[4 * tid]) + fabsf(cb[4 * tid + 1]) + fabsf(cb[4 * tid + 2]) + fabsf(cb[4 * tid + 3]);
+    // non-negative floats order as their bit patterns
+    const unsigned ux = __reduce_max_sync(0xffffffffu, __float_as_uint(xm));
+    const unsigned uc = __reduce_max_sync(0xffffffffu, __float_as_uint(c1));
+    if ((tid & 31) == 0) {
+        red[tid >> 5] = ux;
+        red[LW + (tid >> 5)] = uc;
+    }
+    __syncthreads();
+    unsigned mx = 0, mc = 0;
+    for (int w = 0; w < LW; ++w) {
+        mx = max(mx, red[w]);
+        mc = max(mc, red[LW + w]);
+    }
+    int ex = 0, ec = 0;
+    frexpf(__uint_as_float(mx), &ex);  // max |x| < 2^ex
+    frexpf(__uint_as_float(mc), &ec);
+    return min(max(ex + ec - 15, -120), 120);
+}
+__device__ __forceinline__ float exp2_int(int e) { return __int_as_float((e + 127) << 23); }  // 2^e, |e| <= 126
+
 // Table of one K-range from xs (inputs at xs_at, fp32) and cb (the fp32
-// codebook, [128][4]): a thread takes a quad of words (the 4 lanes
-// 4 lq .. 4 lq + 3 of scale block bq, in group-slot pair (j0, j0 + 1),
-// j0 = 4p + 2jj: the 8 consecutive groups 32 bq + 4 j0 + 0..7) and every
-// LW-th code.  nkb: scale blocks (x 128 inputs) in the K-range.
-__device__ __forceinline__ void build_table(const float* xs, const float* cb, int nkb, int tid) {
+// codebook, [128][4]), its entries divided by 2^e (table_exponent): a thread
+// takes a quad of words (the 4 lanes 4 lq .. 4 lq + 3 of scale block bq, in
+// group-slot pair (j0, j0 + 1), j0 = 4p + 2jj: the 8 consecutive groups
+// 32 bq + 4 j0 + 0..7) and every LW-th code.  nkb: scale blocks (x 128
+// inputs) in the K-range.
+__device__ __forceinline__ void build_table(const float* xs, const float* cb, int nkb, int e, int tid) {
     const int warp = tid >> 5;
     const int q = tid & 31, lq = q & 7, jj = (q >> 3) & 1, p = q >> 4, bq = lane_block(4 * lq);
     if (bq >= nkb) return;
     const int g0 = 32 * bq + 4 * (4 * p + 2 * jj);
     // xp[m][i] = (x[4(g0+m)+i], x[4(g0+4+m)+i]): the low / high half of word m
     float2 xp[4][4];
+    const float inv = exp2_int(-e);
 #pragma unroll
     for (int mm = 0; mm < 4; ++mm) {
         const float4 lo = *reinterpret_cast<const float4*>(&xs[xs_at(4 * (g0 + mm))]);
         const float4 hi = *reinterpret_cast<const float4*>(&xs[xs_at(4 * (g0 + 4 + mm))]);
-        xp[mm][0] = make_float2(lo.x, hi.x);
-        xp[mm][1] = make_float2(lo.y, hi.y);
-        xp[mm][2] = make_float2(lo.z, hi.z);
-        xp[mm][3] = make_float2(lo.w, hi.w);
+        xp[mm][0] = make_float2(lo.x * inv, hi.x * inv);
+        xp[mm][1] = make_float2(lo.y * inv, hi.y * inv);
+        xp[mm][2] = make_float2(lo.z * inv, hi.z * inv);
+        xp[mm][3] = make_float2(lo.w * inv, hi.w * inv);
     }
     const uint32_t a0 = TAB + (uint32_t)p * PLANE + 128u * jj + 16u * lq;
     // (run once per table: kept rolled, two codes per pass, so that its

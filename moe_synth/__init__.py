@@ -153,6 +153,21 @@ def tokens(T: int, H: int, seed: int, layer: int = 0, stream: int = 0) -> np.nda
     return bf16_bits(r.normal(0.0, 1.0, size=(T, H)).astype(np.float32))
 
 
+def tokens_outliers(T: int, H: int, seed: int, n_channels: int = 4, lo: float = 1e3, hi: float = 1e5,
+                    stream: int = 0) -> np.ndarray:
+    """bf16 bits [T, H]: N(0,1) activations with n_channels outlier channels
+    (the same channels for every token, as activation outliers of language
+    models are), each value of magnitude log-uniform in [lo, hi] with a
+    random sign; the first outlier of token 0 has magnitude hi."""
+    r = _rng(seed, 0, _TAG_TOKENS, 1000 + stream)
+    x = r.normal(0.0, 1.0, size=(T, H))
+    ch = r.choice(H, size=n_channels, replace=False)
+    mag = np.exp(r.uniform(np.log(lo), np.log(hi), size=(T, n_channels)))
+    mag[0, 0] = hi
+    x[:, ch] = mag * r.choice([-1.0, 1.0], size=(T, n_channels))
+    return bf16_bits(x.astype(np.float32))
+
+
 # The five workloads of the benchmark and parity suite.
 def spec_tiny(seed: int = 0) -> LayerSpec:
     """hidden 256, intermediate 128, 8 experts, top-2, 4 tokens."""
