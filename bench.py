@@ -76,6 +76,10 @@ WORKLOADS = {
                          desc="decode batch 8, 52 most routed experts FP4 (MXFP4), 204 VQ2, Zipf(1.1)"),
     "prefill_4096": dict(T=4096, layers=1, zipf=1.1, fp4_top=0, pool=1,
                          desc="prefill chunk 4096 tokens, Zipf(1.1), H4096 I2048 E256 top-8"),
+    "tandem_mixed_b8": dict(T=8, layers=1, zipf=1.1, fp4_top=52, pool=8, gpu_resident=96,
+                            desc="decode batch 8, 52 most routed experts FP4, 204 VQ2, Zipf(1.1); only the 96 most "
+                                 "routed experts in the GPU slot table, the pairs of the other 160 computed on "
+                                 "the host's cores at the same time (GPU partial + CPU remainder)"),
     "decode_b1_fetch": dict(T=1, layers=1, zipf=1.1, fp4_top=0, pool=256, slots=64,
                             desc="decode batch 1, Zipf(1.1) router bias, H4096 I2048 E256 top-8, the 256 "
                                  "experts in page-locked host memory, a GPU expert cache of 64 slots "
@@ -488,6 +492,120 @@ def run_fetch(args, wl, world, rank, local):
                        "steps_with_a_miss": sum(1 for n in fetched if n > 0)})
 
 
+def run_tandem(args, wl, world, rank, local):
+    """The decode step with the GPU holding only the wl["gpu_resident"] most
+    routed experts and the host's cores computing the pairs of the others,
+    overlapped with the GPU's call (TandemForward)."""
+    import torch
+    import bit_vq_routed_gb300 as bv
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    layer = make_layers(wl)[0]
+    s = layer.spec
+    T, G = wl["T"], wl["pool"]
+    res = np.zeros(s.E, bool)
+    res[ms.most_popular(layer, wl["gpu_resident"])] = True
+    dev, keep = bv.upload_layer(s.H, s.I, s.E, s.k, T, layer.codebook, layer.w_router, layer.bias,
+                                lambda e: (lambda ex: (ex.fmt, ex.codes, ex.scales))(layer.expert(e, cache=False)),
+                                s.renormalize, np.nonzero(res)[0])
+    hx = bv.HostExperts(s.E)
+    host_bytes = 0
+    for e in np.nonzero(~res)[0]:
+        ex = layer.expert(int(e), cache=False)
+        fmt, pc, ps = bv.host_pack_expert(ex.fmt, ex.codes, ex.scales)
+        hx.set(int(e), fmt, pc, ps)
+        host_bytes += sum(a.nbytes for a in pc) + sum(a.nbytes for a in ps)
+    pool = bv.CpuPool(0)
+    step = bv.TandemForward(dev, pool, hx, T)
+    toks = torch.from_numpy(token_pool(wl, 0).view(np.int16)).view(torch.bfloat16).pin_memory()  # [G, T, H]
+    stream = torch.cuda.current_stream()
+    for w in range(args.warmup):
+        step.step(toks[w % G])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    cpu_s, cpu_pairs, cpu_bytes = [], [], []
+    clocks = ClockSampler(local)
+    clocks.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(args.steps):
+        sl = (args.warmup + i) % G
+        step.step(toks[sl], evs[i])
+        cpu_s.append(step.last["cpu_s"])
+        cpu_pairs.append(step.last["cpu_pairs"])
+        ids = step.ids_host.numpy()
+        miss = np.unique(ids[~res[ids]])
+        cpu_bytes.append(sum(VQ2_EXPERT_BYTES if layer.formats[e] == ms.FMT_VQ2 else FP4_EXPERT_BYTES for e in miss))
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_total = max_over_ranks(start.elapsed_time(end))
+    gpu_ms = [a.elapsed_time(b) for a, b in evs]
+    # the same steps' GPU expert bytes (resident experts touched)
+    gpu_bytes = []
+    for i in range(args.steps):
+        dev.route(toks[(args.warmup + i) % G].cuda())
+        ids = dev.ids[:T].cpu().numpy()
+        hit = np.unique(ids[res[ids]])
+        gpu_bytes.append(sum(VQ2_EXPERT_BYTES if layer.formats[e] == ms.FMT_VQ2 else FP4_EXPERT_BYTES for e in hit))
+    pool_threads = pool.threads
+    launches = args.steps * step.kernels_per_step
+    pool.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return dict(ms_total=ms_total, gpu_ms=gpu_ms, cpu_s=cpu_s, cpu_pairs=cpu_pairs, cpu_bytes=cpu_bytes,
+                gpu_bytes=gpu_bytes, clocks=clk, threads=pool_threads, host_bytes=host_bytes, launches=launches)
+
+
+def tandem_line(args, wl, r, world, config):
+    T = wl["T"]
+    ms_step = r["ms_total"] / args.steps
+    hbm, _, peak_src = measured_peaks()
+    gpu_ms = float(np.mean(r["gpu_ms"]))
+    achieved = float(np.mean(r["gpu_bytes"])) / (gpu_ms / 1000.0) / 1e9
+    cpu_ms = 1000.0 * float(np.mean(r["cpu_s"]))
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)",
+            "kernel": "the GPU's expert graph (moe_vq2_expert_ffn over the 96 resident experts + moe_combine), "
+                      "timed with events around its replay while the host computes the remainder",
+            "algorithmic_bytes_per_launch": float(np.mean(r["gpu_bytes"])), "avg_launch_ms": gpu_ms,
+            "traffic": None, "traffic_source": "no ncu capture of this workload"}
+    if args.no_cpu:
+        tps, cores, what = None, None, "skipped (--no-cpu)"
+    else:
+        tps, cores, what, _, _ = oracle_time(wl, make_layers(wl), budget_s=args.cpu_budget, max_steps=4)
+    return {
+        "metric": METRIC, "value": job_rate(T, world, ms_step), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16*f16->f32 (bf16 activations); host fp32",
+        "data": "synthetic (seeded; random weights, no trained checkpoint)", "config": config,
+        "roofline": roof,
+        "host_experts": {"threads": r["threads"], "cpu_ms_per_step": cpu_ms,
+                         "pairs_per_step": float(np.mean(r["cpu_pairs"])),
+                         "code_bytes_per_step": float(np.mean(r["cpu_bytes"])),
+                         "gbs": float(np.mean(r["cpu_bytes"])) / (cpu_ms / 1000.0) / 1e9 if cpu_ms > 0 else None,
+                         "host_base_bytes": r["host_bytes"],
+                         "overlap": "the GPU's expert graph is enqueued before the host computes; the step waits "
+                                    "for both, then adds the remainder on the device"},
+        "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what,
+                         "cpu": cpu_model()},
+        "e2e": {"value": job_rate(T, world, ms_step), "unit": UNIT, "h2d_bytes_per_step": T * 4096 * 2 + T * 4096 * 4,
+                "d2h_bytes_per_step": T * 8 * 8,
+                "how": "every step copies its tokens from page-locked host memory and reads the routed ids and "
+                       "weights back, inside the timed region (the step's output stays on the device)"},
+        "gpu_launches": r["launches"],
+        "launch": "routing graph, read-back of ids/weights, expert graph (GPU) and moe_cpu_expert_ffn (host) "
+                  "at the same time, then the remainder's copy and moe_accumulate",
+        "clocks": r["clocks"],
+    }
+
+
 def fetch_line(args, wl, r, world, config):
     T = wl["T"]
     ms_step = r["ms_total"] / args.steps
@@ -564,6 +682,12 @@ def main():
         print(json.dumps(line))
         return
 
+    if "gpu_resident" in wl:
+        r = run_tandem(args, wl, world, rank, local)
+        if rank == 0:
+            config["l2"] = f"tokens rotate over a pool of {wl['pool']} batches; the host computes from its own memory"
+            print(json.dumps(tandem_line(args, wl, r, world, config)))
+        return
     if "slots" in wl:
         r = run_fetch(args, wl, world, rank, local)
         if rank == 0:

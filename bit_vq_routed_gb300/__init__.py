@@ -56,7 +56,9 @@ EXPORTED = [
     "moe_launch_count", "moe_route_workspace_size", "moe_route", "moe_vq2_expert_ffn_combine",
     "moe_selftest", "moe_expert_cache_slot_bytes", "moe_expert_cache_create", "moe_expert_cache_set_host",
     "moe_expert_cache_fetch", "moe_expert_cache_slot_of", "moe_expert_cache_stats", "moe_expert_cache_plan",
-    "moe_expert_cache_destroy", "moe_expert_cache_set_host_image",
+    "moe_expert_cache_destroy", "moe_expert_cache_set_host_image", "moe_cpu_pool_create", "moe_cpu_pool_threads",
+    "moe_cpu_pool_destroy", "moe_cpu_expert_ffn", "moe_accumulate", "moe_slot_table_resident", "moe_vq2_pack_host",
+    "moe_fp4_pack_host",
 ]
 
 
@@ -104,6 +106,14 @@ def load(path: Optional[str] = None, build_if_stale: bool = True):
         "moe_expert_cache_plan": ([I, I, P, P, P, ctypes.c_uint64, P, I, P, P, ctypes.POINTER(I)], I),
         "moe_expert_cache_destroy": ([P, P], I),
         "moe_expert_cache_set_host_image": ([P, I, I, P], I),
+        "moe_cpu_pool_create": ([I, ctypes.POINTER(P)], I),
+        "moe_cpu_pool_threads": ([P], I),
+        "moe_cpu_pool_destroy": ([P], I),
+        "moe_cpu_expert_ffn": ([P, I, I, P, ctypes.POINTER(_ExpertDesc), I, P, P, P, P, I, I, P], I),
+        "moe_accumulate": ([P, P, Z, P], I),
+        "moe_slot_table_resident": ([P, I], I),
+        "moe_vq2_pack_host": ([P, P, I, I, P, P], I),
+        "moe_fp4_pack_host": ([P, P, I, I, P, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -407,5 +417,137 @@ class ExpertCache:
             pass
 
 
-from .layer import (GraphedForward, GraphedStep, MissFetchForward, MoELayer, host_expert,  # noqa: E402,F401
-                    host_expert_image, upload_layer)
+# ------------------------------------------------------------------ host CPU path
+
+def _np_ptr(a, dtype=None):
+    """(pointer, keep-alive) of a contiguous host array: a numpy array or a
+    CPU torch tensor."""
+    import numpy as np
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda:
+            raise ValueError("expected a host array")
+        a = a.contiguous()
+        return a.data_ptr(), a
+    arr = np.ascontiguousarray(a if dtype is None else np.asarray(a, dtype=dtype))
+    return arr.ctypes.data, arr
+
+
+def moe_vq2_pack_host(codes, scales):
+    """Packs a logical VQ2 matrix on the host (uint8 [rows, K/4], fp16 bits
+    [rows, K/4/32]) into the slot layout; returns (packed codes, packed
+    scales) as numpy arrays of the same shapes and types."""
+    import numpy as np
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.uint16)
+    rows, G = c.shape
+    pc, ps = np.empty_like(c), np.empty_like(sc)
+    _check(load().moe_vq2_pack_host(c.ctypes.data, sc.ctypes.data, rows, 4 * G, pc.ctypes.data, ps.ctypes.data))
+    return pc, ps
+
+
+def moe_fp4_pack_host(codes, scales):
+    """The same for a logical FP4 matrix (uint8 [rows, K/2], uint8 [rows, K/32])."""
+    import numpy as np
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows, nb = c.shape
+    pc, ps = np.empty_like(c), np.empty_like(sc)
+    _check(load().moe_fp4_pack_host(c.ctypes.data, sc.ctypes.data, rows, 2 * nb, pc.ctypes.data, ps.ctypes.data))
+    return pc, ps
+
+
+def host_pack_expert(fmt: int, codes: Sequence, scales: Sequence):
+    """One expert's three matrices packed on the host: (fmt, [codes x3], [scales x3])."""
+    pack = moe_vq2_pack_host if fmt == MOE_FMT_VQ2 else moe_fp4_pack_host
+    pcs, pss = [], []
+    for m in range(3):
+        pc, ps = pack(codes[m], scales[m])
+        pcs.append(pc)
+        pss.append(ps)
+    return fmt, pcs, pss
+
+
+class CpuPool:
+    """moe_cpu_pool: host threads for moe_cpu_expert_ffn (threads <= 0: all)."""
+
+    def __init__(self, threads: int = 0):
+        self.lib = load()
+        h = ctypes.c_void_p()
+        _check(self.lib.moe_cpu_pool_create(threads, ctypes.byref(h)))
+        self.handle = h
+
+    @property
+    def threads(self) -> int:
+        return int(self.lib.moe_cpu_pool_threads(self.handle))
+
+    def close(self):
+        if self.handle is not None:
+            h, self.handle = self.handle, None
+            _check(self.lib.moe_cpu_pool_destroy(h))
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class HostExperts:
+    """The moe_expert_desc array of host-resident packed experts that
+    moe_cpu_expert_ffn reads: entry e is (fmt, [codes x3], [scales x3]) host
+    arrays (host_pack_expert) or None.  Keeps the arrays alive."""
+
+    def __init__(self, E: int):
+        self.E = E
+        self.descs = (_ExpertDesc * E)()
+        self._keep = {}
+
+    def set(self, e: int, fmt: int, codes: Sequence, scales: Sequence):
+        d = self.descs[e]
+        d.format = fmt
+        keep = []
+        for m in range(3):
+            pc, kc = _np_ptr(codes[m])
+            ps, ks = _np_ptr(scales[m])
+            d.codes[m] = pc
+            d.scales[m] = ps
+            keep += [kc, ks]
+        self._keep[e] = keep
+
+
+def moe_cpu_expert_ffn(pool: CpuPool, H: int, I: int, codebook, experts: HostExperts, x, ids, weights,
+                       gpu_status, k: int, out=None):
+    """The remainder of the combine over the pairs with gpu_status 0,
+    computed on the host (see the C header).  x: host bf16 bits [T, H];
+    ids int32 / weights fp32 [T, k]; gpu_status uint8 [T*k]; out: host fp32
+    [T, H] (allocated when None).  Returns out."""
+    import numpy as np
+    xp, xk = _np_ptr(x, np.uint16)
+    ip, ik = _np_ptr(ids, np.int32)
+    wp, wk = _np_ptr(weights, np.float32)
+    sp, sk = _np_ptr(gpu_status, np.uint8)
+    cp, ck = _np_ptr(codebook, np.uint16)
+    T = int(np.prod(xk.shape)) // H
+    if out is None:
+        out = np.empty((T, H), np.float32)
+    op, ok = _np_ptr(out)
+    _check(load().moe_cpu_expert_ffn(pool.handle, H, I, cp, experts.descs, experts.E, xp, ip, wp, sp, T, k, op))
+    return out
+
+
+def moe_accumulate(dst, src, stream=None):
+    """dst += src on the device (fp32 CUDA tensors of equal size)."""
+    if dst.numel() != src.numel():
+        raise ValueError("moe_accumulate: sizes differ")
+    _check(load().moe_accumulate(_ptr(dst), _ptr(src), dst.numel(), _stream(stream)))
+
+
+def moe_slot_table_resident(table: "SlotTable", expert_id: int) -> bool:
+    r = int(load().moe_slot_table_resident(table.handle, expert_id))
+    if r < 0:
+        _check(r)
+    return r == 1
+
+
+from .layer import (GraphedForward, GraphedStep, MissFetchForward, MoELayer, TandemForward,  # noqa: E402,F401
+                    host_expert, host_expert_image, upload_layer)

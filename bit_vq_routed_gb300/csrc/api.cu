@@ -153,6 +153,20 @@ moe_status moe_slot_table_evict(moe_slot_table* t, int expert_id, cudaStream_t s
     return st;
 }
 
+int moe_slot_table_resident(const moe_slot_table* t, int expert_id) {
+    if (!t || expert_id < 0 || expert_id >= t->h.E) {
+        set_error("moe_slot_table_resident: null table or expert_id=%d out of range", expert_id);
+        return MOE_ERR_INVALID_ARG;
+    }
+    return t->h.h_fmt[expert_id] != 0 ? 1 : 0;
+}
+
+moe_status moe_accumulate(float* dst, const float* src, size_t n, cudaStream_t stream) {
+    if (n == 0) return MOE_OK;
+    MOE_CHECK_ARG(dst && src, "moe_accumulate: null pointer");
+    return launch_accumulate(dst, src, n, stream);
+}
+
 moe_status moe_slot_table_destroy(moe_slot_table* t) {
     if (!t) return MOE_OK;
     cudaError_t e = cudaFree(t->h.d_desc);

@@ -57,7 +57,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     }
 }
 
+// dst[i] += src[i] (the GPU's partial output plus a remainder computed elsewhere)
+__global__ void __launch_bounds__(256) accumulate_kernel(float* __restrict__ dst, const float* __restrict__ src,
+                                                         size_t n) {
+    pdl_wait();
+    pdl_launch_dependents();
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] += src[i];
+}
+
 }  // namespace
+
+moe_status launch_accumulate(float* dst, const float* src, size_t n, cudaStream_t s) {
+    const size_t blocks = (n + 255) / 256, cap = (size_t)num_sms() * 8;
+    cudaError_t e = launch_pdl(accumulate_kernel, dim3((unsigned)(blocks < cap ? blocks : cap)), dim3(256), 0, s, dst,
+                               src, n);
+    if (e != cudaSuccess) return cuda_status(e, "moe_accumulate: launch");
+    return MOE_OK;
+}
 
 moe_status launch_combine(const float* ypair, const int32_t* p2s, const float* w, const uint8_t* st, int T,
                           int k, int H, float* out32, uint16_t* out16, cudaStream_t s) {

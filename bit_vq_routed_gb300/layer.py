@@ -291,6 +291,84 @@ class MissFetchForward:
         return self.out
 
 
+class TandemForward:
+    """The forward of a layer whose GPU slot table holds only some experts,
+    with the host's cores computing the pairs of the others at the same time
+    (Tandem-vLLM page, "How it works": experts that miss the GPU cache are
+    computed by the CPU in parallel with the GPU, nothing skipped or
+    substituted).
+
+    Each step: the tokens are copied in and the routing graph replays; the
+    routed ids and weights are read back (one device-to-host copy and one
+    wait); the expert graph (the GPU's expert FFN over its resident experts,
+    then the combine of their pairs: the partial output) is enqueued; while
+    it runs, moe_cpu_expert_ffn computes the remainder over the pairs of the
+    other experts on the host, from host copies of their packed weights
+    (host_experts); the remainder is copied in and added (moe_accumulate).
+    The GPU reports the pairs it skipped in pair_status; the host decides the
+    same set beforehand from the table's host mirror (moe_slot_table_resident).
+    """
+
+    def __init__(self, layer: MoELayer, pool, host_experts, T: int, device="cuda"):
+        from . import moe_slot_table_resident
+        self.layer, self.pool, self.host_experts, self.T = layer, pool, host_experts, T
+        H, k = layer.H, layer.k
+        self.x = torch.zeros(T, H, dtype=torch.bfloat16, device=device)
+        self.out = layer.out[:T]
+        self.ids_host = torch.empty(T, k, dtype=torch.int32).pin_memory()
+        self.w_host = torch.empty(T, k, dtype=torch.float32).pin_memory()
+        self.rem_host = torch.empty(T, H, dtype=torch.float32).pin_memory()
+        self.rem_dev = torch.empty(T, H, dtype=torch.float32, device=device)
+        self.codebook_host = layer.codebook.cpu().view(torch.int16).numpy().view(np.uint16)
+        self.resident = np.array([moe_slot_table_resident(layer.table, e) for e in range(layer.E)], dtype=bool)
+        from . import moe_launch_count
+        layer.forward(self.x)  # first eager call: kernel attributes are set outside capture
+        torch.cuda.synchronize()
+        n0 = moe_launch_count()
+        self.g_route = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_route):
+            layer.route(self.x)
+        self.g_ffn = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_ffn):
+            layer.experts(self.x, MOE_PER_PAIR)
+            moe_combine(layer.ypair[:T * k], layer.pair_to_sorted[:T * k], layer.weights[:T],
+                        layer.pair_status[:T * k], k, self.out)
+        # library kernels per step: the two graphs' nodes and moe_accumulate
+        self.kernels_per_step = moe_launch_count() - n0 + 1
+        self.last = {}
+
+    def step(self, x_host: torch.Tensor, events=None) -> torch.Tensor:
+        """x_host: bf16 [T, H] in page-locked host memory.  Returns the fp32
+        [T, H] output on the device (enqueued: synchronise before reading).
+        events: optional (gpu_start, gpu_end) CUDA events recorded around the
+        expert graph; self.last holds the pairs and the host seconds of the
+        CPU part."""
+        import time
+        from . import moe_accumulate, moe_cpu_expert_ffn
+        L, T, k = self.layer, self.T, self.layer.k
+        self.x.copy_(x_host, non_blocking=True)
+        self.g_route.replay()
+        self.ids_host.copy_(L.ids[:T], non_blocking=True)
+        self.w_host.copy_(L.weights[:T], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        ids = self.ids_host.numpy()
+        status = self.resident[ids].astype(np.uint8).ravel()
+        if events is not None:
+            events[0].record()
+        self.g_ffn.replay()  # the GPU's partial output, running while the host computes
+        if events is not None:
+            events[1].record()
+        t0 = time.perf_counter()
+        moe_cpu_expert_ffn(self.pool, L.H, L.I, self.codebook_host, self.host_experts,
+                           x_host.view(torch.int16).numpy().view(np.uint16), ids, self.w_host.numpy(), status, k,
+                           self.rem_host.numpy())
+        cpu_s = time.perf_counter() - t0
+        self.rem_dev.copy_(self.rem_host, non_blocking=True)
+        moe_accumulate(self.out, self.rem_dev)
+        self.last = dict(cpu_pairs=int((status == 0).sum()), cpu_s=cpu_s)
+        return self.out
+
+
 def upload_layer(H, I, E, k, T_max, codebook, w_router, bias, experts, renormalize=1, resident=None,
                  stream=None, device="cuda"):
     """Builds a MoELayer and makes resident the experts in ``resident`` (all

@@ -398,6 +398,69 @@ moe_status moe_combine(const float* ypair, const int32_t* pair_to_sorted, const 
                        const uint8_t* pair_status, int T, int k, int H, float* out_f32,
                        uint16_t* out_bf16, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------- */
+/* Experts the GPU does not hold, computed on the host's cores              */
+/* ---------------------------------------------------------------------- */
+/*
+ * Tandem-vLLM page, "How it works": experts that miss the GPU cache are
+ * computed by the CPU in parallel with the GPU; nothing is skipped or
+ * substituted.  The GPU computes the pairs of its resident experts
+ * (moe_vq2_expert_ffn reports the others with pair_status 0) and their
+ * combine (moe_combine: the partial output); meanwhile the host computes
+ * the pairs with status 0 (moe_cpu_expert_ffn: the remainder); the layer's
+ * output is partial + remainder (moe_accumulate on the device).
+ */
+typedef struct moe_cpu_pool moe_cpu_pool;
+
+/* A pool of host threads for moe_cpu_expert_ffn: threads - 1 workers (the
+ * calling thread is the last one); threads <= 0 takes every hardware thread.
+ * One pool serves one caller at a time.  Errors: MOE_ERR_INVALID_ARG,
+ * MOE_ERR_NO_MEM (threads could not be started). */
+moe_status moe_cpu_pool_create(int threads, moe_cpu_pool** out);
+/* Threads of the pool, the calling one included (0 for NULL). */
+int moe_cpu_pool_threads(const moe_cpu_pool* pool);
+moe_status moe_cpu_pool_destroy(moe_cpu_pool* pool);
+
+/* The remainder of the combine over the pairs the GPU did not compute:
+ *     out[t] = sum over j = 0..k-1 (in that order) with gpu_status[t*k+j]
+ *              == 0 of weights[t,j] * y_{t,j},
+ *     y_{t,j} = Wd_e (silu(Wg_e x_t) * (Wu_e x_t)),  e = ids[t,j],
+ * in fp32 on the pool's threads, from HOST copies of the experts' packed
+ * codes and scales (the layouts of moe_vq2_pack / moe_fp4_pack: the bytes a
+ * slot holds, e.g. an expert cache's page-locked base).
+ * experts: host array [E] of descriptors with host pointers; the entries of
+ * the experts that gpu_status names need all six buffers, the others are not
+ * read.  codebook: host fp16 [128*4]; x: host bf16 [T, H]; ids int32 and
+ * weights fp32 [T, k] (host copies of moe_route's outputs); gpu_status:
+ * host uint8 [T*k] (pair_status of moe_vq2_expert_ffn, or computed from
+ * moe_slot_table_resident before the GPU call); out: host fp32 [T, H],
+ * written (rows of tokens without such a pair are zero).  Synchronous: it
+ * returns when out is written; it touches no device memory and makes no
+ * CUDA call, so it overlaps GPU work the caller enqueued before.
+ * Requires H % 256 == 0, I % 128 == 0.  Errors: MOE_ERR_INVALID_ARG (a null
+ * pointer, an id outside [0, E), a needed expert without buffers),
+ * MOE_ERR_UNSUPPORTED (shape), MOE_ERR_NO_MEM (host scratch). */
+moe_status moe_cpu_expert_ffn(moe_cpu_pool* pool, int H, int I, const uint16_t* codebook,
+                              const moe_expert_desc* experts, int E, const uint16_t* x, const int32_t* ids,
+                              const float* weights, const uint8_t* gpu_status, int T, int k, float* out);
+
+/* dst[i] += src[i] for i < n, fp32, on the device (the GPU's partial output
+ * plus the host's remainder, copied to the device).  Enqueue only. */
+moe_status moe_accumulate(float* dst, const float* src, size_t n, cudaStream_t stream);
+
+/* 1 if the table holds an entry for expert_id, 0 if not (from the table's
+ * host mirror: no device access, no synchronisation); MOE_ERR_INVALID_ARG
+ * for a null table or an id out of range. */
+int moe_slot_table_resident(const moe_slot_table* t, int expert_id);
+
+/* moe_vq2_pack / moe_fp4_pack on the host (the same packed layouts, for a
+ * host-resident base or where no GPU is at hand): host pointers, no CUDA
+ * call.  Same requirements and errors as the device calls. */
+moe_status moe_vq2_pack_host(const uint8_t* codes, const uint16_t* scales, int rows, int K,
+                             uint8_t* packed_codes, uint16_t* packed_scales);
+moe_status moe_fp4_pack_host(const uint8_t* codes, const uint8_t* scales, int rows, int K,
+                             uint8_t* packed_codes, uint8_t* packed_scales);
+
 /* Boot self-check (Tandem-vLLM page, "New in 0.2.0": each kernel is checked
  * against a reference at boot).  Runs a tiny layer (hidden 256, intermediate
  * 128, 8 experts, top-2) through the entry points above on the current
