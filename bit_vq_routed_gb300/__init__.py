@@ -58,7 +58,7 @@ EXPORTED = [
     "moe_expert_cache_fetch", "moe_expert_cache_slot_of", "moe_expert_cache_stats", "moe_expert_cache_plan",
     "moe_expert_cache_destroy", "moe_expert_cache_set_host_image", "moe_cpu_pool_create", "moe_cpu_pool_threads",
     "moe_cpu_pool_destroy", "moe_cpu_expert_ffn", "moe_accumulate", "moe_slot_table_resident", "moe_vq2_pack_host",
-    "moe_fp4_pack_host",
+    "moe_fp4_pack_host", "moe_vq2_encoder_workspace_size", "moe_vq2_train_codebook", "moe_vq2_encode",
 ]
 
 
@@ -114,6 +114,9 @@ def load(path: Optional[str] = None, build_if_stale: bool = True):
         "moe_slot_table_resident": ([P, I], I),
         "moe_vq2_pack_host": ([P, P, I, I, P, P], I),
         "moe_fp4_pack_host": ([P, P, I, I, P, P], I),
+        "moe_vq2_encoder_workspace_size": ([I, I], Z),
+        "moe_vq2_train_codebook": ([P, I, I, P, I, P, P, P, Z, P], I),
+        "moe_vq2_encode": ([P, I, I, P, I, P, P, P, Z, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -547,6 +550,37 @@ def moe_slot_table_resident(table: "SlotTable", expert_id: int) -> bool:
     if r < 0:
         _check(r)
     return r == 1
+
+
+# ------------------------------------------------------------------ encoder
+
+def moe_vq2_train_codebook(W: torch.Tensor, init_idx, iters: int, stream=None):
+    """The layer codebook from dense fp32 weights W [rows, K] (CUDA): k-means
+    from the normalised group vectors at init_idx (128 indices).  Returns
+    (codebook fp16 [128, 4], centroids fp32 [128, 4]) on the device."""
+    import numpy as np
+    rows, K = W.shape
+    idx = np.ascontiguousarray(np.asarray(init_idx, dtype=np.int64).ravel())
+    if idx.size != 128:
+        raise ValueError("init_idx needs 128 indices")
+    ws = torch.empty(load().moe_vq2_encoder_workspace_size(rows, K), dtype=torch.uint8, device=W.device)
+    cb = torch.empty(128, 4, dtype=torch.float16, device=W.device)
+    C = torch.empty(128, 4, dtype=torch.float32, device=W.device)
+    _check(load().moe_vq2_train_codebook(_ptr(W), rows, K, idx.ctypes.data, iters, _ptr(cb), _ptr(C), _ptr(ws),
+                                         ws.numel(), _stream(stream)))
+    return cb, C
+
+
+def moe_vq2_encode(W: torch.Tensor, codebook: torch.Tensor, iters: int = 3, stream=None):
+    """Codes uint8 [rows, K/4] and scales fp16 [rows, K/128] (logical layout)
+    of dense fp32 weights W [rows, K] (CUDA) with a fp16 codebook [128, 4]."""
+    rows, K = W.shape
+    ws = torch.empty(load().moe_vq2_encoder_workspace_size(rows, K), dtype=torch.uint8, device=W.device)
+    codes = torch.empty(rows, K // 4, dtype=torch.uint8, device=W.device)
+    scales = torch.empty(rows, K // 128, dtype=torch.float16, device=W.device)
+    _check(load().moe_vq2_encode(_ptr(W), rows, K, _ptr(codebook), iters, _ptr(codes), _ptr(scales), _ptr(ws),
+                                 ws.numel(), _stream(stream)))
+    return codes, scales
 
 
 from .layer import (GraphedForward, GraphedStep, MissFetchForward, MoELayer, TandemForward,  # noqa: E402,F401

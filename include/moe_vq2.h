@@ -461,6 +461,43 @@ moe_status moe_vq2_pack_host(const uint8_t* codes, const uint16_t* scales, int r
 moe_status moe_fp4_pack_host(const uint8_t* codes, const uint8_t* scales, int rows, int K,
                              uint8_t* packed_codes, uint8_t* packed_scales);
 
+/* ---------------------------------------------------------------------- */
+/* VQ2 encoder: dense weights -> codebook, codes and scales                 */
+/* ---------------------------------------------------------------------- */
+/*
+ * The vLLM-Moet page ("2-bit experts on vLLM v0.24.0") puts the routed
+ * experts on a sign-symmetric 2-bit codebook (naive 2-bit fails through sign
+ * asymmetry); the German vLLM-Moet page quantises the weights at start-up.
+ * The pages give no algorithm; this library's (every decision in fp32 in one
+ * fixed operation order, the k-means sums exact integers, so results are the
+ * same on every run):
+ *   1. block scale sigma[r, b] = sqrt(mean of W[r, i]^2 over the 128 inputs
+ *      of block b); normalised group vectors u = W[r, 4g..4g+3] / sigma;
+ *   2. codebook (moe_vq2_train_codebook): k-means over the normalised
+ *      vectors with the codebook read as 128 pairs {+c, -c}: u goes to the
+ *      pair i maximising 2 |u . c_i| - |c_i|^2, sign s = sign(u . c_i); c_i
+ *      becomes the mean of s u over its members; started from the vectors at
+ *      init_idx (host int64 [128], indices into the rows*K/4 groups,
+ *      row-major); the codebook is the result rounded to fp16;
+ *   3. encoding (moe_vq2_encode): the block's scale starts at sigma; each
+ *      iteration assigns its 32 groups (u = W / scale) and refits the scale by
+ *      least squares (sum W.q / sum q.q, q = s c_i); the scale is rounded to
+ *      fp16 and the groups assigned once more: codes uint8 [rows, K/4] (bit 7
+ *      = 1 for s = -1), scales fp16 [rows, K/128], the logical layout of
+ *      moe_vq2_pack.
+ * W: device fp32 [rows, K] row-major, K % 128 == 0.  ws: device scratch of
+ * moe_vq2_encoder_workspace_size(rows, K) bytes.  centroids (optional):
+ * device fp32 [128*4], the codebook before rounding.  Enqueue only.
+ * Errors: MOE_ERR_INVALID_ARG (null pointers, an index out of range, a
+ * workspace too small), MOE_ERR_UNSUPPORTED (K % 128 != 0), MOE_ERR_CUDA.
+ */
+size_t moe_vq2_encoder_workspace_size(int rows, int K);
+moe_status moe_vq2_train_codebook(const float* W, int rows, int K, const int64_t* init_idx, int iters,
+                                  uint16_t* codebook, float* centroids, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream);
+moe_status moe_vq2_encode(const float* W, int rows, int K, const uint16_t* codebook, int iters, uint8_t* codes,
+                          uint16_t* scales, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Boot self-check (Tandem-vLLM page, "New in 0.2.0": each kernel is checked
  * against a reference at boot).  Runs a tiny layer (hidden 256, intermediate
  * 128, 8 experts, top-2) through the entry points above on the current

@@ -36,6 +36,7 @@ FMT_FP4 = 1
 # stream tags
 _TAG_TOKENS, _TAG_WR, _TAG_CB, _TAG_RANK = 1, 2, 3, 4
 _TAG_CODES, _TAG_SCALES = 10, 20
+_TAG_DENSE = 30
 
 
 def bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -166,6 +167,18 @@ def tokens_outliers(T: int, H: int, seed: int, n_channels: int = 4, lo: float = 
     mag[0, 0] = hi
     x[:, ch] = mag * r.choice([-1.0, 1.0], size=(T, n_channels))
     return bf16_bits(x.astype(np.float32))
+
+
+def dense_weights(rows: int, K: int, seed: int, std: float = 0.013, stream: int = 0) -> np.ndarray:
+    """fp32 [rows, K] of N(0, std^2) weights (dense input of the encoder)."""
+    r = _rng(seed, 0, _TAG_DENSE, stream)
+    return r.normal(0.0, std, size=(rows, K)).astype(np.float32)
+
+
+def encoder_init_indices(n_groups: int, seed: int, n: int = 128) -> np.ndarray:
+    """n distinct indices in [0, n_groups) (int64): where the codebook's
+    k-means starts."""
+    return _rng(seed, 0, _TAG_DENSE, 999).choice(n_groups, size=n, replace=False).astype(np.int64)
 
 
 # The five workloads of the benchmark and parity suite.
