@@ -58,7 +58,7 @@ EXPORTED = [
     "moe_expert_cache_fetch", "moe_expert_cache_slot_of", "moe_expert_cache_stats", "moe_expert_cache_plan",
     "moe_expert_cache_destroy", "moe_expert_cache_set_host_image", "moe_cpu_pool_create", "moe_cpu_pool_threads",
     "moe_cpu_pool_destroy", "moe_cpu_expert_ffn", "moe_accumulate", "moe_slot_table_resident", "moe_vq2_pack_host",
-    "moe_fp4_pack_host", "moe_vq2_encoder_workspace_size", "moe_vq2_train_codebook", "moe_vq2_encode",
+    "moe_fp4_pack_host", "moe_confidence_gate", "moe_vq2_encoder_workspace_size", "moe_vq2_train_codebook", "moe_vq2_encode",
 ]
 
 
@@ -114,6 +114,7 @@ def load(path: Optional[str] = None, build_if_stale: bool = True):
         "moe_slot_table_resident": ([P, I], I),
         "moe_vq2_pack_host": ([P, P, I, I, P, P], I),
         "moe_fp4_pack_host": ([P, P, I, I, P, P], I),
+        "moe_confidence_gate": ([P, P, P, I, I, I, ctypes.c_float, P, P], I),
         "moe_vq2_encoder_workspace_size": ([I, I], Z),
         "moe_vq2_train_codebook": ([P, I, I, P, I, P, P, P, Z, P], I),
         "moe_vq2_encode": ([P, I, I, P, I, P, P, P, Z, P], I),
@@ -552,6 +553,14 @@ def moe_slot_table_resident(table: "SlotTable", expert_id: int) -> bool:
     return r == 1
 
 
+def moe_confidence_gate(table: "SlotTable", ids, weights, E: int, tau: float, gated_ids, stream=None):
+    """gated_ids = ids + E where weights >= tau and the table holds entry
+    E + id (the expert's FP4 weights), ids elsewhere (see the C header)."""
+    T, k = ids.shape
+    _check(load().moe_confidence_gate(table.handle, _ptr(ids), _ptr(weights), T, k, E, tau, _ptr(gated_ids),
+                                      _stream(stream)))
+
+
 # ------------------------------------------------------------------ encoder
 
 def moe_vq2_train_codebook(W: torch.Tensor, init_idx, iters: int, stream=None):
@@ -583,5 +592,5 @@ def moe_vq2_encode(W: torch.Tensor, codebook: torch.Tensor, iters: int = 3, stre
     return codes, scales
 
 
-from .layer import (GraphedForward, GraphedStep, MissFetchForward, MoELayer, TandemForward,  # noqa: E402,F401
-                    host_expert, host_expert_image, upload_layer)
+from .layer import (GatedForward, GraphedForward, GraphedStep, MissFetchForward, MoELayer,  # noqa: E402,F401
+                    TandemForward, host_expert, host_expert_image, upload_layer, upload_expert)

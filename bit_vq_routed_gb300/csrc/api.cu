@@ -161,6 +161,20 @@ int moe_slot_table_resident(const moe_slot_table* t, int expert_id) {
     return t->h.h_fmt[expert_id] != 0 ? 1 : 0;
 }
 
+moe_status moe_confidence_gate(const moe_slot_table* table, const int32_t* ids, const float* weights, int T, int k,
+                               int E, float tau, int32_t* gated_ids, cudaStream_t stream) {
+    MOE_CHECK_ARG(table, "moe_confidence_gate: null table");
+    MOE_CHECK_ARG(T >= 0 && k >= 1 && E >= 1, "moe_confidence_gate: T=%d k=%d E=%d", T, k, E);
+    MOE_CHECK_ARG(table->h.E >= 2 * E, "moe_confidence_gate: the table has %d entries, 2E = %d needed", table->h.E,
+                  2 * E);
+    MOE_CHECK_ARG(!(tau != tau), "moe_confidence_gate: tau is NaN");
+    if (T == 0) return MOE_OK;
+    MOE_CHECK_ARG(ids && weights && gated_ids, "moe_confidence_gate: null pointer");
+    long long P = (long long)T * k;
+    MOE_CHECK_SUPPORTED(P <= (1 << 24), "moe_confidence_gate: T*k=%lld above 2^24", P);
+    return launch_gate(table->h.d_desc, ids, weights, (int)P, E, tau, gated_ids, stream);
+}
+
 moe_status moe_accumulate(float* dst, const float* src, size_t n, cudaStream_t stream) {
     if (n == 0) return MOE_OK;
     MOE_CHECK_ARG(dst && src, "moe_accumulate: null pointer");

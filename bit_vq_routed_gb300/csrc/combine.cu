@@ -66,7 +66,29 @@ __global__ void __launch_bounds__(256) accumulate_kernel(float* __restrict__ dst
         dst[i] += src[i];
 }
 
+// gated[p] = ids[p] + E when weights[p] >= tau and entry E + ids[p] is resident
+__global__ void __launch_bounds__(256) gate_kernel(const SlotDesc* __restrict__ desc, const int32_t* __restrict__ ids,
+                                                   const float* __restrict__ weights, int P, int E, float tau,
+                                                   int32_t* __restrict__ gated) {
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P; p += gridDim.x * blockDim.x) {
+        const int e = ids[p];
+        const bool g = e >= 0 && e < E && weights[p] >= tau && desc[E + e].resident != 0;
+        gated[p] = g ? e + E : e;
+    }
+}
+
 }  // namespace
+
+moe_status launch_gate(const SlotDesc* desc, const int32_t* ids, const float* weights, int P, int E, float tau,
+                       int32_t* gated, cudaStream_t s) {
+    const int blocks = (P + 255) / 256, cap = num_sms() * 4;
+    cudaError_t e = launch_pdl(gate_kernel, dim3((unsigned)(blocks < cap ? blocks : cap)), dim3(256), 0, s, desc, ids,
+                               weights, P, E, tau, gated);
+    if (e != cudaSuccess) return cuda_status(e, "moe_confidence_gate: launch");
+    return MOE_OK;
+}
 
 moe_status launch_accumulate(float* dst, const float* src, size_t n, cudaStream_t s) {
     const size_t blocks = (n + 255) / 256, cap = (size_t)num_sms() * 8;

@@ -293,6 +293,8 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
                              const int32_t* pair_to_sorted = nullptr, float* comb32 = nullptr,
                              uint16_t* comb16 = nullptr);
 moe_status launch_accumulate(float* dst, const float* src, size_t n, cudaStream_t s);
+moe_status launch_gate(const SlotDesc* desc, const int32_t* ids, const float* weights, int P, int E, float tau,
+                       int32_t* gated, cudaStream_t s);
 moe_status launch_combine(const float* ypair, const int32_t* p2s, const float* w, const uint8_t* st,
                           int T, int k, int H, float* out32, uint16_t* out16, cudaStream_t s);
 

@@ -53,26 +53,31 @@ def upload_expert(fmt: int, codes: Sequence, scales: Sequence, stream=None, devi
 
 
 class MoELayer:
+    """Device buffers and the call sequence of one layer.  table_experts: the
+    slot table's entries (E when None; 2E for the confidence gate, whose
+    entries E..2E-1 hold FP4 weights)."""
+
     def __init__(self, H: int, I: int, E: int, k: int, T_max: int, codebook, w_router, bias=None,
-                 renormalize: int = 1, device="cuda"):
+                 renormalize: int = 1, device="cuda", table_experts: Optional[int] = None):
         self.H, self.I, self.E, self.k, self.T_max = H, I, E, k, T_max
+        self.table_experts = E if table_experts is None else table_experts
         self.renormalize = renormalize
         self.codebook = _dev(codebook, torch.float16, device).contiguous()
         self.w_router = _dev(w_router, torch.bfloat16, device).contiguous()
         self.bias = None if bias is None else _dev(bias, torch.float32, device).contiguous()
-        self.table = SlotTable(E, H, I, self.codebook)
+        self.table = SlotTable(self.table_experts, H, I, self.codebook)
         P = T_max * k
         f32, i32 = torch.float32, torch.int32
         self.logits = torch.empty(T_max, E, dtype=f32, device=device)
         self.ids = torch.empty(T_max, k, dtype=i32, device=device)
         self.weights = torch.empty(T_max, k, dtype=f32, device=device)
-        self.offsets = torch.empty(E + 1, dtype=i32, device=device)
+        self.offsets = torch.empty(self.table_experts + 1, dtype=i32, device=device)
         self.sorted_pair = torch.empty(P, dtype=i32, device=device)
         self.pair_to_sorted = torch.empty(P, dtype=i32, device=device)
         self.pair_status = torch.empty(P, dtype=torch.uint8, device=device)
         self.ypair = torch.empty(P, H, dtype=f32, device=device)
         self.out = torch.empty(T_max, H, dtype=f32, device=device)
-        self.ws = torch.empty(moe_vq2_expert_ffn_workspace_size(T_max, k, E, H, I), dtype=torch.uint8,
+        self.ws = torch.empty(moe_vq2_expert_ffn_workspace_size(T_max, k, self.table_experts, H, I), dtype=torch.uint8,
                               device=device)
         # (zero-filled once; moe_route leaves its counter at zero)
         self.route_ws = torch.zeros(moe_route_workspace_size(T_max, k, E), dtype=torch.uint8, device=device)
@@ -366,6 +371,91 @@ class TandemForward:
         self.rem_dev.copy_(self.rem_host, non_blocking=True)
         moe_accumulate(self.out, self.rem_dev)
         self.last = dict(cpu_pairs=int((status == 0).sum()), cpu_s=cpu_s)
+        return self.out
+
+
+class GatedForward:
+    """The forward with the confidence gate over an FP4 delta cache (the
+    vLLM-Moet page, "2-bit experts on vLLM v0.24.0": a delta cache and a
+    confidence gate bring FP4 back where it matters; its bench table: "FP4
+    delta (auto) + confidence gate tau=0.60").  The layer's slot table has
+    2E entries: the 2-bit base of expert e at e, its FP4 weights at E + e
+    while held.  A step: the routing; moe_confidence_gate (pairs with router
+    weight >= tau whose FP4 entry is set go to entry E + e); the permutation
+    over 2E entries; the expert FFN; the combine.
+
+    With cache (an ExpertCache over the same table whose host images are the
+    experts' FP4 weights, named E + e), the step is split at the routing:
+    the routed ids and weights are read back, the cache fetches the FP4
+    entries of the pairs the gate wants (routing counts decide the
+    evictions), then the rest runs.  Without it, the FP4 entries set on the
+    table are used as they are and the whole step is one CUDA graph."""
+
+    def __init__(self, layer: MoELayer, T: int, tau: float = 0.6, cache=None, device="cuda"):
+        from . import moe_confidence_gate, moe_permute_workspace_size
+        if layer.table_experts < 2 * layer.E:
+            raise ValueError("the layer's table needs 2E entries")
+        self.layer, self.T, self.tau, self.cache = layer, T, tau, cache
+        E, k = layer.E, layer.k
+        P = T * k
+        i32 = torch.int32
+        self.x = torch.zeros(T, layer.H, dtype=torch.bfloat16, device=device)
+        self.out = layer.out[:T]
+        self.gated = torch.empty(T, k, dtype=i32, device=device)
+        self.offsets2 = torch.empty(2 * E + 1, dtype=i32, device=device)
+        self.sorted2 = torch.empty(P, dtype=i32, device=device)
+        self.p2s2 = torch.empty(P, dtype=i32, device=device)
+        self.perm_ws = torch.empty(max(moe_permute_workspace_size(T, k, 2 * E), 16), dtype=torch.uint8,
+                                   device=device)
+        self.ids_host = torch.empty(T, k, dtype=i32).pin_memory()
+        self.w_host = torch.empty(T, k, dtype=torch.float32).pin_memory()
+        self._gate = moe_confidence_gate
+        if cache is not None:
+            layer.route(self.x)  # (the rest reads the routing)
+        self._rest()  # first eager call: kernel attributes are set outside capture
+        torch.cuda.synchronize()
+        self.g_route = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_route):
+            layer.route(self.x)
+        self._capture_rest()
+        self.last = {}
+
+    def _rest(self):
+        L, T, k, E = self.layer, self.T, self.layer.k, self.layer.E
+        P = T * k
+        if self.cache is None:
+            L.route(self.x)
+        self._gate(L.table, L.ids[:T], L.weights[:T], E, self.tau, self.gated)
+        moe_permute(self.gated, 2 * E, self.offsets2, self.sorted2, self.p2s2, self.perm_ws)
+        moe_vq2_expert_ffn(L.table, self.x, self.offsets2, self.sorted2, L.weights[:T], k, MOE_PER_PAIR,
+                           L.ypair[:P], L.pair_status[:P], L.ws)
+        moe_combine(L.ypair[:P], self.p2s2, L.weights[:T], L.pair_status[:P], k, self.out)
+
+    def _capture_rest(self):
+        self.g_rest = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_rest):
+            self._rest()
+
+    def step(self, x=None) -> torch.Tensor:
+        """x: bf16 [T, H] on the device (or None when self.x holds the
+        tokens).  Returns the fp32 [T, H] output (enqueued)."""
+        if x is not None:
+            self.x.copy_(x, non_blocking=True)
+        if self.cache is None:
+            self.g_rest.replay()  # (the routing is inside)
+            return self.out
+        L, T, E = self.layer, self.T, self.layer.E
+        self.g_route.replay()
+        self.ids_host.copy_(L.ids[:T], non_blocking=True)
+        self.w_host.copy_(L.weights[:T], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        ids, w = self.ids_host.numpy(), self.w_host.numpy()
+        want = np.unique(ids[w >= self.tau]) + E
+        r = self.cache.fetch(want) if want.size else dict(n_fetched=0, n_unplaced=0, recapture=False)
+        if r["recapture"]:
+            self._capture_rest()
+        self.last = dict(wanted=int(want.size), **r)
+        self.g_rest.replay()
         return self.out
 
 

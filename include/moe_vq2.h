@@ -462,6 +462,32 @@ moe_status moe_fp4_pack_host(const uint8_t* codes, const uint8_t* scales, int ro
                              uint8_t* packed_codes, uint8_t* packed_scales);
 
 /* ---------------------------------------------------------------------- */
+/* Confidence gate over an FP4 delta cache                                  */
+/* ---------------------------------------------------------------------- */
+/*
+ * vLLM-Moet page, "2-bit experts on vLLM v0.24.0": a delta cache and a
+ * confidence gate bring FP4 back where it matters; its bench table runs
+ * "FP4 delta (auto) + confidence gate tau=0.60".  The pages say no more; this
+ * library's reading:
+ *   - a slot table of (at least) 2E entries holds expert e's 2-bit base at
+ *     entry e and, while the delta cache holds them, e's FP4 weights at entry
+ *     E + e (any number of them, set like any entry or by an expert cache);
+ *   - the confidence of a pair is its router weight; a pair whose weight is
+ *     at least tau and whose expert's FP4 entry is set uses the FP4 weights,
+ *     every other pair the 2-bit base.
+ * moe_confidence_gate writes gated_ids [T, k] (device int32): ids + E for
+ * such pairs, ids otherwise (entry residency read on the device, so a
+ * captured graph follows the cache).  moe_permute over the gated ids with
+ * 2E experts, moe_vq2_expert_ffn over the 2E-entry table and moe_combine
+ * then compute the layer; nothing else changes.  tau = 0.60 is the pages'
+ * value; a tau above 1 turns the gate off.  ids, weights: device, from
+ * moe_route_topk (E = the router's expert count).  Errors:
+ * MOE_ERR_INVALID_ARG (null pointers, a table of fewer than 2E entries, NaN
+ * tau). */
+moe_status moe_confidence_gate(const moe_slot_table* table, const int32_t* ids, const float* weights, int T, int k,
+                               int E, float tau, int32_t* gated_ids, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* VQ2 encoder: dense weights -> codebook, codes and scales                 */
 /* ---------------------------------------------------------------------- */
 /*
