@@ -45,11 +45,14 @@ FFN_FLOP_PER_PAIR = 2 * 3 * 4096 * 2048  # gate, up and down matvecs of one (tok
 L2_BYTES = 129 * 2 ** 20
 
 # DRAM bytes (read + write) of one expert-FFN call, from one ncu capture of its
-# kernels (profiles/ffn_lut_decode_b1.md: FC1 35,737,856 + 512, FC2 18,547,456
-# at decode batch 1).  Reported only while the kernel sources hash to the ones
-# the counters were taken on.
-TRAFFIC = {"decode_b1": {"bytes": 54_285_824, "profile": "profiles/ffn_lut_decode_b1.md",
-                         "sources": ["ffn_lut.cu", "ffn_common.cuh", "common.cuh"],
+# kernels (the two single-token table kernels, ffn_lut_kernel<1,1> and
+# ffn_lut_kernel<0,1>, of `python bench.py --layers 1 --steps 3 --warmup 3
+# --no-cpu` under ncu: FC1 35,737,856 + 512, FC2 18,547,456 at decode batch 1).
+# Reported only while the kernel sources hash to the ones the counters were
+# taken on.
+TRAFFIC = {"decode_b1": {"bytes": 54_285_824,
+                         "profile": "ncu capture of ffn_lut_kernel<1,1> and ffn_lut_kernel<0,1>, decode batch 1",
+                         "sources": ["ffn_lut.cu", "lut_core.cuh", "ffn_common.cuh", "common.cuh"],
                          "sha256": "f2c050a3bd2af8d485068e1620e39826e385fa04d5dd574552113867a7e04d06"}}
 
 

@@ -96,9 +96,20 @@ def test_prefill_4096_routing_exact_and_sampled_outputs(torch):
     assert np.array_equal(g["offsets"], off) and np.array_equal(g["sorted_pair"], sp)
     counts = np.diff(off)
     assert counts.max() > 1000  # hot experts get prefill-sized batches
-    # sample: 12 spread tokens + every token of the coldest non-empty expert
-    cold = int(np.argmin(np.where(counts > 0, counts, 1 << 30)))
-    cold_tokens = sp[off[cold]:off[cold + 1]] // 8
-    sample = np.unique(np.concatenate([np.linspace(0, T - 1, 12).astype(int), cold_tokens]))
+    # sample: 256 spread tokens, every token of the 4 coldest non-empty
+    # experts, and every token of the two busiest experts with 4..31 tokens
+    # (the mma.sync kernels inside the prefill call; hotter experts take the
+    # tcgen05 kernels, the spread tokens reach them)
+    nz = np.nonzero(counts)[0]
+    cold4 = nz[np.argsort(counts[nz], kind="stable")[:4]]
+    band = nz[(counts[nz] >= 4) & (counts[nz] <= 31)]
+    mma2 = band[np.argsort(counts[band], kind="stable")[-2:]]
+    assert len(cold4) == 4 and len(mma2) == 2
+    toks = [sp[off[e]:off[e + 1]] // 8 for e in np.concatenate([cold4, mma2])]
+    sample = np.unique(np.concatenate([np.linspace(0, T - 1, 256).astype(int)] + toks))
     r = O.moe_layer(layer, x, tokens=sample)
     assert_close(g["out"][sample], r["out"], "prefill sample")
+    for e in np.concatenate([cold4, mma2]):  # each expert's own tokens too
+        te = np.unique(sp[off[e]:off[e + 1]] // 8)
+        rows = np.searchsorted(sample, te)
+        assert_close(g["out"][te], r["out"][rows], f"prefill tokens of expert {e} ({counts[e]} tokens)")
