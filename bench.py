@@ -654,6 +654,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling)")
+    ap.add_argument("--tokens", type=int, default=0, help="override the workload's tokens per step (profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--eager", dest="graph", action="store_false",
                     help="launch every call from Python instead of replaying one CUDA graph per step")
@@ -662,6 +663,8 @@ def main():
     wl = dict(WORKLOADS[args.workload])
     if args.layers:
         wl["layers"] = args.layers
+    if args.tokens:
+        wl["T"] = args.tokens
     config = {"workload": wl["desc"], "name": args.workload, "tokens_per_step": wl["T"],
               "layers_per_step": wl["layers"],
               "l2": f"inputs larger than L2: each step touches its layers' routed experts "

@@ -151,6 +151,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     if (err) atomicExch(err, code);
     return false;
 }
+// try_wait that may suspend the thread for up to hint_ns nanoseconds while
+// the phase is incomplete (it returns as soon as the phase completes), so a
+// waiting warp issues a few instructions instead of a spin.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+// Bounded suspending wait: at most 2^18 tries of up to 1 us each; on
+// timeout records code in *err and returns false.
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint32_t bar, uint32_t parity, int* err, int code) {
+#pragma unroll 1
+    for (uint32_t it = 0; it < (1u << 18); ++it)
+        if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+    if (err) atomicExch(err, code);
+    return false;
+}
 // 1-D bulk copy global -> shared, completing on an mbarrier (16-byte
 // aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

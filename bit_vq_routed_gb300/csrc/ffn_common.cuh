@@ -12,7 +12,7 @@ constexpr int MMA_NT_VQ2 = 32; // tokens per mma.sync chunk of a VQ2 expert (fou
 constexpr int MMA_NT_FP4 = 16; // tokens per mma.sync chunk of an FP4 expert (two n8 MMA tiles)
 constexpr int LUT_KB = 8;      // scale blocks (x 128 inputs) per activation-table K-range
 constexpr int UMMA_MIN = 32;   // tokens from which an expert takes the tcgen05 path
-constexpr int UMMA_NT = 128;   // tokens per tcgen05 chunk
+constexpr int UMMA_NT = 256;   // tokens per tcgen05 chunk
 constexpr int MAX_LUT_CTAS = 1024;  // grid of the activation-table kernels (one CTA per SM) at most
 constexpr int LUT_MAX_M = 3;   // VQ2 experts with up to this many tokens take the activation-table path
 
@@ -48,8 +48,8 @@ enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NU
 // Range: x16s[s] holds x / xsc[s] and a16[s] holds a / asc[s], with xsc and
 // asc powers of two that bring the row's largest magnitude to at most 2^14,
 // so neither overflows fp16 whatever the range of the activations; the FC1
-// epilogues write a in fp32 (a32) with its largest magnitude per sorted
-// position (amax, float bits), from which the conversion kernel makes a16.
+// epilogues write a in fp32 (a32) and flag the sorted positions they wrote
+// (amax), from which the conversion kernel makes a16.
 struct WsLayout {
     size_t chunks_off, rec_off, grp_start_off, p1_off, p2_off, cnt_off, cnt2_off, range_off;
     size_t uchunks_off, x16s_off, a16_off, xsc_off, asc_off, amax_off, a32_off, total;

@@ -66,7 +66,7 @@ __device__ __forceinline__ uint32_t sh_u32(const uint8_t* p) { return *reinterpr
 // FC1 = false: A tiles are two down tiles (32 H-rows), B = a16 (K = I).
 // The B rows are scaled by powers of two (x16s = x / xsc, a16 = a / asc, per
 // sorted position); the epilogues multiply the scale back in fp32.  FC1
-// writes a in fp32 (a32) and the largest |a| of each sorted position (amax).
+// writes a in fp32 (a32) and flags each sorted position it wrote (amax).
 template <bool FC1, int NTOK_>
 __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_>::MIN_BLOCKS)
     ffn_mma_kernel(const SlotDesc* __restrict__ desc, const uint16_t* __restrict__ codebook,
@@ -282,22 +282,14 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_>::MIN_BLOCKS)
                 const int spos = ch.start + (valid ? tok : 0);
                 const float sc = valid ? (FC1 ? xsc[spos] : asc[spos]) : 0.0f;
                 if (FC1) {
-                    float am = 0.0f;
+                    if (valid) {
 #pragma unroll
-                    for (int hi = 0; hi < 2; ++hi) {
-                        const float g = acc[0][nt][b + 2 * hi] * sc, u = acc[1][nt][b + 2 * hi] * sc;
-                        const float av = g / (1.0f + expf(-g)) * u;
-                        if (valid) a32[(size_t)spos * I + rtt[0] * 16 + i + 8 * hi] = av;
-                        am = fmaxf(am, fabsf(av));
+                        for (int hi = 0; hi < 2; ++hi) {
+                            const float g = acc[0][nt][b + 2 * hi] * sc, u = acc[1][nt][b + 2 * hi] * sc;
+                            a32[(size_t)spos * I + rtt[0] * 16 + i + 8 * hi] = g / (1.0f + expf(-g)) * u;
+                        }
+                        if (i == 0) amax[spos] = 1;  // written: the conversion takes this position
                     }
-                    // largest |a| of this token over the warp's 16 rows (the 8 lanes
-                    // of this j; non-negative floats order as their bits), at least
-                    // 1 so that the conversion sees the position as written
-                    uint32_t mb = __float_as_uint(am);
-                    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-                    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
-                    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
-                    if (valid && i == 0) atomicMax(amax + spos, max(mb, 1u));
                 } else if (valid) {
 #pragma unroll
                     for (int t = 0; t < 2; ++t)

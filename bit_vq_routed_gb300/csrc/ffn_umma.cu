@@ -2,26 +2,28 @@
 // prefill-sized batch of tokens (m_e >= UMMA_MIN).  Here the expert FFN is a
 // dense contraction: FC1 is [m_e x H] x [H x 2I], FC2 [m_e x I] x [I x H].
 //
-// One CTA per SM loops over work items (chunk of <= 128 tokens of one
+// One CTA per SM loops over work items (chunk of <= 256 tokens of one
 // expert, two 128-row weight tiles: FC1 the gate and the up tile of the same
-// 128 rows, FC2 two consecutive down tiles).  Warp roles:
+// 128 rows, FC2 two consecutive down tiles): each decoded weight tile serves
+// up to 256 tokens.  Warp roles:
 //   - 8 decoder warps turn the item's VQ2 codes into fp16 weights
 //     (sign-folded codebook entry x row scale, rounded once to fp16) and store
 //     them into shared memory in the 128-byte-swizzled K-major layout the
 //     tensor core reads (A operand, 128 rows x 64 per K-block); each thread
 //     fetches its codes three K-blocks ahead;
-//   - a TMA warp loads the chunk's activations (B operand, 128 tokens x 64,
+//   - a TMA warp loads the chunk's activations (B operand, 256 tokens x 64,
 //     fp16, same swizzle) with cp.async.bulk.tensor from a token-gathered
 //     copy in the workspace;
-//   - one thread issues tcgen05.mma (M128 N128 K16, fp16 in, fp32 in TMEM)
-//     and tcgen05.commit frees each stage when the tensor core is done;
+//   - one thread issues tcgen05.mma (M128, N = the chunk's tokens rounded up
+//     to 16, at most 256, K16; fp16 in, fp32 in TMEM) and tcgen05.commit
+//     frees each stage when the tensor core is done;
 //   - 4 epilogue warps read the accumulators back with tcgen05.ld (each warp
 //     owns one quarter of the TMEM lanes = weight rows) and store FC1's
-//     a = silu(g) * u in fp32 with its largest magnitude per token (a
-//     conversion kernel then makes the fp16 FC2 B operand), or FC2's y per
-//     pair / w*y into the token's output.
-// The accumulators are double-buffered in TMEM, so the epilogue of one item
-// overlaps the main loop of the next.  Every wait is bounded: a wait that
+//     a = silu(g) * u in fp32 (a conversion kernel then makes the fp16 FC2 B
+//     operand), or FC2's y per pair / w*y into the token's output.
+// The two accumulators (2 x 256 columns) fill TMEM's 512 columns, so the
+// next item's MMAs start when the epilogue has read them (the decoders and
+// the TMA warp run ahead meanwhile).  Every wait is bounded: a wait that
 // gives up records an error word and the CTA runs on to its end without
 // issuing more work.
 #include <cudaTypedefs.h>
@@ -32,21 +34,24 @@ namespace moe {
 namespace {
 
 constexpr int UM_M = 128, UM_N = UMMA_NT, UM_K = 64;
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int DEC_WARPS = 8, EPI_WARPS = 4;
 constexpr int TMA_WARP = DEC_WARPS, MMA_WARP = DEC_WARPS + 1;  // then the epilogue warps
 constexpr int THREADS = 32 * (DEC_WARPS + 2 + EPI_WARPS);
 constexpr int A_BYTES = UM_M * UM_K * 2;      // 16 KB per A tile
-constexpr int B_BYTES = UM_N * UM_K * 2;      // 16 KB
+constexpr int B_BYTES = UM_N * UM_K * 2;      // 32 KB
 constexpr int CB_COPIES = 16;
-// instruction descriptor: D f32, A/B f16, both K-major, N = 128, M = 128
-constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(UM_N >> 3) << 17) | ((uint32_t)(UM_M >> 4) << 24);
+// instruction descriptor: D f32, A/B f16, both K-major, M = 128, N = n
+// (a multiple of 16, 16..256)
+__host__ __device__ constexpr uint32_t idesc_n(int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(UM_M >> 4) << 24);
+}
 
 struct __align__(1024) Smem {
     uint8_t a[STAGES][2][A_BYTES];  // FC1: gate tile, up tile; FC2: two down tiles
     uint8_t b[STAGES][B_BYTES];
     uint2 cbt[256 * CB_COPIES];     // sign-folded codebook, 16 copies
-    uint64_t full[STAGES], empty[STAGES], acc_full[2], acc_empty[2];
+    uint64_t full[STAGES], empty[STAGES], acc_full, acc_empty;
     uint32_t tmem_base;
     int failed;
 };
@@ -57,11 +62,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate));
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -104,7 +110,7 @@ struct DecRegs {
 // FC2: items = (chunk, 256-row tile of H), A = two 128-row down tiles.
 // The B rows are scaled by powers of two (x16s = x / xsc, a16 = a / asc, per
 // sorted position); the epilogue multiplies the scale back in fp32.  FC1
-// writes a in fp32 (a32) and the largest |a| of each sorted position (amax).
+// writes a in fp32 (a32) and flags each sorted position it wrote (amax).
 template <bool FC1>
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_umma_kernel(const __grid_constant__ CUtensorMap bmap, const SlotDesc* __restrict__ desc,
@@ -118,8 +124,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int* err = header + HDR_ERR;
     constexpr int NA = 2;                        // A tiles (and accumulators) per item
-    constexpr uint32_t ACC_COLS = NA * UM_N;     // TMEM columns of one accumulator set
-    constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
+    constexpr uint32_t TMEM_COLS = NA * UM_N;    // the two accumulators: all 512 columns
     const int K = FC1 ? H : I;
     const int R = FC1 ? I : H;
     const int n_rt = R / (FC1 ? UM_M : 2 * UM_M);
@@ -137,10 +142,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&S.full[s]), 32 * DEC_WARPS + 1);
             mbar_init(smem_u32(&S.empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&S.acc_full[b]), 1);
-            mbar_init(smem_u32(&S.acc_empty[b]), 32 * EPI_WARPS);
-        }
+        mbar_init(smem_u32(&S.acc_full), 1);
+        mbar_init(smem_u32(&S.acc_empty), 32 * EPI_WARPS);
         S.failed = 0;
     }
     if (warp == MMA_WARP) {  // allocate the accumulator columns (whole warp)
@@ -162,7 +165,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto failed = [&]() { return *reinterpret_cast<volatile int*>(&S.failed) != 0; };
     auto wait = [&](uint64_t* bar, uint32_t parity, int code) {
         if (failed()) return false;
-        if (!mbar_wait_bounded(smem_u32(bar), parity, err, code)) {
+        if (!mbar_wait_sleep_bounded(smem_u32(bar), parity, err, code)) {
             *reinterpret_cast<volatile int*>(&S.failed) = 1;
             return false;
         }
@@ -212,17 +215,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint8_t* abase = &S.a[stage][mat][0];
                 const uint32_t cw[4] = {r.c.x, r.c.y, r.c.z, r.c.w};
                 const uint32_t sw[8] = {r.s0.x, r.s0.y, r.s0.z, r.s0.w, r.s1.x, r.s1.y, r.s1.z, r.s1.w};
-                // plain shared-memory accesses, so the 16 independent
-                // lookup -> scale -> store chains can overlap
+                // the 16 codebook entries are loaded before any store into the
+                // tile (the compiler cannot tell the tile from the codebook,
+                // so loads placed after a store would wait for it), then
+                // scaled and stored: 16 independent chains in flight
+                uint2 e[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const uint32_t c = (cw[j >> 2] >> (8 * (j & 3))) & 0xffu;
+                    e[j] = S.cbt[c * CB_COPIES + (lane & 15)];
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
                     const int row = (j >> 1) + 8 * (j & 1);  // byte 2i+h holds row i + 8h
                     // the row's fp16 scale in both halves
                     const uint32_t s2 = prmt(sw[row >> 1], 0u, (row & 1) ? 0x3232u : 0x1010u);
-                    const uint2 e = S.cbt[c * CB_COPIES + (lane & 15)];
-                    __half2 w0 = __hmul2(*reinterpret_cast<const __half2*>(&e.x), *reinterpret_cast<const __half2*>(&s2));
-                    __half2 w1 = __hmul2(*reinterpret_cast<const __half2*>(&e.y), *reinterpret_cast<const __half2*>(&s2));
+                    __half2 w0 = __hmul2(*reinterpret_cast<const __half2*>(&e[j].x), *reinterpret_cast<const __half2*>(&s2));
+                    __half2 w1 = __hmul2(*reinterpret_cast<const __half2*>(&e[j].y), *reinterpret_cast<const __half2*>(&s2));
                     *reinterpret_cast<uint2*>(abase + boff[row & 7] + 128u * (uint32_t)row) =
                         make_uint2(*reinterpret_cast<uint32_t*>(&w0), *reinterpret_cast<uint32_t*>(&w1));
                 }
@@ -272,11 +281,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             int it = 0, nitem = 0;
             for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++nitem) {
-                const int buf = nitem & 1;
-                // the epilogue of item nitem - 2 must have read this accumulator set
-                if (nitem >= 2 && !wait(&S.acc_empty[buf], ((nitem >> 1) - 1) & 1, MOE_DEVERR_WAIT_EMPTY)) break;
+                const Chunk ch = uchunks[item / n_rt];
+                const uint32_t idesc = idesc_n(min(UM_N, (ch.count + 15) & ~15));
+                // the epilogue of the previous item must have read the accumulators
+                if (nitem >= 1 && !wait(&S.acc_empty, (nitem - 1) & 1, MOE_DEVERR_WAIT_EMPTY)) break;
                 tc_fence_after();
-                const uint32_t d0 = tmem + (uint32_t)buf * ACC_COLS;
+                const uint32_t d0 = tmem;
                 for (int kb64 = 0; kb64 < n_kblk; ++kb64, ++it) {
                     const int stage = it % STAGES, use = it / STAGES;
                     if (!wait(&S.full[stage], use & 1, MOE_DEVERR_WAIT_FULL)) break;
@@ -287,11 +297,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const uint64_t ad = sw128_desc(smem_u32(&S.a[stage][t][0]));
 #pragma unroll
                         for (int j = 0; j < UM_K / 16; ++j)  // 32 bytes of K per step inside the swizzle row
-                            umma_f16(d0 + t * UM_N, ad + 2 * j, bd + 2 * j, (kb64 > 0 || j > 0) ? 1u : 0u);
+                            umma_f16(d0 + t * UM_N, ad + 2 * j, bd + 2 * j, idesc, (kb64 > 0 || j > 0) ? 1u : 0u);
                     }
                     umma_commit(smem_u32(&S.empty[stage]));
                 }
-                umma_commit(smem_u32(&S.acc_full[buf]));
+                umma_commit(smem_u32(&S.acc_full));
             }
         }
     } else {
@@ -302,13 +312,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++nitem) {
             const Chunk ch = uchunks[item / n_rt];
             const int rt = item % n_rt;
-            const int buf = nitem & 1;
             int ok = 0;
-            if (lane == 0) ok = wait(&S.acc_full[buf], (nitem >> 1) & 1, MOE_DEVERR_WAIT_FULL) ? 1 : 0;
+            if (lane == 0) ok = wait(&S.acc_full, nitem & 1, MOE_DEVERR_WAIT_FULL) ? 1 : 0;
             __syncwarp();
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)buf * ACC_COLS;
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
             for (int c0 = 0; c0 < UM_N; c0 += 32) {
                 if (c0 >= ch.count) break;
@@ -325,13 +334,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             const int spos = ch.start + tok;
                             const float sc = xsc[spos];
                             const float gv = v[q] * sc, uv = u[q] * sc;
-                            const float av = gv / (1.0f + expf(-gv)) * uv;
-                            a32[(size_t)spos * I + irow] = av;
-                            // largest |a| of the token over the warp's 32 rows
-                            // (non-negative floats order as their bits), at least
-                            // 1 so that the conversion sees the position as written
-                            const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(av)));
-                            if (lane == 0) atomicMax(amax + spos, max(mb, 1u));
+                            a32[(size_t)spos * I + irow] = gv / (1.0f + expf(-gv)) * uv;
+                            if (lane == 0) amax[spos] = 1;  // written: the conversion takes this position
                         }
                     }
                 } else {
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(smem_u32(&S.acc_empty[buf]));
+            mbar_arrive(smem_u32(&S.acc_empty));
         }
     }
     tc_fence_before();
@@ -383,7 +387,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D fp16 [rows, cols] row-major, box of 64 columns x 128 rows, 128B swizzle
+// 2-D fp16 [rows, cols] row-major, box of 64 columns x 256 rows, 128B swizzle
 bool make_map(CUtensorMap* map, const void* base, int rows, int cols) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -398,6 +402,7 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int cols) {
 
 }  // namespace
 
+static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "tcgen05 kernel shared memory");
 size_t umma_smem_bytes() { return sizeof(Smem) + 1024; }
 
 moe_status launch_umma(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,

@@ -6,8 +6,8 @@
 //            position s (FC1's B operand), xsc[s] = 2^e with max |x[t, :]|
 //            / 2^e <= 2^14; amax[s] is cleared for the FC1 epilogues.
 //   convert: a16[s, :] = fp16(a32[s, :] / asc[s]) (FC2's B operand) for the
-//            sorted positions the tensor-core FC1 wrote (amax[s] > 0),
-//            asc[s] = 2^e with amax[s] / 2^e <= 2^14.
+//            sorted positions the tensor-core FC1 wrote (flag amax[s] set),
+//            asc[s] = 2^e with max |a32[s, :]| / 2^e <= 2^14.
 //
 // Dividing by a power of two is exact, so for activations in fp16's normal
 // range the operands, and the results once the epilogues multiply the scale
@@ -77,13 +77,19 @@ __global__ void __launch_bounds__(THREADS) a_to_f16_kernel(const float* __restri
                                                            uint16_t* __restrict__ a16, float* __restrict__ asc) {
     pdl_wait();
     pdl_launch_dependents();
+    __shared__ uint32_t red[THREADS / 32];
     for (int s = blockIdx.x; s < P; s += gridDim.x) {
-        const uint32_t mb = amax[s];
-        if (mb == 0) continue;  // not a tensor-core position (the FC1 epilogues store at least 1)
-        const int e = range_exponent(__uint_as_float(mb), 14);
-        const float inv = exp2_i(-e);
+        if (amax[s] == 0) continue;  // not a tensor-core position
         const float4* src = reinterpret_cast<const float4*>(a32 + (size_t)s * I);
         uint4* dst = reinterpret_cast<uint4*>(a16 + (size_t)s * I);
+        // largest |a| of the row (non-negative floats order as their bits)
+        uint32_t m = 0;
+        for (int c = threadIdx.x; c < I / 4; c += THREADS) {
+            const float4 v = src[c];
+            m = max(m, __float_as_uint(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)))));
+        }
+        const int e = range_exponent(__uint_as_float(block_max_u32(m, red)), 14);
+        const float inv = exp2_i(-e);
         for (int c = threadIdx.x; c < I / 8; c += THREADS) {
             const float4 lo = src[2 * c], hi = src[2 * c + 1];
             dst[c] = make_uint4(f2_to_h2(lo.x * inv, lo.y * inv), f2_to_h2(lo.z * inv, lo.w * inv),
