@@ -399,7 +399,7 @@ __global__ void __maxnreg__(MAX_REG)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int i = i0 + q * THREADS;
-                    if (i < nin) S.xs[xs_at(i)] = g[q] / (1.0f + expf(-g[q])) * up[q];
+                    if (i < nin) S.xs[xs_at(i)] = silu_mul(g[q], up[q]);
                 }
             }
             __syncthreads();

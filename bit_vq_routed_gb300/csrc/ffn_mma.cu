@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_>::MIN_BLOCKS)
 #pragma unroll
                         for (int hi = 0; hi < 2; ++hi) {
                             const float g = acc[0][nt][b + 2 * hi] * sc, u = acc[1][nt][b + 2 * hi] * sc;
-                            a32[(size_t)spos * I + rtt[0] * 16 + i + 8 * hi] = g / (1.0f + expf(-g)) * u;
+                            a32[(size_t)spos * I + rtt[0] * 16 + i + 8 * hi] = silu_mul(g, u);
                         }
                         if (i == 0) amax[spos] = 1;  // written: the conversion takes this position
                     }

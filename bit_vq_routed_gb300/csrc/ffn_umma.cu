@@ -10,7 +10,7 @@
 //     (sign-folded codebook entry x row scale, rounded once to fp16) and store
 //     them into shared memory in the 128-byte-swizzled K-major layout the
 //     tensor core reads (A operand, 128 rows x 64 per K-block); each thread
-//     fetches its codes three K-blocks ahead;
+//     fetches its codes and row scales (through L1) four K-blocks ahead;
 //   - a TMA warp loads the chunk's activations (B operand, 256 tokens x 64,
 //     fp16, same swizzle) with cp.async.bulk.tensor from a token-gathered
 //     copy in the workspace;
@@ -20,7 +20,9 @@
 //   - 4 epilogue warps read the accumulators back with tcgen05.ld (each warp
 //     owns one quarter of the TMEM lanes = weight rows) and store FC1's
 //     a = silu(g) * u in fp32 (a conversion kernel then makes the fp16 FC2 B
-//     operand), or FC2's y per pair / w*y into the token's output.
+//     operand), or FC2's y per pair / w*y into the token's output; per 32
+//     tokens the values are computed for all columns first (independent
+//     chains), then only the chunk's tokens are stored.
 // The two accumulators (2 x 256 columns) fill TMEM's 512 columns, so the
 // next item's MMAs start when the epilogue has read them (the decoders and
 // the TMA warp run ahead meanwhile).  Every wait is bounded: a wait that
@@ -204,9 +206,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             auto fetch = [&](int kb64, DecRegs& r) {
                 if (kb64 >= n_kblk) return;
                 const int kb = kb64 >> 1, half = kb64 & 1;
-                r.c = ldg_stream(codes + (size_t)kb * 512 + 16 * (16 * half + g));
-                r.s0 = ldg_stream(scales + (size_t)kb * 16);
-                r.s1 = ldg_stream(scales + (size_t)kb * 16 + 8);
+                // through L1: a scale row serves both K-block halves
+                r.c = __ldg(reinterpret_cast<const uint4*>(codes + (size_t)kb * 512 + 16 * (16 * half + g)));
+                r.s0 = __ldg(reinterpret_cast<const uint4*>(scales + (size_t)kb * 16));
+                r.s1 = __ldg(reinterpret_cast<const uint4*>(scales + (size_t)kb * 16 + 8));
             };
             auto step = [&](const DecRegs& r) {
                 const int stage = it % STAGES, use = it / STAGES;
@@ -318,43 +321,59 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+            // per 32 tokens: their scales (and FC2's pair weights) are loaded
+            // once, one per lane, and handed to the token loop by shuffles
 #pragma unroll 1
             for (int c0 = 0; c0 < UM_N; c0 += 32) {
                 if (c0 >= ch.count) break;
+                const int nt = min(32, ch.count - c0);  // (the same for every lane)
+                const int spos0 = ch.start + c0;
                 float v[32];
                 tmem_ld32(taddr + c0, v);
                 if (FC1) {
                     float u[32];
                     tmem_ld32(taddr + UM_N + c0, u);
-                    const int irow = rt * UM_M + row;
+                    const float sc_l = lane < nt ? xsc[spos0 + lane] : 0.0f;
+                    // written: the conversion takes these positions
+                    if (quarter == 0 && lane < nt) amax[spos0 + lane] = 1;
+                    float* dst = a32 + (size_t)spos0 * I + rt * UM_M + row;
+                    // all 32 columns computed (independent chains the
+                    // compiler interleaves), then only the chunk's tokens stored
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
-                        const int tok = c0 + q;
-                        if (tok < ch.count) {  // (the same for every lane)
-                            const int spos = ch.start + tok;
-                            const float sc = xsc[spos];
-                            const float gv = v[q] * sc, uv = u[q] * sc;
-                            a32[(size_t)spos * I + irow] = gv / (1.0f + expf(-gv)) * uv;
-                            if (lane == 0) amax[spos] = 1;  // written: the conversion takes this position
-                        }
+                        const float sc = __shfl_sync(0xffffffffu, sc_l, q);
+                        const float gv = v[q] * sc, uv = u[q] * sc;
+                        v[q] = silu_mul(gv, uv);
                     }
+#pragma unroll
+                    for (int q = 0; q < 32; ++q)
+                        if (q < nt) dst[(size_t)q * I] = v[q];
                 } else {
+                    const float sc_l = lane < nt ? asc[spos0 + lane] : 0.0f;
+                    int tok_l = 0;
+                    float w_l = 0.0f;
+                    if (mode != MOE_PER_PAIR && lane < nt) {
+                        const int p = sorted_pair[spos0 + lane];
+                        tok_l = p / k;
+                        w_l = weights[p];
+                    }
 #pragma unroll 1
                     for (int t = 0; t < 2; ++t) {
                         if (t == 1) tmem_ld32(taddr + UM_N + c0, v);
                         const int h = rt * 2 * UM_M + t * UM_M + row;
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) {
-                            const int tok = c0 + q;
-                            if (tok < ch.count) {
-                                const int spos = ch.start + tok;
-                                const float y = v[q] * asc[spos];
-                                if (mode == MOE_PER_PAIR) {
-                                    out[(size_t)spos * H + h] = y;
-                                } else {
-                                    const int p = sorted_pair[spos];
-                                    atomicAdd(out + (size_t)(p / k) * H + h, weights[p] * y);
-                                }
+                        for (int q = 0; q < 32; ++q) v[q] *= __shfl_sync(0xffffffffu, sc_l, q);
+                        if (mode == MOE_PER_PAIR) {
+                            float* dst = out + (size_t)spos0 * H + h;
+#pragma unroll
+                            for (int q = 0; q < 32; ++q)
+                                if (q < nt) dst[(size_t)q * H] = v[q];
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 32; ++q) {
+                                const int tok = __shfl_sync(0xffffffffu, tok_l, q);
+                                const float w = __shfl_sync(0xffffffffu, w_l, q);
+                                if (q < nt) atomicAdd(out + (size_t)tok * H + h, w * v[q]);
                             }
                         }
                     }
