@@ -38,6 +38,11 @@ namespace {
 constexpr int UM_M = 128, UM_N = UMMA_NT, UM_K = 64;
 constexpr int STAGES = 3;
 constexpr int DEC_WARPS = 8, EPI_WARPS = 4;
+constexpr int EPI_SLOTS = 1 + DEC_WARPS / 4;  // warps sharing one TMEM lane quarter's epilogue
+// registers per thread: each of the SM's four schedulers holds 16384
+// registers for its share of the CTA's warps (the busiest holds
+// ceil(warps / 4) of them)
+constexpr int MAX_REG = 16384 / (32 * ((DEC_WARPS + 2 + EPI_WARPS + 3) / 4)) / 8 * 8;
 constexpr int TMA_WARP = DEC_WARPS, MMA_WARP = DEC_WARPS + 1;  // then the epilogue warps
 constexpr int THREADS = 32 * (DEC_WARPS + 2 + EPI_WARPS);
 constexpr int A_BYTES = UM_M * UM_K * 2;      // 16 KB per A tile
@@ -79,19 +84,16 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
@@ -114,7 +116,7 @@ struct DecRegs {
 // sorted position); the epilogue multiplies the scale back in fp32.  FC1
 // writes a in fp32 (a32) and flags each sorted position it wrote (amax).
 template <bool FC1>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __maxnreg__(MAX_REG)
     ffn_umma_kernel(const __grid_constant__ CUtensorMap bmap, const SlotDesc* __restrict__ desc,
                     const uint16_t* __restrict__ codebook, const int32_t* __restrict__ sorted_pair,
                     const float* __restrict__ weights, int k, int H, int I, int* __restrict__ header,
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&S.empty[s]), 1);
         }
         mbar_init(smem_u32(&S.acc_full), 1);
-        mbar_init(smem_u32(&S.acc_empty), 32 * EPI_WARPS);
+        mbar_init(smem_u32(&S.acc_empty), 32 * (EPI_WARPS + DEC_WARPS));
         S.failed = 0;
     }
     if (warp == MMA_WARP) {  // allocate the accumulator columns (whole warp)
@@ -174,6 +176,74 @@ __global__ void __launch_bounds__(THREADS, 1)
         return true;
     };
 
+    // The epilogue of one item, shared by the three warps of each TMEM lane
+    // quarter (its epilogue warp, slot 0, and two decoder warps, slots 1 and
+    // 2, which are idle then: their next stages are filled and the MMA waits
+    // for the accumulators): 16-column chunks slot, slot + 3, ...  Per chunk
+    // the row scales (and FC2's pair weights) are loaded once, one per lane,
+    // and the values of all 16 columns computed before the guarded stores.
+    auto epi_share = [&](int item, int slot) {
+        const Chunk ch = uchunks[item / n_rt];
+        const int rt = item % n_rt;
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter.. are this warp's
+        const int row = quarter * 32 + lane;
+        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int n16 = (ch.count + 15) >> 4;
+#pragma unroll 1
+        for (int c16 = slot; c16 < n16; c16 += EPI_SLOTS) {
+            const int c0 = 16 * c16;
+            const int nt = min(16, ch.count - c0);  // (the same for every lane)
+            const int spos0 = ch.start + c0;
+            float v[16];
+            tmem_ld16(taddr + c0, v);
+            if (FC1) {
+                float u[16];
+                tmem_ld16(taddr + UM_N + c0, u);
+                const float sc_l = lane < nt ? xsc[spos0 + lane] : 0.0f;
+                // written: the conversion takes these positions
+                if (quarter == 0 && lane < nt) amax[spos0 + lane] = 1;
+                float* dst = a32 + (size_t)spos0 * I + rt * UM_M + row;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float sc = __shfl_sync(0xffffffffu, sc_l, q);
+                    v[q] = silu_mul(v[q] * sc, u[q] * sc);
+                }
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    if (q < nt) dst[(size_t)q * I] = v[q];
+            } else {
+                const float sc_l = lane < nt ? asc[spos0 + lane] : 0.0f;
+                int tok_l = 0;
+                float w_l = 0.0f;
+                if (mode != MOE_PER_PAIR && lane < nt) {
+                    const int p = sorted_pair[spos0 + lane];
+                    tok_l = p / k;
+                    w_l = weights[p];
+                }
+#pragma unroll 1
+                for (int t = 0; t < 2; ++t) {
+                    if (t == 1) tmem_ld16(taddr + UM_N + c0, v);
+                    const int h = rt * 2 * UM_M + t * UM_M + row;
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) v[q] *= __shfl_sync(0xffffffffu, sc_l, q);
+                    if (mode == MOE_PER_PAIR) {
+                        float* dst = out + (size_t)spos0 * H + h;
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            if (q < nt) dst[(size_t)q * H] = v[q];
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const int tok = __shfl_sync(0xffffffffu, tok_l, q);
+                            const float w = __shfl_sync(0xffffffffu, w_l, q);
+                            if (q < nt) atomicAdd(out + (size_t)tok * H + h, w * v[q]);
+                        }
+                    }
+                }
+            }
+        }
+    };
+
     if (warp < DEC_WARPS) {
         // ------------------------------------------------ decoders
         // 256 threads = (A tile) x 8 row tiles x 16 groups, one chunk each.
@@ -194,8 +264,23 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             return __shfl_sync(0xffffffffu, ok, 0) != 0;
         };
-        int it = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        // this warp's share of the previous item's epilogue: when the first
+        // STAGES K-blocks of the next item are submitted (or after the last
+        // item)
+        const int slot = 1 + warp / 4;
+        int prev = -1, nprev = 0;
+        auto dec_epi = [&]() {
+            if (prev < 0) return;
+            const int pi = prev;
+            prev = -1;
+            if (!warp_wait(&S.acc_full, nprev & 1, MOE_DEVERR_WAIT_FULL)) return;
+            tc_fence_after();
+            epi_share(pi, slot);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&S.acc_empty));
+        };
+        int it = 0, nitem = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++nitem) {
             const Chunk ch = uchunks[item / n_rt];
             const int rt = item % n_rt;
             const SlotDesc& d = desc[ch.expert];
@@ -211,7 +296,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 r.s0 = __ldg(reinterpret_cast<const uint4*>(scales + (size_t)kb * 16));
                 r.s1 = __ldg(reinterpret_cast<const uint4*>(scales + (size_t)kb * 16 + 8));
             };
-            auto step = [&](const DecRegs& r) {
+            auto step = [&](int kb64, const DecRegs& r) {
+                if (kb64 == STAGES) dec_epi();
                 const int stage = it % STAGES, use = it / STAGES;
                 ++it;
                 if (use > 0 && !warp_wait(&S.empty[stage], (use - 1) & 1, MOE_DEVERR_WAIT_EMPTY)) return;
@@ -248,22 +334,26 @@ __global__ void __launch_bounds__(THREADS, 1)
             fetch(2, r2);
             fetch(3, r3);
             for (int kb64 = 0; kb64 < n_kblk; kb64 += 4) {
-                step(r0);
+                step(kb64, r0);
                 fetch(kb64 + 4, r0);
                 if (kb64 + 1 < n_kblk) {
-                    step(r1);
+                    step(kb64 + 1, r1);
                     fetch(kb64 + 5, r1);
                 }
                 if (kb64 + 2 < n_kblk) {
-                    step(r2);
+                    step(kb64 + 2, r2);
                     fetch(kb64 + 6, r2);
                 }
                 if (kb64 + 3 < n_kblk) {
-                    step(r3);
+                    step(kb64 + 3, r3);
                     fetch(kb64 + 7, r3);
                 }
             }
+            dec_epi();  // (items of at most STAGES K-blocks)
+            prev = item;
+            nprev = nitem;
         }
+        dec_epi();
     } else if (warp == TMA_WARP) {
         // ------------------------------------------------ activations (B)
         if (lane == 0) {
@@ -309,76 +399,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ------------------------------------------------ epilogue
-        const int quarter = warp & 3;  // TMEM lanes 32*quarter.. are this warp's
-        const int row = quarter * 32 + lane;
         int nitem = 0;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++nitem) {
-            const Chunk ch = uchunks[item / n_rt];
-            const int rt = item % n_rt;
             int ok = 0;
             if (lane == 0) ok = wait(&S.acc_full, nitem & 1, MOE_DEVERR_WAIT_FULL) ? 1 : 0;
             __syncwarp();
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-            // per 32 tokens: their scales (and FC2's pair weights) are loaded
-            // once, one per lane, and handed to the token loop by shuffles
-#pragma unroll 1
-            for (int c0 = 0; c0 < UM_N; c0 += 32) {
-                if (c0 >= ch.count) break;
-                const int nt = min(32, ch.count - c0);  // (the same for every lane)
-                const int spos0 = ch.start + c0;
-                float v[32];
-                tmem_ld32(taddr + c0, v);
-                if (FC1) {
-                    float u[32];
-                    tmem_ld32(taddr + UM_N + c0, u);
-                    const float sc_l = lane < nt ? xsc[spos0 + lane] : 0.0f;
-                    // written: the conversion takes these positions
-                    if (quarter == 0 && lane < nt) amax[spos0 + lane] = 1;
-                    float* dst = a32 + (size_t)spos0 * I + rt * UM_M + row;
-                    // all 32 columns computed (independent chains the
-                    // compiler interleaves), then only the chunk's tokens stored
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const float sc = __shfl_sync(0xffffffffu, sc_l, q);
-                        const float gv = v[q] * sc, uv = u[q] * sc;
-                        v[q] = silu_mul(gv, uv);
-                    }
-#pragma unroll
-                    for (int q = 0; q < 32; ++q)
-                        if (q < nt) dst[(size_t)q * I] = v[q];
-                } else {
-                    const float sc_l = lane < nt ? asc[spos0 + lane] : 0.0f;
-                    int tok_l = 0;
-                    float w_l = 0.0f;
-                    if (mode != MOE_PER_PAIR && lane < nt) {
-                        const int p = sorted_pair[spos0 + lane];
-                        tok_l = p / k;
-                        w_l = weights[p];
-                    }
-#pragma unroll 1
-                    for (int t = 0; t < 2; ++t) {
-                        if (t == 1) tmem_ld32(taddr + UM_N + c0, v);
-                        const int h = rt * 2 * UM_M + t * UM_M + row;
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) v[q] *= __shfl_sync(0xffffffffu, sc_l, q);
-                        if (mode == MOE_PER_PAIR) {
-                            float* dst = out + (size_t)spos0 * H + h;
-#pragma unroll
-                            for (int q = 0; q < 32; ++q)
-                                if (q < nt) dst[(size_t)q * H] = v[q];
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < 32; ++q) {
-                                const int tok = __shfl_sync(0xffffffffu, tok_l, q);
-                                const float w = __shfl_sync(0xffffffffu, w_l, q);
-                                if (q < nt) atomicAdd(out + (size_t)tok * H + h, w * v[q]);
-                            }
-                        }
-                    }
-                }
-            }
+            epi_share(item, 0);
             tc_fence_before();
             mbar_arrive(smem_u32(&S.acc_empty));
         }
