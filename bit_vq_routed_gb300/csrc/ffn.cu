@@ -53,8 +53,10 @@ constexpr size_t SCHED_SMEM = sizeof(int) * (1025 + (MAX_TP + 1) + 4 * MAX_TP + 
 //     (one per token: the expert's codes are streamed once per token, which
 //     costs less than the mma.sync decode at such counts);
 //   VQ2 with m_e >= UMMA_MIN (and use_umma) -> ceil(m_e / UMMA_NT) tcgen05 chunks;
-//   otherwise -> mma.sync chunks of MMA_NT_VQ2 (VQ2) or MMA_NT_FP4 (FP4)
-//     tokens, the VQ2 chunks listed first.
+//   otherwise -> mma.sync chunks of MMA_NT_VQ2 (VQ2) or MMA_NT_FP4 (FP4,
+//     and with split16 VQ2 experts of at most MMA_NT_FP4 tokens) tokens; the
+//     chunks of the 32-token configuration are listed first (header
+//     HDR_NVQ2 of them), then those of the 16-token one.
 // Table pairs are listed sorted by (token, expert) and grouped by token, so
 // the experts of one token share each activation table.  pair_status of every
 // pair from the residency of its expert; the header's error word is cleared.
@@ -66,7 +68,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
                                                         Chunk* __restrict__ chunks, LutRec* __restrict__ recs,
                                                         int32_t* __restrict__ grp_start, int use_lut,
                                                         Chunk* __restrict__ uchunks, int use_umma, int H, int I,
-                                                        int C, int4* __restrict__ fc1_range) {
+                                                        int C, int4* __restrict__ fc1_range, int split16) {
     __shared__ unsigned long long warp_tot[33];
     extern __shared__ __align__(16) int sched_smem[];
     int* s_off = sched_smem;                       // [1025]
@@ -98,18 +100,19 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
     const int nl = lut ? m : 0;  // this expert's table pairs
     const bool um = res && use_umma && m >= UMMA_MIN && d.format == MOE_FMT_VQ2;
     const bool fp4 = d.format == MOE_FMT_FP4;
-    const int nt_e = fp4 ? MMA_NT_FP4 : MMA_NT_VQ2;  // tokens per mma.sync chunk of this expert
+    const bool part2 = fp4 || (split16 && m <= MMA_NT_FP4);  // the 16-token configuration
+    const int nt_e = part2 ? MMA_NT_FP4 : MMA_NT_VQ2;  // tokens per mma.sync chunk of this expert
     const int n = (res && !lut && !um) ? (m + nt_e - 1) / nt_e : 0;
     const int nu = um ? (m + UMMA_NT - 1) / UMMA_NT : 0;
     // one scan for the three counts (fields of 21 bits: n, nu, table pairs)
     unsigned long long tot;
     const unsigned long long ex =
-        block_scan64((unsigned long long)(fp4 ? 0 : n) | ((unsigned long long)nu << 21) | ((unsigned long long)nl << 42),
+        block_scan64((unsigned long long)(part2 ? 0 : n) | ((unsigned long long)nu << 21) | ((unsigned long long)nl << 42),
                      warp_tot, &tot);
-    unsigned long long tot4;  // the FP4 chunks, listed after the VQ2 ones
-    const unsigned long long ex4 = block_scan64(fp4 ? (unsigned long long)n : 0ull, warp_tot, &tot4);
+    unsigned long long tot4;  // the 16-token chunks, listed after the others
+    const unsigned long long ex4 = block_scan64(part2 ? (unsigned long long)n : 0ull, warp_tot, &tot4);
     const int n_vq2 = (int)(tot & 0x1fffff);
-    const int cbase = fp4 ? n_vq2 + (int)ex4 : (int)(ex & 0x1fffff), ubase = (int)((ex >> 21) & 0x1fffff);
+    const int cbase = part2 ? n_vq2 + (int)ex4 : (int)(ex & 0x1fffff), ubase = (int)((ex >> 21) & 0x1fffff);
     const int n_chunks = n_vq2 + (int)tot4, n_umma = (int)((tot >> 21) & 0x1fffff), n_lut = (int)(tot >> 42);
     for (int c = 0; c < n; ++c) {
         Chunk ch;
@@ -272,6 +275,7 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     // With one token no expert gets two pairs, so the mma.sync kernels only
     // have work if the table holds FP4 experts.
     const bool mma = T > 1 || t->n_fp4 > 0 || !use_lut;
+    const int split16 = T >= MMA_SPLIT_T ? 1 : 0;
 
     moe_status st;
     if (T == 1 && t->n_fp4 == 0) {
@@ -287,21 +291,21 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule shared memory");
     e = launch_pdl(schedule_kernel, dim3(1), dim3(1024), SCHED_SMEM, s, (const SlotDesc*)t->d_desc, E, offsets,
                                sorted_pair, P, k, status, header, chunks, recs, grp_start, use_lut,
-                               uchunks, use_umma, H, I, num_sms(), reinterpret_cast<int4*>(w + L.range_off));
+                               uchunks, use_umma, H, I, num_sms(), reinterpret_cast<int4*>(w + L.range_off), split16);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule launch");
     if ((mma || use_umma) && (st = launch_gather_f16(x, sorted_pair, k, H, P, w, L, s)) != MOE_OK) return st;
     if (use_lut &&
         (st = launch_lut_fc(true, false, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s)) !=
             MOE_OK)
         return st;
-    if (mma && (st = launch_mma_fc(true, t, sorted_pair, weights, k, mode, out, w, L, s)) != MOE_OK) return st;
+    if (mma && (st = launch_mma_fc(true, t, sorted_pair, weights, k, mode, out, w, L, s, split16)) != MOE_OK) return st;
     if (use_umma && (st = launch_umma(true, t, sorted_pair, weights, k, P, mode, out, w, L, s)) != MOE_OK) return st;
     if ((mma || use_umma) && (st = launch_a_to_f16(P, I, w, L, s)) != MOE_OK) return st;
     if (use_lut &&
         (st = launch_lut_fc(false, false, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s)) !=
             MOE_OK)
         return st;
-    if (mma && (st = launch_mma_fc(false, t, sorted_pair, weights, k, mode, out, w, L, s)) != MOE_OK) return st;
+    if (mma && (st = launch_mma_fc(false, t, sorted_pair, weights, k, mode, out, w, L, s, split16)) != MOE_OK) return st;
     if (use_umma && (st = launch_umma(false, t, sorted_pair, weights, k, P, mode, out, w, L, s)) != MOE_OK) return st;
     if (comb) return launch_combine(out, pair_to_sorted, weights, status, T, k, H, comb32, comb16, s);
     return MOE_OK;

@@ -10,6 +10,12 @@ namespace moe {
 
 constexpr int MMA_NT_VQ2 = 32; // tokens per mma.sync chunk of a VQ2 expert (four n8 MMA tiles)
 constexpr int MMA_NT_FP4 = 16; // tokens per mma.sync chunk of an FP4 expert (two n8 MMA tiles)
+// From this many tokens per call, VQ2 experts with at most MMA_NT_FP4 tokens
+// take the 16-token mma.sync configuration (two CTAs per SM) in a launch of
+// their own: with many such experts the extra launch pays (measured: prefill
+// of 4096 tokens 2.55 -> 2.34 ms per call), with few it does not (batch 32:
+// 256 -> 276 us).
+constexpr int MMA_SPLIT_T = 128;
 constexpr int LUT_KB = 8;      // scale blocks (x 128 inputs) per activation-table K-range
 constexpr int UMMA_MIN = 32;   // tokens from which an expert takes the tcgen05 path
 constexpr int UMMA_NT = 256;   // tokens per tcgen05 chunk
@@ -32,7 +38,8 @@ static_assert(sizeof(LutRec) == 64 && offsetof(LutRec, codes) == 0 && offsetof(L
               "table pair record layout");
 
 // Header words at the start of the workspace.
-// HDR_NVQ2: the chunks list holds the VQ2 chunks first, then the FP4 ones.
+// HDR_NVQ2: the chunks list holds the 32-token chunks first (HDR_NVQ2 of
+// them), then the 16-token ones (FP4, and small VQ2 experts in large calls).
 enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NUMMA = 4, HDR_NVQ2 = 5 };
 
 // Activation-table pairs (VQ2 experts with at most LUT_MAX_M tokens, one pair
@@ -144,5 +151,5 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(
 moe_status launch_umma(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
                        int P, int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s);
 moe_status launch_mma_fc(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
-                         int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s);
+                         int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s, bool split16);
 }  // namespace moe

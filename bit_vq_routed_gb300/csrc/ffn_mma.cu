@@ -18,7 +18,7 @@
 // tiles.  K is walked in slabs: the chunk's fp16 activations (gathered by
 // sorted position) and each warp's code and scale tiles for the next slab
 // stream into shared memory with cp.async while the current slab is computed.
-// Chunk size, slab length and CTAs per SM differ for VQ2 and FP4 (MmaCfg).
+// Chunk size, slab length and CTAs per SM come in two configurations (MmaCfg).
 #include "ffn_common.cuh"
 
 namespace moe {
@@ -28,10 +28,11 @@ constexpr int WARPS = 8;
 constexpr int THREADS = 32 * WARPS;
 constexpr int CB_COPIES = 16;
 
-// Two configurations.  VQ2 chunks: 32 tokens, 512-input slabs, one CTA per SM
-// (an expert's codes are read once per 32 tokens).  FP4 chunks (the most
-// routed experts, at small batches with few tokens each): 16 tokens, 256-input
-// slabs, two CTAs per SM, whose independent slab barriers hide more latency.
+// Two configurations.  32-token chunks (VQ2): 512-input slabs, one CTA per SM
+// (an expert's codes are read once per 32 tokens).  16-token chunks (FP4
+// experts, the most routed ones at small batches with few tokens each, and in
+// large calls the VQ2 experts with at most 16 tokens): 256-input slabs, two
+// CTAs per SM, whose independent slab barriers hide more latency.
 template <int NTOK_>
 struct MmaCfg {
     static constexpr int NTOK = NTOK_;                   // tokens per chunk
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_>::MIN_BLOCKS)
                    const float* __restrict__ weights, int k, int H, int I, const int* __restrict__ header,
                    const Chunk* __restrict__ chunks, const float* __restrict__ xsc, const float* __restrict__ asc,
                    float* __restrict__ a32, uint32_t* __restrict__ amax, float* __restrict__ out, int mode,
-                   int fp4_part) {
+                   int part16) {
     using Cfg = MmaCfg<NTOK_>;
     using Smem = typename Cfg::Smem;
     constexpr int NTOK = Cfg::NTOK, NNT = Cfg::NNT, SLAB = Cfg::SLAB, XSTRIDE = Cfg::XSTRIDE;
@@ -90,9 +91,9 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_>::MIN_BLOCKS)
 
     pdl_wait();
     pdl_launch_dependents();  // dependents may start their prologues now
-    // the chunks list holds the VQ2 chunks, then the FP4 ones: this launch's part
-    const int c0 = fp4_part ? header[HDR_NVQ2] : 0;
-    const int n_chunks = (fp4_part ? header[HDR_NCHUNKS] : header[HDR_NVQ2]) - c0;
+    // the chunks list holds the 32-token chunks, then the 16-token ones: this launch's part
+    const int c0 = part16 ? header[HDR_NVQ2] : 0;
+    const int n_chunks = (part16 ? header[HDR_NCHUNKS] : header[HDR_NVQ2]) - c0;
     const int n_items = n_chunks * n_rg;
     if ((int)blockIdx.x >= n_items) return;
     for (int idx = tid; idx < 256 * CB_COPIES; idx += THREADS) {
@@ -334,9 +335,9 @@ static moe_status launch_mma_cfg(bool fc1, const SlotTableHost* t, const int32_t
 }
 
 moe_status launch_mma_fc(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
-                         int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s) {
+                         int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s, bool split16) {
     moe_status st = launch_mma_cfg<MMA_NT_VQ2>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s);
-    if (st == MOE_OK && t->n_fp4 > 0)
+    if (st == MOE_OK && (t->n_fp4 > 0 || split16))
         st = launch_mma_cfg<MMA_NT_FP4>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s);
     return st;
 }

@@ -49,3 +49,25 @@ def test_tensor_core_fused_scatter(torch):
     torch.cuda.synchronize()
     assert np.abs(out.cpu().numpy() - g["out"]).max() <= 1e-5 * np.abs(g["out"]).max()
     assert device_error_word(dev) == 0
+
+
+def test_every_path_in_one_large_call(torch):
+    """A call of 160 tokens (at least the split threshold of 128) whose routing
+    gives VQ2 experts in every band: 1-3 tokens (activation table), 4-16
+    (16-token mma.sync configuration), 17-31 (32-token configuration) and
+    32 or more (tcgen05), and an FP4 expert (16-token configuration, in the
+    same launch as the small VQ2 experts)."""
+    spec = ms.LayerSpec(H=512, I=256, E=48, k=4, seed=91, zipf_s=1.1, fp4_top=1)
+    layer = ms.Layer(spec)
+    x = ms.tokens(160, 512, seed=91)
+    dev, keep = device_layer(layer, 160)
+    g = run(dev, x)
+    r = O.moe_layer(layer, x)
+    assert_routing_exact(g, r)
+    counts = np.diff(g["offsets"])
+    vq = layer.formats == ms.FMT_VQ2
+    for lo, hi in [(1, 3), (4, 16), (17, 31), (32, 160)]:
+        assert ((counts >= lo) & (counts <= hi) & vq).any(), (lo, hi)
+    assert (counts[~vq] > 0).any()
+    assert_close(g["out"], r["out"], "every path, 160 tokens")
+    assert device_error_word(dev) == 0
