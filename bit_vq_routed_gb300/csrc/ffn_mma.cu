@@ -8,9 +8,11 @@
 // half-warps of an 8-byte lookup hit distinct banks; the entry's 4 fp16
 // values are exactly one thread's A-fragment for one row: the K order inside
 // each 16-wide MMA step is permuted so a thread's 4 k-slots are one code's 4
-// inputs, and the activations use the same permutation.  The row scale is
-// applied in fp32 once per 128-input block.  FP4 (e2m1) bytes become f16x2
-// with cvt and are scaled per 32 inputs.
+// inputs, and the activations use the same permutation.  The entry is
+// multiplied by its row scale in fp16 (the weight rounded once, as the
+// tcgen05 decoders do), which keeps one set of fp32 accumulators (two CTAs
+// fit per SM).  FP4 (e2m1) bytes become f16x2 with cvt and are scaled per 32
+// inputs.
 //
 // A CTA of 8 warps takes items (chunk of tokens of one expert, 8 x 32 weight
 // rows); each warp owns two 16-row tiles (FC1: the gate and the up tile of the
@@ -18,7 +20,7 @@
 // tiles.  K is walked in slabs: the chunk's fp16 activations (gathered by
 // sorted position) and each warp's code and scale tiles for the next slab
 // stream into shared memory with cp.async while the current slab is computed.
-// Chunk size, slab length and CTAs per SM come in two configurations (MmaCfg).
+// Chunk size, slab length and CTAs per SM come in three configurations (MmaCfg).
 #include "ffn_common.cuh"
 
 namespace moe {
@@ -28,21 +30,24 @@ constexpr int WARPS = 8;
 constexpr int THREADS = 32 * WARPS;
 constexpr int CB_COPIES = 16;
 
-// Two configurations.  32-token chunks (VQ2): 512-input slabs, one CTA per SM
-// (an expert's codes are read once per 32 tokens).  16-token chunks (FP4
-// experts, the most routed ones at small batches with few tokens each, and in
-// large calls the VQ2 experts with at most 16 tokens): 256-input slabs, two
-// CTAs per SM, whose independent slab barriers hide more latency.
-template <int NTOK_>
+// Configurations.  32-token chunks (VQ2; an expert's codes are read once per
+// 32 tokens): in calls of at least MMA_SPLIT_T tokens ("wide") 512-input
+// slabs and one CTA per SM, below that 256-input slabs and two CTAs per SM
+// (measured: batch 32 255 -> 239 us per call with two; prefill of 4096
+// tokens 2.33 -> 2.56 ms).  16-token chunks (FP4 experts, the most routed ones
+// at small batches with few tokens each, and in large calls the VQ2 experts
+// with at most 16 tokens): 256-input slabs, two CTAs per SM, whose independent
+// slab barriers hide more latency.
+template <int NTOK_, bool WIDE_>
 struct MmaCfg {
     static constexpr int NTOK = NTOK_;                   // tokens per chunk
     static constexpr int NNT = NTOK / 8;                 // n8 MMA tiles per chunk
-    static constexpr int SLAB = NTOK == 32 ? 512 : 256;  // inputs per slab (VQ2; FP4 slabs are half as many)
+    static constexpr int SLAB = WIDE_ ? 512 : 256;       // inputs per slab (VQ2; FP4 slabs are half as many)
     static constexpr int XSTRIDE = 2 * SLAB + 32;        // bytes per token row of a slab (padding: B-fragment banks)
     static constexpr int TILE_CODES = 4 * SLAB;          // one 16-row tile x one slab
     static constexpr int TILE_SCALES = SLAB / 4;         // 16 rows x SLAB/128 fp16 (VQ2) or x SLAB/64 ue8m0 (FP4)
     static constexpr int WARP_BYTES = 2 * (TILE_CODES + TILE_SCALES);  // per warp per slab (two tiles)
-    static constexpr int MIN_BLOCKS = NTOK == 32 ? 1 : 2;
+    static constexpr int MIN_BLOCKS = WIDE_ ? 1 : 2;
     struct __align__(16) Smem {
         uint2 cbt[256 * CB_COPIES];
         uint8_t xs[2][NTOK * XSTRIDE];
@@ -62,21 +67,25 @@ __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_g
 __device__ __forceinline__ uint32_t sh_u16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
 __device__ __forceinline__ uint2 sh_u64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
 __device__ __forceinline__ uint32_t sh_u32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
 
 // FC1 = true: A tiles are the gate and up tiles of 16 I-rows, B = x16s (K = H);
 // FC1 = false: A tiles are two down tiles (32 H-rows), B = a16 (K = I).
 // The B rows are scaled by powers of two (x16s = x / xsc, a16 = a / asc, per
 // sorted position); the epilogues multiply the scale back in fp32.  FC1
 // writes a in fp32 (a32) and flags each sorted position it wrote (amax).
-template <bool FC1, int NTOK_>
-__global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_>::MIN_BLOCKS)
+template <bool FC1, int NTOK_, bool WIDE_>
+__global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_, WIDE_>::MIN_BLOCKS)
     ffn_mma_kernel(const SlotDesc* __restrict__ desc, const uint16_t* __restrict__ codebook,
                    const uint16_t* __restrict__ bsrc, const int32_t* __restrict__ sorted_pair,
                    const float* __restrict__ weights, int k, int H, int I, const int* __restrict__ header,
                    const Chunk* __restrict__ chunks, const float* __restrict__ xsc, const float* __restrict__ asc,
                    float* __restrict__ a32, uint32_t* __restrict__ amax, float* __restrict__ out, int mode,
                    int part16) {
-    using Cfg = MmaCfg<NTOK_>;
+    using Cfg = MmaCfg<NTOK_, WIDE_>;
     using Smem = typename Cfg::Smem;
     constexpr int NTOK = Cfg::NTOK, NNT = Cfg::NNT, SLAB = Cfg::SLAB, XSTRIDE = Cfg::XSTRIDE;
     constexpr int TILE_CODES = Cfg::TILE_CODES, TILE_SCALES = Cfg::TILE_SCALES;
@@ -182,13 +191,14 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_>::MIN_BLOCKS)
             const uint8_t* wb = &S.w[buf][warp][0];
             if (vq2) {
                 for (int kb = 0; kb < kn / 128; ++kb) {
-                    float tmp[2][NNT][4];
+                    // the rows' fp16 scales (rows i and i + 8 of each tile) in both halves
+                    uint32_t sl2[2], sh2[2];
 #pragma unroll
-                    for (int t = 0; t < 2; ++t)
-#pragma unroll
-                        for (int nt = 0; nt < NNT; ++nt)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) tmp[t][nt][q] = 0.0f;
+                    for (int t = 0; t < 2; ++t) {
+                        const uint8_t* sa = wb + 2 * TILE_CODES + t * TILE_SCALES + kb * 32;
+                        sl2[t] = sh_u16(sa + 2 * i) * 0x10001u;
+                        sh2[t] = sh_u16(sa + 2 * (i + 8)) * 0x10001u;
+                    }
 #pragma unroll
                     for (int s = 0; s < 8; ++s) {
                         const int g = 4 * s + j;  // this thread's group in the scale block
@@ -201,26 +211,15 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_>::MIN_BLOCKS)
                             const uint32_t pr = sh_u16(wb + t * TILE_CODES + kb * 512 + 16 * g + 2 * i);
                             const uint2 lo = sh_u64(cbt + 128u * (pr & 0xffu));
                             const uint2 hi = sh_u64(cbt + 128u * (pr >> 8));
+                            const uint32_t a0 = hmul2_u32(lo.x, sl2[t]), a1 = hmul2_u32(hi.x, sh2[t]);
+                            const uint32_t a2 = hmul2_u32(lo.y, sl2[t]), a3 = hmul2_u32(hi.y, sh2[t]);
 #pragma unroll
                             for (int nt = 0; nt < NNT; ++nt)
-                                if (nt < n_nt) mma_16816(tmp[t][nt], lo.x, hi.x, lo.y, hi.y, b[nt].x, b[nt].y);
-                        }
-                    }
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        const uint8_t* sa = wb + 2 * TILE_CODES + t * TILE_SCALES + kb * 32;
-                        const float s_lo = __half2float(__ushort_as_half((unsigned short)sh_u16(sa + 2 * i)));
-                        const float s_hi = __half2float(__ushort_as_half((unsigned short)sh_u16(sa + 2 * (i + 8))));
-#pragma unroll
-                        for (int nt = 0; nt < NNT; ++nt) {
-                            acc[t][nt][0] = fmaf(s_lo, tmp[t][nt][0], acc[t][nt][0]);
-                            acc[t][nt][1] = fmaf(s_lo, tmp[t][nt][1], acc[t][nt][1]);
-                            acc[t][nt][2] = fmaf(s_hi, tmp[t][nt][2], acc[t][nt][2]);
-                            acc[t][nt][3] = fmaf(s_hi, tmp[t][nt][3], acc[t][nt][3]);
+                                if (nt < n_nt) mma_16816(acc[t][nt], a0, a1, a2, a3, b[nt].x, b[nt].y);
                         }
                     }
                 }
-            } else {
+            } else if constexpr (NTOK == MMA_NT_FP4) {
                 for (int kt = 0; kt < kn / 64; ++kt) {
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {  // 32-element scale blocks
@@ -314,18 +313,18 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_>::MIN_BLOCKS)
 }  // namespace
 
 
-template <int NTOK_>
+template <int NTOK_, bool WIDE_>
 static moe_status launch_mma_cfg(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights,
                                  int k, int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s) {
-    using Smem = typename MmaCfg<NTOK_>::Smem;
+    using Smem = typename MmaCfg<NTOK_, WIDE_>::Smem;
     const int* header = reinterpret_cast<const int*>(ws);
     const Chunk* chunks = reinterpret_cast<const Chunk*>(ws + L.chunks_off);
     const uint16_t* x16s = reinterpret_cast<const uint16_t*>(ws + L.x16s_off);
     const uint16_t* a16 = reinterpret_cast<const uint16_t*>(ws + L.a16_off);
-    auto kern = fc1 ? ffn_mma_kernel<true, NTOK_> : ffn_mma_kernel<false, NTOK_>;
+    auto kern = fc1 ? ffn_mma_kernel<true, NTOK_, WIDE_> : ffn_mma_kernel<false, NTOK_, WIDE_>;
     cudaError_t e = ensure_smem_attr(kern, (int)sizeof(Smem));
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: mma kernel shared memory");
-    e = launch_pdl(kern, dim3((unsigned)(MmaCfg<NTOK_>::MIN_BLOCKS * num_sms())), dim3(THREADS), sizeof(Smem), s,
+    e = launch_pdl(kern, dim3((unsigned)(MmaCfg<NTOK_, WIDE_>::MIN_BLOCKS * num_sms())), dim3(THREADS), sizeof(Smem), s,
                    (const SlotDesc*)t->d_desc, t->codebook, fc1 ? x16s : a16, sorted_pair, weights, k, t->H, t->I,
                    header, chunks, reinterpret_cast<const float*>(ws + L.xsc_off),
                    reinterpret_cast<const float*>(ws + L.asc_off), reinterpret_cast<float*>(ws + L.a32_off),
@@ -336,9 +335,11 @@ static moe_status launch_mma_cfg(bool fc1, const SlotTableHost* t, const int32_t
 
 moe_status launch_mma_fc(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
                          int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s, bool split16) {
-    moe_status st = launch_mma_cfg<MMA_NT_VQ2>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s);
+    // (split16 is set exactly for the calls of at least MMA_SPLIT_T tokens)
+    moe_status st = split16 ? launch_mma_cfg<MMA_NT_VQ2, true>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s)
+                            : launch_mma_cfg<MMA_NT_VQ2, false>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s);
     if (st == MOE_OK && (t->n_fp4 > 0 || split16))
-        st = launch_mma_cfg<MMA_NT_FP4>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s);
+        st = launch_mma_cfg<MMA_NT_FP4, false>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s);
     return st;
 }
 
