@@ -271,7 +271,11 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     int32_t* grp_start = reinterpret_cast<int32_t*>(w + L.grp_start_off);
     Chunk* uchunks = reinterpret_cast<Chunk*>(w + L.uchunks_off);
     const int use_lut = 1;
-    const int use_umma = T >= UMMA_MIN ? 1 : 0;  // an expert gets at most T of the pairs
+    // An expert gets at most T of the pairs: at T == UMMA_MIN only an expert
+    // routed by every token would qualify, and the 32-token mma.sync chunk
+    // serves it as well, so the tcgen05 launches start above that (at
+    // batch 32 they found work in one batch of eight and cost two launches).
+    const int use_umma = T > UMMA_MIN ? 1 : 0;
     // With one token no expert gets two pairs, so the mma.sync kernels only
     // have work if the table holds FP4 experts.
     const bool mma = T > 1 || t->n_fp4 > 0 || !use_lut;

@@ -17,7 +17,7 @@ constexpr int MMA_NT_FP4 = 16; // tokens per mma.sync chunk of an FP4 expert (tw
 // 256 -> 276 us).
 constexpr int MMA_SPLIT_T = 128;
 constexpr int LUT_KB = 8;      // scale blocks (x 128 inputs) per activation-table K-range
-constexpr int UMMA_MIN = 32;   // tokens from which an expert takes the tcgen05 path
+constexpr int UMMA_MIN = 32;   // tokens from which an expert takes the tcgen05 path (calls of more than UMMA_MIN tokens)
 constexpr int UMMA_NT = 256;   // tokens per tcgen05 chunk
 constexpr int MAX_LUT_CTAS = 1024;  // grid of the activation-table kernels (one CTA per SM) at most
 constexpr int LUT_MAX_M = 3;   // VQ2 experts with up to this many tokens take the activation-table path
