@@ -392,14 +392,14 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __rest
 #pragma unroll
     for (int u = 0; u < U; ++u)
         if (u < per) wv[u] = __ldg(wr + lane + 32 * u);
-    // the activations are complete at launch (no library kernel still running
-    // writes them), so they are read before the wait too
+    // The activations are complete at launch (no library kernel still running
+    // writes them), so the logits are computed before the wait too: only the
+    // global writes wait for the kernels before this one.
     for (int i = tid; i < nch; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(x + (size_t)t * H)[i];
-    pdl_wait();
     pdl_launch_dependents();  // dependents may start their prologues now
     __syncthreads();
+    float acc = 0.0f;
     if (e < E) {
-        float acc = 0.0f;
         for (int m0 = 0; m0 < per; m0 += U) {
             if (m0 > 0) {
 #pragma unroll
@@ -419,8 +419,9 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __rest
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(FULL, acc, off));
-        if (lane == 0) logits[(size_t)t * E + e] = bias ? __fadd_rn(acc, bias[e]) : acc;
     }
+    pdl_wait();
+    if (e < E && lane == 0) logits[(size_t)t * E + e] = bias ? __fadd_rn(acc, bias[e]) : acc;
     // the last CTA to finish goes on (thread 0's fence, after the barrier,
     // orders the whole CTA's logits before its arrival)
     __syncthreads();
@@ -630,10 +631,11 @@ __global__ void __launch_bounds__(32 * RC_WARPS) route_cluster_kernel(const uint
             if (m0 + u < per) wv[u] = __ldg(wr + lane + 32 * (m0 + u));
     };
     load_w(e, 0);
-    // the activations are complete at launch (no library kernel still running
-    // writes them), so they are read before the wait too
+    // The activations are complete at launch (no library kernel still running
+    // writes them), so the logits are computed and gathered in CTA 0's shared
+    // memory before the wait: only the global writes (CTA 0's, after the
+    // cluster barrier) wait for the kernels before this one.
     for (int i = tid; i < nch; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(x)[i];
-    pdl_wait();
     pdl_launch_dependents();  // dependents may start their prologues now
     __syncthreads();
     for (; e < E; e += stride) {
@@ -653,15 +655,13 @@ __global__ void __launch_bounds__(32 * RC_WARPS) route_cluster_kernel(const uint
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(FULL, acc, off));
-        if (lane == 0) {
-            const float v = bias ? __fadd_rn(acc, bias[e]) : acc;
-            logits[e] = v;
-            st_cta0_f32((uint32_t)__cvta_generic_to_shared(&lg[e]), v);
-        }
+        if (lane == 0) st_cta0_f32((uint32_t)__cvta_generic_to_shared(&lg[e]), bias ? __fadd_rn(acc, bias[e]) : acc);
         if (e + stride < E) load_w(e + stride, 0);
     }
     cluster_barrier();  // every CTA's logits are in CTA 0's shared memory
     if (cluster_rank() != 0 || warp != 0) return;
+    pdl_wait();
+    for (int i = lane; i < E; i += 32) logits[i] = lg[i];
     route_one_token<NPER>([&](int ee) { return lg[ee]; }, E, k, renorm, ids, weights, offsets, sorted_pair,
                           pair_to_sorted);
 }
