@@ -332,6 +332,12 @@ moe_status moe_expert_cache_fetch(moe_expert_cache* c, const int32_t* experts, i
         for (size_t j = failed_at + 1; j < req.size(); ++j)
             if (fill[j] >= 0) c->slot_expert[fill[j]] = ev[j];
     }
+    // the outputs as far as the call got, on the error returns too
+    auto outputs = [&]() {
+        if (n_fetched) *n_fetched = fetched;
+        if (n_unplaced) *n_unplaced = left;
+        if (recapture) *recapture = had_fp4 != (t.n_fp4 > 0);
+    };
     for (size_t u0 = 0; u0 < upd.size(); u0 += SLOT_BATCH) {
         SlotBatch b;
         b.n = (int)std::min(upd.size() - u0, (size_t)SLOT_BATCH);
@@ -339,7 +345,10 @@ moe_status moe_expert_cache_fetch(moe_expert_cache* c, const int32_t* experts, i
             b.ids[j] = upd[u0 + j].id;
             b.d[j] = upd[u0 + j].d;
         }
-        if ((st = launch_slot_set_many(t.d_desc, b, stream)) != MOE_OK) return st;
+        if ((st = launch_slot_set_many(t.d_desc, b, stream)) != MOE_OK) {
+            outputs();
+            return st;
+        }
         for (int j = 0; j < b.n; ++j) {  // the host mirror of the table, as set / evict keep it
             const int id = b.ids[j];
             const int f = b.d[j].resident ? 1 + b.d[j].format : 0;
@@ -349,11 +358,12 @@ moe_status moe_expert_cache_fetch(moe_expert_cache* c, const int32_t* experts, i
     }
     c->misses += (uint64_t)fetched;
     c->bytes += nbytes;
-    if (failed_at < req.size()) return cuda_status(copy_err, "moe_expert_cache_fetch: cudaMemcpyAsync");
+    if (failed_at < req.size()) {
+        outputs();
+        return cuda_status(copy_err, "moe_expert_cache_fetch: cudaMemcpyAsync");
+    }
     c->unplaced += (uint64_t)left;
-    if (n_fetched) *n_fetched = fetched;
-    if (n_unplaced) *n_unplaced = left;
-    if (recapture) *recapture = had_fp4 != (t.n_fp4 > 0);
+    outputs();
     return MOE_OK;
 }
 

@@ -211,7 +211,9 @@ moe_status moe_expert_cache_set_host_image(moe_expert_cache* c, int expert_id, i
  * passes run on the same stream).  An expert already set in the table by
  * the caller is left as it is.  Every named expert must have a host copy,
  * else nothing is enqueued (MOE_ERR_INVALID_ARG).  After MOE_ERR_CUDA the
- * cache and the table may disagree: destroy both.
+ * cache and the table may disagree (a slot may already hold the copy of an
+ * expert whose entry was not written): destroy both.  The outputs are
+ * written on that error too, counting what the call had done.
  * Outputs (each may be NULL): n_fetched = experts copied in, n_unplaced =
  * named experts left non-resident for lack of a slot, recapture = 1 if the
  * call changed whether the table holds any FP4 expert (the expert-FFN call
