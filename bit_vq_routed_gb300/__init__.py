@@ -592,5 +592,5 @@ def moe_vq2_encode(W: torch.Tensor, codebook: torch.Tensor, iters: int = 3, stre
     return codes, scales
 
 
-from .layer import (GatedForward, GraphedForward, GraphedStep, MissFetchForward, MoELayer,  # noqa: E402,F401
+from .layer import (GatedForward, GraphedForward, GraphedStep, MissFetchForward, MoELayer, PipelinedSteps,  # noqa: E402,F401
                     TandemForward, host_expert, host_expert_image, upload_layer, upload_expert)

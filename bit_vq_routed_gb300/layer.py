@@ -185,6 +185,79 @@ class GraphedStep:
         self.graph.replay()
 
 
+class PipelinedSteps:
+    """Steps over several layers with the host copies overlapping the layers
+    of the neighbouring steps: the layers run as one CUDA graph per device
+    buffer pair (tokens bf16 [L, T, H], outputs fp32 [L, T, H], two pairs),
+    a step's tokens are copied in from page-locked host memory on one stream
+    and its outputs copied out on another, ordered by events.
+
+    ``step(host_in, host_out)`` enqueues one step: the copy of ``host_in``
+    (pinned bf16 [L, T, H]) into the free buffer, the layers on the current
+    stream once that copy is done, and the copy of the outputs into
+    ``host_out`` (pinned fp32 [L, T, H]) once they are done.  The copy of
+    step s + 1 in runs while step s computes, and the copy of step s out
+    while step s + 1 computes.  ``join()`` makes the current stream wait for
+    every enqueued copy; synchronise it before reading ``host_out``.  The
+    host buffers of a step must stay unchanged until its copies are done."""
+
+    def __init__(self, layers: Sequence[MoELayer], T: int, device="cuda"):
+        self.layers = list(layers)
+        L, H = len(self.layers), self.layers[0].H
+        self.x = [torch.zeros(L, T, H, dtype=torch.bfloat16, device=device) for _ in range(2)]
+        self.out = [torch.empty(L, T, H, dtype=torch.float32, device=device) for _ in range(2)]
+        self.copy_in = torch.cuda.Stream(device=device)
+        self.copy_out = torch.cuda.Stream(device=device)
+        # per buffer: tokens copied in, layers done, outputs copied out
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_done = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+        self.used = [False, False]
+        self.n = 0
+        self._run(0)  # first eager call: kernel attributes are set outside capture
+        torch.cuda.synchronize()
+        self.graphs = []
+        for b in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._run(b)
+            self.graphs.append(g)
+
+    def _run(self, b: int):
+        for i, layer in enumerate(self.layers):
+            layer.forward(self.x[b][i], out=self.out[b][i])
+
+    def step(self, host_in: torch.Tensor, host_out: torch.Tensor):
+        b = self.n & 1
+        cur = torch.cuda.current_stream()
+        if self.n == 0:  # the copies start after the work enqueued before the first step
+            self.ev_first = torch.cuda.Event()
+            self.ev_first.record(cur)
+        self.n += 1
+        if self.used[b]:  # the buffer's previous step is done with its tokens
+            self.copy_in.wait_event(self.ev_done[b])
+        else:
+            self.copy_in.wait_event(self.ev_first)
+        with torch.cuda.stream(self.copy_in):
+            self.x[b].copy_(host_in, non_blocking=True)
+            self.ev_in[b].record(self.copy_in)
+        cur.wait_event(self.ev_in[b])
+        if self.used[b]:  # and the outputs of its previous step are copied out
+            cur.wait_event(self.ev_out[b])
+        self.graphs[b].replay()
+        self.ev_done[b].record(cur)
+        self.copy_out.wait_event(self.ev_done[b])
+        with torch.cuda.stream(self.copy_out):
+            host_out.copy_(self.out[b], non_blocking=True)
+            self.ev_out[b].record(self.copy_out)
+        self.used[b] = True
+
+    def join(self):
+        cur = torch.cuda.current_stream()
+        cur.wait_stream(self.copy_in)
+        cur.wait_stream(self.copy_out)
+
+
 def host_expert(fmt: int, codes: Sequence, scales: Sequence, stream=None, device="cuda"):
     """Packs one expert on the device (upload_expert) and returns page-locked
     host copies of the packed buffers (codes[3], scales[3]): the host-resident

@@ -34,3 +34,27 @@ def test_graphed_step_matches_eager_layers(torch, T):
             assert np.array_equal(host_out[L].numpy().view(np.uint32), ref.view(np.uint32)), (b, L)
     with pytest.raises(ValueError):
         bv.GraphedStep(devs, torch.zeros(3, T, 512, dtype=torch.bfloat16), host_out)
+
+
+@pytest.mark.parametrize("T", [1, 5])
+def test_pipelined_steps_match_eager_layers(torch, T):
+    """PipelinedSteps: the copies of a step overlap the neighbouring steps'
+    layers (two copy streams, double-buffered device tokens and outputs); every
+    step's outputs still equal the eager forward's bit for bit."""
+    import bit_vq_routed_gb300 as bv
+    specs = [ms.LayerSpec(H=512, I=256, E=16, k=4, seed=70 + L, layer=L) for L in range(3)]
+    layers = [ms.Layer(s) for s in specs]
+    devs, keeps = zip(*[device_layer(layer, T) for layer in layers])
+    n = 5
+    toks = [np.stack([ms.tokens(T, 512, seed=90 + b, layer=L) for L in range(3)]) for b in range(n)]
+    host_in = [torch.from_numpy(t).view(torch.bfloat16).pin_memory() for t in toks]
+    host_out = [torch.zeros(3, T, 512, dtype=torch.float32).pin_memory() for _ in range(n)]
+    pipe = bv.PipelinedSteps(devs, T)
+    for b in range(n):  # enqueued back to back, one synchronisation at the end
+        pipe.step(host_in[b], host_out[b])
+    pipe.join()
+    torch.cuda.synchronize()
+    for b in range(n):
+        for L, dev in enumerate(devs):
+            ref = dev.forward(torch.from_numpy(toks[b][L]).view(torch.bfloat16).cuda()).cpu().numpy()
+            assert np.array_equal(host_out[b][L].numpy().view(np.uint32), ref.view(np.uint32)), (b, L)
