@@ -53,7 +53,7 @@ L2_BYTES = 129 * 2 ** 20
 TRAFFIC = {"decode_b1": {"bytes": 54_267_392,
                          "profile": "ncu capture of ffn_lut_kernel<1,1> and ffn_lut_kernel<0,1>, decode batch 1",
                          "sources": ["ffn_lut.cu", "lut_core.cuh", "ffn_common.cuh", "common.cuh"],
-                         "sha256": "d8b1f60e546c42c2fd6d61f0ea13c87e9dedb927e62155143f0c6ed3be0e99fc"}}
+                         "sha256": "a647cbed88054ba61af381c753247846f118872b62283f18c84e3156c1a99d26"}}
 
 
 def measured_traffic(name):
