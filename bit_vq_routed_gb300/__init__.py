@@ -54,7 +54,7 @@ EXPORTED = [
     "moe_route_topk", "moe_permute_workspace_size", "moe_permute",
     "moe_vq2_expert_ffn_workspace_size", "moe_vq2_expert_ffn", "moe_vq2_expert_ffn_noalloc", "moe_combine",
     "moe_launch_count", "moe_route_workspace_size", "moe_route", "moe_vq2_expert_ffn_combine",
-    "moe_selftest", "moe_expert_cache_slot_bytes", "moe_expert_cache_create", "moe_expert_cache_set_host",
+    "moe_selftest", "moe_selftest_wait_timeout", "moe_expert_cache_slot_bytes", "moe_expert_cache_create", "moe_expert_cache_set_host",
     "moe_expert_cache_fetch", "moe_expert_cache_slot_of", "moe_expert_cache_stats", "moe_expert_cache_plan",
     "moe_expert_cache_destroy", "moe_expert_cache_set_host_image", "moe_cpu_pool_create", "moe_cpu_pool_threads",
     "moe_cpu_pool_destroy", "moe_cpu_expert_ffn", "moe_accumulate", "moe_slot_table_resident", "moe_vq2_pack_host",
@@ -97,6 +97,7 @@ def load(path: Optional[str] = None, build_if_stale: bool = True):
         "moe_route": ([P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, Z, P], I),
         "moe_vq2_expert_ffn_combine": ([P, P, P, P, P, P, I, I, P, P, P, P, P, Z, P], I),
         "moe_selftest": ([P], I),
+        "moe_selftest_wait_timeout": ([P, P], I),
         "moe_expert_cache_slot_bytes": ([I, I, I], Z),
         "moe_expert_cache_create": ([P, P, Z, Z, ctypes.POINTER(P)], I),
         "moe_expert_cache_set_host": ([P, I, ctypes.POINTER(_ExpertDesc)], I),
@@ -282,6 +283,15 @@ def moe_selftest(stream=None) -> None:
     results.  Synchronises the stream; raises MoeError (status
     MOE_ERR_MISMATCH for a wrong result) on failure."""
     _check(load().moe_selftest(_stream(stream)))
+
+
+def moe_selftest_wait_timeout(stream=None) -> dict:
+    """Self-check of the kernels' bounded-wait pattern: two waits on mbarriers
+    that nothing completes give up, record their codes and return.  Raises
+    MoeError if they do not; returns the codes and each wait's microseconds."""
+    codes = (ctypes.c_int * 6)()
+    _check(load().moe_selftest_wait_timeout(codes, _stream(stream)))
+    return dict(codes=(codes[0], codes[1]), gave_up=(codes[2] == 0, codes[3] == 0), us=(codes[4], codes[5]))
 
 
 def moe_route_workspace_size(T: int, k: int, E: int) -> int:

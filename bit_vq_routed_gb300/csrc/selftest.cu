@@ -402,10 +402,77 @@ moe_status run_cases(moe_slot_table* vq2, moe_slot_table* mixed, const Buffers& 
     return MOE_OK;
 }
 
+// The bounded-wait pattern of the kernels (a limited loop over
+// mbarrier.try_wait, then an error code and a return), on mbarriers that
+// nothing completes, with both wait primitives the kernels use: plain
+// try_wait and try_wait with a 1 us suspend hint.  Short limits (64 and 256
+// tries), so the check ends in well under a second whatever the hardware's
+// suspend time; the time each wait took (globaltimer, ns) is reported.
+__device__ __forceinline__ uint64_t gtimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__global__ void wait_timeout_kernel(int* codes, unsigned long long* ns) {
+    __shared__ uint64_t bars[2];
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_u32(&bars[0]), 1);
+    mbar_init(smem_u32(&bars[1]), 1);
+    mbar_fence_init();
+    codes[0] = 0;
+    codes[1] = 0;
+    uint64_t t0 = gtimer_ns();
+    bool ok = false;
+#pragma unroll 1
+    for (int it = 0; it < 64 && !ok; ++it) ok = mbar_try_wait(smem_u32(&bars[0]), 0);
+    if (!ok) atomicExch(codes + 0, MOE_DEVERR_WAIT_FULL);
+    codes[2] = ok ? 1 : 0;
+    uint64_t t1 = gtimer_ns();
+    ns[0] = t1 - t0;
+    ok = false;
+#pragma unroll 1
+    for (int it = 0; it < 256 && !ok; ++it) ok = mbar_try_wait_sleep(smem_u32(&bars[1]), 0, 1000u);
+    if (!ok) atomicExch(codes + 1, MOE_DEVERR_WAIT_EMPTY);
+    codes[3] = ok ? 1 : 0;
+    ns[1] = gtimer_ns() - t1;
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
+
+extern "C" moe_status moe_selftest_wait_timeout(int* codes, cudaStream_t stream) {
+    MOE_CHECK_ARG(codes, "moe_selftest_wait_timeout: null codes");
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t ce = cudaStreamIsCapturing(stream, &cap);
+    if (ce != cudaSuccess) return cuda_status(ce, "moe_selftest_wait_timeout: stream");
+    MOE_CHECK_ARG(cap == cudaStreamCaptureStatusNone, "moe_selftest_wait_timeout: the stream is being captured");
+    int* d = nullptr;
+    ce = cudaMalloc(&d, 4 * sizeof(int) + 2 * sizeof(unsigned long long));
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        set_error("moe_selftest_wait_timeout: cudaMalloc: %s", cudaGetErrorString(ce));
+        return MOE_ERR_NO_MEM;
+    }
+    unsigned long long* dns = reinterpret_cast<unsigned long long*>(d + 4);
+    unsigned long long hns[2] = {0, 0};
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(d, dns);
+    ce = cudaGetLastError();
+    if (ce == cudaSuccess) ce = cudaMemcpyAsync(codes, d, 4 * sizeof(int), cudaMemcpyDeviceToHost, stream);
+    if (ce == cudaSuccess) ce = cudaMemcpyAsync(hns, dns, sizeof(hns), cudaMemcpyDeviceToHost, stream);
+    if (ce == cudaSuccess) ce = cudaStreamSynchronize(stream);
+    cudaFree(d);
+    if (ce != cudaSuccess) return cuda_status(ce, "moe_selftest_wait_timeout");
+    codes[4] = (int)(hns[0] / 1000 > 0x7fffffff ? 0x7fffffff : hns[0] / 1000);  // us
+    codes[5] = (int)(hns[1] / 1000 > 0x7fffffff ? 0x7fffffff : hns[1] / 1000);
+    if (codes[0] != MOE_DEVERR_WAIT_FULL || codes[1] != MOE_DEVERR_WAIT_EMPTY || codes[2] != 0 || codes[3] != 0) {
+        set_error("moe_selftest_wait_timeout: codes %d %d, waits returned %d %d", codes[0], codes[1], codes[2],
+                  codes[3]);
+        return MOE_ERR_MISMATCH;
+    }
+    return MOE_OK;
+}
 
 extern "C" moe_status moe_selftest(cudaStream_t stream) {
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;

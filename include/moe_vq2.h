@@ -546,6 +546,19 @@ moe_status moe_vq2_encode(const float* W, int rows, int K, const uint16_t* codeb
  * of a failing entry point. */
 moe_status moe_selftest(cudaStream_t stream);
 
+/* Self-check of the bounded-wait pattern the kernels use (a limited loop of
+ * mbarrier.try_wait, then an error code in the workspace and a return): one
+ * thread waits on two mbarriers that nothing completes, with plain try_wait
+ * (64 tries) and with try_wait and a 1 us suspend hint (256 tries).  Both give
+ * up, record their codes and return, so the context stays usable.  codes:
+ * HOST int[6]: the two recorded codes (MOE_DEVERR_WAIT_FULL = 1,
+ * MOE_DEVERR_WAIT_EMPTY = 2), the two waits' results (0 = gave up) and the
+ * microseconds each wait took.  Allocates and frees 32 bytes, synchronises
+ * `stream`; not while the stream is being captured.  Returns MOE_OK when both
+ * waits gave up as designed, else MOE_ERR_MISMATCH, MOE_ERR_NO_MEM or
+ * MOE_ERR_CUDA. */
+moe_status moe_selftest_wait_timeout(int* codes, cudaStream_t stream);
+
 /* Number of kernel launches the library has issued on the host since it was
  * loaded, over all devices and threads (atomic).  A launch made while a
  * stream is being captured counts once, as the one kernel node it adds to

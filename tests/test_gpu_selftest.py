@@ -36,3 +36,21 @@ def test_selftest_refuses_a_capturing_stream():
     g.replay()
     torch.cuda.synchronize()
     assert float(x.sum()) == 4.0
+
+
+@pytest.mark.gpu
+def test_bounded_waits_give_up_and_the_context_stays_usable():
+    """Failure detection without a fault: two waits on mbarriers that nothing
+    completes (the kernels' bounded-wait pattern, plain and suspending
+    try_wait) give up after their limits, record their error codes and
+    return; the device then runs the self-check as before."""
+    torch = torch_cuda()
+    import bit_vq_routed_gb300 as bv
+    r = bv.moe_selftest_wait_timeout()
+    assert r["codes"] == (1, 2) and r["gave_up"] == (True, True), r
+    # the suspending wait's 256 tries with a 1 us hint take at least ~0.1 ms and,
+    # like the plain one, end well within a second
+    assert 0 <= r["us"][0] < 1_000_000 and 100 <= r["us"][1] < 1_000_000, r
+    print("bounded waits gave up after", r["us"], "us")
+    bv.moe_selftest()
+    torch.cuda.synchronize()
