@@ -327,7 +327,8 @@ moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* b
  * memory (scratch: the schedule, the fp32 intermediate a [P, I] and the
  * K-range partial sums of the activation-table pairs).  Its contents need
  * no initialisation.  A bounded device-side wait that ran out is recorded in
- * the int32 word at byte 8 of ws (0 = none).  Calls that share a workspace
+ * the int32 word at byte 8 of ws (0 = none); such a wait gives up after about
+ * 1 to 4 seconds (measured by moe_selftest_wait_timeout's per-try times).  Calls that share a workspace
  * must not overlap on the GPU.
  * Requires H % 256 == 0, I % 128 == 0, k <= 32, x 16-byte aligned. */
 size_t moe_vq2_expert_ffn_workspace_size(int T, int k, int E, int H, int I);
