@@ -7,6 +7,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "permute.cuh"
 
 namespace moe {
 
@@ -212,11 +213,10 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k, int renormal
     return launch_route_topk(logits, T, E, k, renormalize, ids, weights, stream);
 }
 
+// The fused routing's counter, then the permutation's chunk arrays.
 size_t moe_route_workspace_size(int T, int k, int E) {
-    (void)T;
-    (void)k;
-    (void)E;
-    return 256;
+    const long long P = (long long)T * k;
+    return 256 + (P > 0 && P <= (1 << 24) && E > 0 ? permute_ws_bytes((int)P, E) : 0);
 }
 
 moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E, int k,
@@ -249,28 +249,27 @@ moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* b
     moe_status st = launch_router_logits(x, w_router, bias, logits, T, H, E, stream);
     if (st != MOE_OK) return st;
     if ((st = launch_route_topk(logits, T, E, k, renormalize, ids, weights, stream)) != MOE_OK) return st;
-    return launch_permute(ids, T * k, E, expert_offsets, sorted_pair, pair_to_sorted, stream);
+    // (the permutation's chunk arrays follow the fused routing's counter)
+    const bool pws = ws && ws_bytes >= 256 + permute_ws_bytes(T * k, E);
+    return launch_permute_ws(ids, T * k, E, expert_offsets, sorted_pair, pair_to_sorted, stream,
+                             pws ? static_cast<char*>(ws) + 256 : nullptr, pws ? ws_bytes - 256 : 0);
 }
 
 size_t moe_permute_workspace_size(int T, int k, int E) {
-    (void)T;
-    (void)k;
-    (void)E;
-    return 0;
+    const long long P = (long long)T * k;
+    return P > 0 && P <= (1 << 24) && E > 0 ? permute_ws_bytes((int)P, E) : 0;
 }
 
 moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_offsets,
                        int32_t* sorted_pair, int32_t* pair_to_sorted, void* ws, size_t ws_bytes,
                        cudaStream_t stream) {
-    (void)ws;
-    (void)ws_bytes;
     MOE_CHECK_ARG(T >= 0 && k >= 1 && E >= 1, "moe_permute: T=%d k=%d E=%d", T, k, E);
     MOE_CHECK_SUPPORTED(E <= 1024, "moe_permute: E=%d above 1024", E);
     long long P = (long long)T * k;
     MOE_CHECK_SUPPORTED(P <= (1 << 24), "moe_permute: T*k=%lld above 2^24", P);
     MOE_CHECK_ARG(expert_offsets, "moe_permute: expert_offsets is null");
     if (P > 0) MOE_CHECK_ARG(ids && sorted_pair && pair_to_sorted, "moe_permute: null pointer");
-    return launch_permute(ids, (int)P, E, expert_offsets, sorted_pair, pair_to_sorted, stream);
+    return launch_permute_ws(ids, (int)P, E, expert_offsets, sorted_pair, pair_to_sorted, stream, ws, ws_bytes);
 }
 
 size_t moe_vq2_expert_ffn_workspace_size(int T, int k, int E, int H, int I) {

@@ -233,13 +233,23 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
         header[HDR_NUMMA] = n_umma;
         header[HDR_NVQ2] = n_vq2;
     }
-    for (int s2 = tid; s2 < P; s2 += 1024) {
-        int lo = 0, hi = E;  // find e with off[e] <= s2 < off[e+1]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (s_off[mid] <= s2) lo = mid; else hi = mid;
+    // eight positions per thread at a time: their sorted_pair loads (beyond
+    // the staged part) are in flight together
+    for (int s0 = tid; s0 < P; s0 += 8 * 1024) {
+        int spv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) spv[u] = s0 + 1024 * u < P ? sp_at(s0 + 1024 * u) : 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int s2 = s0 + 1024 * u;
+            if (s2 >= P) break;
+            int lo = 0, hi = E;  // find e with off[e] <= s2 < off[e+1]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_off[mid] <= s2) lo = mid; else hi = mid;
+            }
+            status[spv[u]] = s_res[lo];
         }
-        status[sp_at(s2)] = s_res[lo];
     }
 }
 

@@ -285,7 +285,10 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k, int renormal
  * sorted_pair int32 [P] (pair at each sorted position), pair_to_sorted
  * int32 [P] (inverse).  Requires every id in [0, E), E <= 1024, P <= 2^24.
  * ws: device workspace of moe_permute_workspace_size() bytes (may be NULL
- * when that size is 0). */
+ * when that size is 0): from 8192 pairs the sort runs over chunks of 1024
+ * pairs on many CTAs and keeps per-chunk counts there (no initialisation
+ * needed); with a smaller or NULL workspace it runs on one CTA, with the
+ * same outputs. */
 size_t moe_permute_workspace_size(int T, int k, int E);
 moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_offsets,
                        int32_t* sorted_pair, int32_t* pair_to_sorted, void* ws, size_t ws_bytes,
@@ -300,8 +303,9 @@ moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* expert_
  * routes the token; for 2..8 tokens the CTA that finishes its share of the
  * logits last does the top-k and the permutation.  Otherwise it enqueues the
  * three steps.
- * ws: moe_route_workspace_size() bytes of device memory holding a counter;
- * zero-fill it once before the first call (each call leaves it at zero).
+ * ws: moe_route_workspace_size() bytes of device memory holding a counter
+ * (and, for large calls, the permutation's per-chunk counts); zero-fill it
+ * once before the first call (each call leaves the counter at zero).
  * Calls that share a workspace must not overlap on the GPU. */
 size_t moe_route_workspace_size(int T, int k, int E);
 moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E,

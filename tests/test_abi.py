@@ -96,7 +96,12 @@ def test_workspace_sizes(lib):
     assert lib.moe_vq2_expert_ffn_workspace_size(4096, 8, 256, 4096, 2048) >= 32768 * 2048 * 4
     # decode batch 32 at top-8 fits the scratch-free variant's fixed scratch
     assert lib.moe_vq2_expert_ffn_workspace_size(32, 8, 256, 4096, 2048) <= bv.MOE_NOALLOC_SCRATCH_BYTES
-    assert lib.moe_permute_workspace_size(4096, 8, 256) == 0
+    # the permutation needs no workspace below 8192 pairs; from there two int32
+    # per (1024-pair chunk, expert), after the routing counter's 256 bytes
+    assert lib.moe_permute_workspace_size(1023, 8, 256) == 0
+    assert lib.moe_permute_workspace_size(4096, 8, 256) == 2 * 4 * 32 * 256
+    assert lib.moe_route_workspace_size(4096, 8, 256) == 256 + 2 * 4 * 32 * 256
+    assert lib.moe_route_workspace_size(1, 8, 256) == 256
 
 
 def test_launch_count_ignores_rejected_calls(lib):

@@ -24,6 +24,11 @@ def torch():
     (1, 4096, 1024, 32, 0, True), (1, 512, 48, 5, 1, False),  # one token over a cluster: 1024 and 48 experts
     (1, 8192, 300, 8, 1, True),  # one token, two weight batches per lane (H > 4096), ragged expert count
     (100, 512, 64, 4, 1, True),  # above the one-kernel limit: the three-step fallback
+    # from 8192 pairs moe_route sorts over 1024-pair chunks on many CTAs (its
+    # workspace), route_stepwise on one CTA (no workspace): the same bits
+    (1100, 256, 64, 8, 1, True),    # 8800 pairs: nine chunks, the last one ragged
+    (2048, 256, 256, 8, 1, False),  # 16384 pairs: whole chunks
+    (1500, 256, 1024, 8, 0, True),  # 1024 experts: 128 KB of per-warp counts per chunk
 ])
 def test_route_matches_stepwise(torch, T, H, E, k, renorm, with_bias):
     import bit_vq_routed_gb300 as bv
