@@ -86,6 +86,9 @@ WORKLOADS = {
                             desc="decode batch 32, Zipf(1.1) router bias, H4096 I2048 E256 top-8"),
     "mixed_fp4_b8": dict(T=8, layers=1, zipf=1.1, fp4_top=52, pool=8,
                          desc="decode batch 8, 52 most routed experts FP4 (MXFP4), 204 VQ2, Zipf(1.1)"),
+    "mixed_fp4_b1": dict(T=1, layers=4, zipf=1.1, fp4_top=52, pool=64,
+                         desc="decode batch 1, 52 most routed experts FP4 (MXFP4), 204 VQ2, Zipf(1.1), 4 layers "
+                              "with independent seeded weights"),
     "prefill_4096": dict(T=4096, layers=1, zipf=1.1, fp4_top=0, pool=1,
                          desc="prefill chunk 4096 tokens, Zipf(1.1), H4096 I2048 E256 top-8"),
     "tandem_mixed_b8": dict(T=8, layers=1, zipf=1.1, fp4_top=52, pool=8, gpu_resident=96,

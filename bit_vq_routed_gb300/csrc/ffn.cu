@@ -4,6 +4,8 @@
 // its token count m_e:
 //   - VQ2, m_e <= LUT_MAX_M: the activation-table kernels (ffn_lut.cu), one
 //     table pair per token;
+//   - FP4 in single-token calls (m_e == 1, calls of at most LUT4_MAX_T
+//     tokens): the e2m1 activation-table kernels (ffn_lut.cu);
 //   - VQ2, m_e >= 32: the tcgen05 kernels (ffn_umma.cu);
 //   - otherwise: the mma.sync kernels (ffn_mma.cu), chunks of <= 32 (VQ2) or
 //     <= 16 (FP4) tokens.
@@ -52,6 +54,8 @@ constexpr size_t SCHED_SMEM = sizeof(int) * (1025 + (MAX_TP + 1) + 4 * MAX_TP + 
 //   VQ2 with m_e <= LUT_MAX_M (and use_lut) -> m_e activation-table pairs
 //     (one per token: the expert's codes are streamed once per token, which
 //     costs less than the mma.sync decode at such counts);
+//   FP4 with m_e == 1 (and use_lut4, single-token calls) -> one e2m1 table
+//     pair (listed in expert order, all in one token group);
 //   VQ2 with m_e >= UMMA_MIN (and use_umma) -> ceil(m_e / UMMA_NT) tcgen05 chunks;
 //   otherwise -> mma.sync chunks of MMA_NT_VQ2 (VQ2) or MMA_NT_FP4 (FP4,
 //     and with split16 VQ2 experts of at most MMA_NT_FP4 tokens) tokens; the
@@ -68,7 +72,8 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
                                                         Chunk* __restrict__ chunks, LutRec* __restrict__ recs,
                                                         int32_t* __restrict__ grp_start, int use_lut,
                                                         Chunk* __restrict__ uchunks, int use_umma, int H, int I,
-                                                        int C, int4* __restrict__ fc1_range, int split16) {
+                                                        int C, int4* __restrict__ fc1_range, int split16,
+                                                        LutRec* __restrict__ recs4, int use_lut4) {
     __shared__ unsigned long long warp_tot[33];
     extern __shared__ __align__(16) int sched_smem[];
     int* s_off = sched_smem;                       // [1025]
@@ -100,20 +105,38 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
     const int nl = lut ? m : 0;  // this expert's table pairs
     const bool um = res && use_umma && m >= UMMA_MIN && d.format == MOE_FMT_VQ2;
     const bool fp4 = d.format == MOE_FMT_FP4;
+    const bool lut4 = res && use_lut4 && m == 1 && fp4;
     const bool part2 = fp4 || (split16 && m <= MMA_NT_FP4);  // the 16-token configuration
     const int nt_e = part2 ? MMA_NT_FP4 : MMA_NT_VQ2;  // tokens per mma.sync chunk of this expert
-    const int n = (res && !lut && !um) ? (m + nt_e - 1) / nt_e : 0;
+    const int n = (res && !lut && !um && !lut4) ? (m + nt_e - 1) / nt_e : 0;
     const int nu = um ? (m + UMMA_NT - 1) / UMMA_NT : 0;
     // one scan for the three counts (fields of 21 bits: n, nu, table pairs)
     unsigned long long tot;
     const unsigned long long ex =
         block_scan64((unsigned long long)(part2 ? 0 : n) | ((unsigned long long)nu << 21) | ((unsigned long long)nl << 42),
                      warp_tot, &tot);
-    unsigned long long tot4;  // the 16-token chunks, listed after the others
-    const unsigned long long ex4 = block_scan64(part2 ? (unsigned long long)n : 0ull, warp_tot, &tot4);
+    // the 16-token chunks, listed after the others, and the e2m1 table pairs
+    unsigned long long tot4;
+    const unsigned long long ex4 = block_scan64((part2 ? (unsigned long long)n : 0ull) | ((unsigned long long)lut4 << 21),
+                                                warp_tot, &tot4);
     const int n_vq2 = (int)(tot & 0x1fffff);
-    const int cbase = part2 ? n_vq2 + (int)ex4 : (int)(ex & 0x1fffff), ubase = (int)((ex >> 21) & 0x1fffff);
-    const int n_chunks = n_vq2 + (int)tot4, n_umma = (int)((tot >> 21) & 0x1fffff), n_lut = (int)(tot >> 42);
+    const int cbase = part2 ? n_vq2 + (int)(ex4 & 0x1fffff) : (int)(ex & 0x1fffff), ubase = (int)((ex >> 21) & 0x1fffff);
+    const int n_chunks = n_vq2 + (int)(tot4 & 0x1fffff), n_umma = (int)((tot >> 21) & 0x1fffff), n_lut = (int)(tot >> 42);
+    const int n_lut4 = (int)(tot4 >> 21);
+    if (lut4) {
+        LutRec r;
+        for (int mtx = 0; mtx < 3; ++mtx) {
+            r.codes[mtx] = d.codes[mtx];
+            r.scales[mtx] = d.scales[mtx];
+        }
+        r.sorted = s_off[tid];
+        r.token = sp_at(s_off[tid]) / k;
+        // one token: its e2m1 pairs form one group (they share each FC1 table)
+        static_assert(LUT4_MAX_T == 1, "e2m1 pairs of one token");
+        r.gs = 0;
+        r.gc = n_lut4;
+        recs4[(int)(ex4 >> 21)] = r;
+    }
     for (int c = 0; c < n; ++c) {
         Chunk ch;
         ch.expert = tid;
@@ -232,6 +255,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
         header[HDR_NGROUPS] = n_groups;
         header[HDR_NUMMA] = n_umma;
         header[HDR_NVQ2] = n_vq2;
+        header[HDR_NLUT4] = n_lut4;
     }
     // eight positions per thread at a time: their sorted_pair loads (beyond
     // the staged part) are in flight together
@@ -286,9 +310,12 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     // serves it as well, so the tcgen05 launches start above that (at
     // batch 32 they found work in one batch of eight and cost two launches).
     const int use_umma = T > UMMA_MIN ? 1 : 0;
+    // FP4 experts with one token take the e2m1 table kernels in single-token
+    // calls.
+    const bool use_lut4 = T <= LUT4_MAX_T && t->n_fp4 > 0;
     // With one token no expert gets two pairs, so the mma.sync kernels only
-    // have work if the table holds FP4 experts.
-    const bool mma = T > 1 || t->n_fp4 > 0 || !use_lut;
+    // have work if FP4 experts do not take the table path.
+    const bool mma = T > 1 || (t->n_fp4 > 0 && !use_lut4) || !use_lut;
     const int split16 = T >= MMA_SPLIT_T ? 1 : 0;
 
     moe_status st;
@@ -305,12 +332,16 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule shared memory");
     e = launch_pdl(schedule_kernel, dim3(1), dim3(1024), SCHED_SMEM, s, (const SlotDesc*)t->d_desc, E, offsets,
                                sorted_pair, P, k, status, header, chunks, recs, grp_start, use_lut,
-                               uchunks, use_umma, H, I, num_sms(), reinterpret_cast<int4*>(w + L.range_off), split16);
+                               uchunks, use_umma, H, I, num_sms(), reinterpret_cast<int4*>(w + L.range_off), split16,
+                               reinterpret_cast<LutRec*>(w + L.rec4_off), use_lut4 ? 1 : 0);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule launch");
     if ((mma || use_umma) && (st = launch_gather_f16(x, sorted_pair, k, H, P, w, L, s)) != MOE_OK) return st;
     if (use_lut &&
         (st = launch_lut_fc(true, false, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s)) !=
             MOE_OK)
+        return st;
+    if (use_lut4 && (st = launch_lut_fc(true, false, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w,
+                                        L, s, nullptr, nullptr, nullptr, true)) != MOE_OK)
         return st;
     if (mma && (st = launch_mma_fc(true, t, sorted_pair, weights, k, mode, out, w, L, s, split16)) != MOE_OK) return st;
     if (use_umma && (st = launch_umma(true, t, sorted_pair, weights, k, P, mode, out, w, L, s)) != MOE_OK) return st;
@@ -318,6 +349,9 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     if (use_lut &&
         (st = launch_lut_fc(false, false, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s)) !=
             MOE_OK)
+        return st;
+    if (use_lut4 && (st = launch_lut_fc(false, false, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w,
+                                        L, s, nullptr, nullptr, nullptr, true)) != MOE_OK)
         return st;
     if (mma && (st = launch_mma_fc(false, t, sorted_pair, weights, k, mode, out, w, L, s, split16)) != MOE_OK) return st;
     if (use_umma && (st = launch_umma(false, t, sorted_pair, weights, k, P, mode, out, w, L, s)) != MOE_OK) return st;

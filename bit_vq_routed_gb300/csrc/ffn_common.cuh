@@ -16,11 +16,21 @@ constexpr int MMA_NT_FP4 = 16; // tokens per mma.sync chunk of an FP4 expert (tw
 // of 4096 tokens 2.55 -> 2.34 ms per call), with few it does not (batch 32:
 // 256 -> 276 us).
 constexpr int MMA_SPLIT_T = 128;
-constexpr int LUT_KB = 8;      // scale blocks (x 128 inputs) per activation-table K-range
+constexpr int LUT_KB = 8;      // packed tiles per activation-table K-range (of 128 inputs for VQ2, 64 for FP4)
 constexpr int UMMA_MIN = 32;   // tokens from which an expert takes the tcgen05 path (calls of more than UMMA_MIN tokens)
 constexpr int UMMA_NT = 256;   // tokens per tcgen05 chunk
 constexpr int MAX_LUT_CTAS = 1024;  // grid of the activation-table kernels (one CTA per SM) at most
 constexpr int LUT_MAX_M = 3;   // VQ2 experts with up to this many tokens take the activation-table path
+// In calls of at most LUT4_MAX_T tokens, FP4 experts with one token take the
+// e2m1 activation-table path.  Measured with 52 of 256 experts FP4
+// (expert-FFN call, us, e2m1 path / mma.sync path): 1 token 50.0 / 100.0;
+// with a first build of the e2m1 kernels (one table per pair) 2 tokens
+// 136.3 / 112.9, 4 tokens 158.6 / 129.3, 8 tokens 176.8 / 174.2.  With one
+// token every FP4 expert takes it and the call needs no mma.sync, gather or
+// conversion kernel; with more, the mma.sync kernels still run for the FP4
+// experts with several tokens and take about as long for a few experts as
+// for all of them.
+constexpr int LUT4_MAX_T = 1;
 
 // A run of sorted positions of one expert (tensor-core paths).
 struct Chunk {
@@ -40,7 +50,8 @@ static_assert(sizeof(LutRec) == 64 && offsetof(LutRec, codes) == 0 && offsetof(L
 // Header words at the start of the workspace.
 // HDR_NVQ2: the chunks list holds the 32-token chunks first (HDR_NVQ2 of
 // them), then the 16-token ones (FP4, and small VQ2 experts in large calls).
-enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NUMMA = 4, HDR_NVQ2 = 5 };
+// HDR_NLUT4: the e2m1 table pairs (rec4).
+enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NUMMA = 4, HDR_NVQ2 = 5, HDR_NLUT4 = 6 };
 
 // Activation-table pairs (VQ2 experts with at most LUT_MAX_M tokens, one pair
 // per token) are listed sorted by (token, expert) in lut_rec, grouped by
@@ -57,10 +68,14 @@ enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NU
 // so neither overflows fp16 whatever the range of the activations; the FC1
 // epilogues write a in fp32 (a32) and flag the sorted positions they wrote
 // (amax), from which the conversion kernel makes a16.
+// The e2m1 table pairs (FP4 experts with one token, calls of at most
+// LUT4_MAX_T tokens) have their own records (rec4, one token group),
+// partial sums (p1_4, p2_4) and FC2 arrival counters (cnt4).
 struct WsLayout {
     size_t chunks_off, rec_off, grp_start_off, p1_off, p2_off, cnt_off, cnt2_off, range_off;
+    size_t rec4_off, p1_4_off, p2_4_off, cnt4_off;
     size_t uchunks_off, x16s_off, a16_off, xsc_off, asc_off, amax_off, a32_off, total;
-    int max_chunks, max_lut, max_uchunks;
+    int max_chunks, max_lut, max_uchunks, max_lut4;
 };
 
 __host__ __device__ inline size_t ws_align(size_t v) { return (v + 255) / 256 * 256; }
@@ -68,6 +83,8 @@ __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; 
 
 // K-ranges of the activation-table path for an input length K.
 __host__ __device__ inline int lut_jobs(int K) { return ceil_div(K / 128, LUT_KB); }
+// K-ranges of the e2m1 table path (LUT_KB tiles of 64 inputs each).
+__host__ __device__ inline int lut4_jobs(int K) { return ceil_div(K / 64, LUT_KB); }
 
 // Units [u0, u1) of CTA i of C for jobs j = 0..J-1 covering the units
 // [start(j), start(j+1)), start(J) = U, where a0(j) = floor(C start(j) / U).
@@ -98,6 +115,15 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I)
     o = ws_align(o + sizeof(int32_t) * (size_t)(H / 16));
     L.range_off = o;
     o = ws_align(o + sizeof(int4) * (size_t)MAX_LUT_CTAS);
+    L.max_lut4 = T <= LUT4_MAX_T ? (int)(P < (long long)E ? P : (long long)E) : 0;
+    L.rec4_off = o;
+    o = ws_align(o + sizeof(LutRec) * (size_t)L.max_lut4);
+    L.p1_4_off = o;
+    o = ws_align(o + sizeof(float) * (size_t)L.max_lut4 * lut4_jobs(H) * 2 * I);
+    L.p2_4_off = o;
+    o = ws_align(o + sizeof(float) * (size_t)L.max_lut4 * lut4_jobs(I) * H);
+    L.cnt4_off = o;
+    o = ws_align(o + sizeof(int32_t) * (size_t)L.max_lut4 * (H / 16));
     const bool umma = T >= UMMA_MIN;
     L.max_uchunks = umma ? (int)(P / UMMA_NT + E) : 0;
     L.uchunks_off = o;
@@ -124,7 +150,7 @@ moe_status launch_lut_fc(bool fc1, bool self, const SlotTableHost* t, const uint
                          const int32_t* sorted_pair, const float* weights, int k, int P, int mode, float* out,
                          uint8_t* status, char* ws, const WsLayout& L, cudaStream_t s,
                          const int32_t* pair_to_sorted = nullptr, float* comb32 = nullptr,
-                         uint16_t* comb16 = nullptr);
+                         uint16_t* comb16 = nullptr, bool f4 = false);
 // x16s, xsc (and amax zeroed) for every sorted position.
 moe_status launch_gather_f16(const uint16_t* x, const int32_t* sorted_pair, int k, int H, int P, char* ws,
                              const WsLayout& L, cudaStream_t s);

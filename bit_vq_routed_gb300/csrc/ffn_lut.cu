@@ -1,7 +1,8 @@
 // Activation-table path of the expert FFN, for VQ2 experts that receive at
 // most LUT_MAX_M tokens in this call (every expert at decode batch 1, most of
 // them at small batches): one table pair per (token, expert), the expert's
-// codes streamed once per token.
+// codes streamed once per token.  In single-token calls the FP4 experts take
+// the same kernels with e2m1 tables (the F4 instances).
 //
 // The table, the lane layout and the per-unit lookups are the shared core in
 // lut_core.cuh.
@@ -62,7 +63,15 @@ static_assert(0x400 + ((sizeof(Smem) + 127) / 128 * 128) + LOW_SLOTS * SLOT_BYTE
 // the kernel lists the call's pairs itself from the expert offsets and the
 // slot table (one token group; pairs in sorted order, non-resident ones
 // reported and skipped).
-template <bool FC1, bool SELF>
+// F4: the FP4 experts of a single-token call (e2m1 tables over K-ranges of
+// 512 inputs; the schedule's second record list, one token group; never
+// SELF).  These kernels read only what the schedule and the kernels before
+// their predecessor wrote (FC2: the e2m1 FC1's partial sums), which is
+// complete when they start, because the predecessor lets its dependents
+// start only after its own wait.  So they run beside their predecessor's
+// last CTAs and wait for it only before they exit, which keeps the chain of
+// completions that the kernels after them rely on.
+template <bool FC1, bool SELF, bool F4>
 __global__ void __maxnreg__(MAX_REG)
     ffn_lut_kernel(const SlotDesc* __restrict__ desc, const int32_t* __restrict__ offsets, int E, int P,
                    uint8_t* __restrict__ status, const uint16_t* __restrict__ codebook, const uint16_t* __restrict__ x,
@@ -76,12 +85,15 @@ __global__ void __maxnreg__(MAX_REG)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int* err = header + HDR_ERR;
 
+    static_assert(!(F4 && SELF), "FP4 pairs come from the schedule");
+    constexpr int TILE_IN = F4 ? 64 : 128;     // inputs per packed tile
+    constexpr int KRI = LUT_KB * TILE_IN;      // inputs per K-range
     const int K = FC1 ? H : I;             // inputs of this matrix
     const int R = FC1 ? 2 * I : H;         // rows per pair (FC1: gate rows, then up rows)
-    const int KB = K / 128;
-    const int KR = lut_jobs(K);
+    const int KB = K / TILE_IN;
+    const int KR = F4 ? lut4_jobs(K) : lut_jobs(K);
     const int RT = R / 16;
-    const int KR1 = lut_jobs(H);
+    const int KR1 = F4 ? lut4_jobs(H) : lut_jobs(H);
     const int per_pair = KR * RT;          // units of one pair
     const int C = gridDim.x;
 
@@ -96,7 +108,8 @@ __global__ void __maxnreg__(MAX_REG)
     }
     const uint32_t slot = warp < LOW_SLOTS ? low_base + warp * SLOT_BYTES : HIGH_BASE + (warp - LOW_SLOTS) * SLOT_BYTES;
     const uint32_t bar = smem_u32(&S.full[warp]);
-    for (int i = tid; i < 128 * 4; i += THREADS) S.cb[i] = __half2float(__ushort_as_half(codebook[i]));
+    if (!F4)
+        for (int i = tid; i < 128 * 4; i += THREADS) S.cb[i] = __half2float(__ushort_as_half(codebook[i]));
     if (tid < NSLOT) mbar_init(smem_u32(&S.full[tid]), 1);
     if (tid == 0) S.failed = 0;
     mbar_fence_init();
@@ -111,7 +124,7 @@ __global__ void __maxnreg__(MAX_REG)
     // the job's CTAs interleaved, so that every CTA meets the same mix of
     // pairs and rows.
     int n_lut, u0, u1, s_off0 = 0, s_step = 0;
-    bool waited = FC1;  // FC2 waits for FC1 once its first job's code copies are issued
+    bool waited = FC1 || F4;  // FC2 waits for FC1 once its first job's code copies are issued
     // every job is RT units (SELF FC1: one token group of n_lut pairs, KR jobs
     // of n_lut * RT units) -> the proportional split is direct
     auto uniform_range = [&](int J, int job_units) {
@@ -135,14 +148,17 @@ __global__ void __maxnreg__(MAX_REG)
     // exponent (block-wide); tab_s = 2^e multiplies each unit's sums back.
     float tab_s = 1.0f;
     auto build_table = [&](int nkb) {
-        const int e = table_exponent(S.xs, 128 * nkb, S.cb, S.red, tid);
+        const int e = table_exponent(S.xs, TILE_IN * nkb, F4 ? nullptr : S.cb, S.red, tid);
         tab_s = exp2_int(e);
-        lut::build_table(S.xs, S.cb, nkb, e, tid);
+        if (F4)
+            lut::build_table_f4(S.xs, nkb, e, tid);
+        else
+            lut::build_table(S.xs, S.cb, nkb, e, tid);
     };
     // The token's activations of a K-range into S.xs (as fp32).
     auto load_x = [&](int t, int kr, int nin) {
         for (int i = tid; i < nin; i += THREADS)
-            S.xs[xs_at(i)] = __uint_as_float((uint32_t)x[(size_t)t * H + KR_IN * kr + i] << 16);
+            S.xs[xs_at(i)] = __uint_as_float((uint32_t)x[(size_t)t * H + KRI * kr + i] << 16);
     };
     // SELF FC1: the CTA's K-range follows from the grid alone (KR jobs of
     // equal size, see uniform_range), so the activations and the table are
@@ -153,7 +169,7 @@ __global__ void __maxnreg__(MAX_REG)
     // sums straight into the zeroed output row (fp32 addition is commutative,
     // so 0 + p0 + p1 does not depend on the order) instead of a finishing
     // step; FC1 zeroes the rows of the table pairs.
-    const bool fc2_adds = mode == MOE_PER_PAIR && lut_jobs(I) == 2;
+    const bool fc2_adds = !F4 && mode == MOE_PER_PAIR && lut_jobs(I) == 2;
     auto zero_rows = [&](auto row_of) {
         const int n4 = H / 4;  // (n_lut <= E <= 1024 table pairs)
         for (int i = blockIdx.x * THREADS + tid; i < n_lut * n4; i += C * THREADS) {
@@ -245,15 +261,20 @@ __global__ void __maxnreg__(MAX_REG)
             if (fc2_adds) zero_rows([&](int p) { return S.all_ys[p]; });
         }
     } else if (FC1) {
-        pdl_wait();
+        if (!F4) pdl_wait();
         // everything a dependent kernel may touch before its own wait is complete
         pdl_launch_dependents();
-        n_lut = header[HDR_NLUT];
-        const int4 rg = fc1_range[blockIdx.x];  // computed by the schedule
-        u0 = rg.x;
-        u1 = rg.y;
-        s_off0 = rg.z;
-        s_step = rg.w;
+        if (F4) {
+            n_lut = __ldcg(header + HDR_NLUT4);
+            uniform_range(KR, n_lut * RT);  // one token group
+        } else {
+            n_lut = header[HDR_NLUT];
+            const int4 rg = fc1_range[blockIdx.x];  // computed by the schedule
+            u0 = rg.x;
+            u1 = rg.y;
+            s_off0 = rg.z;
+            s_step = rg.w;
+        }
         // FC2's arrival counters start at zero
         const int nc = n_lut * (H / 16);
         for (int i = blockIdx.x * THREADS + tid; i < nc; i += C * THREADS) cnt[i] = 0;
@@ -261,8 +282,9 @@ __global__ void __maxnreg__(MAX_REG)
     } else {
         // The schedule is two kernels back, so complete: this CTA's units and
         // their code bytes are known before FC1 completes.
-        n_lut = __ldcg(header + HDR_NLUT);
+        n_lut = __ldcg(header + (F4 ? HDR_NLUT4 : HDR_NLUT));
         uniform_range(n_lut * KR, RT);
+        if (F4) pdl_launch_dependents();
     }
 
     const bool comb = !FC1 && SELF && (comb32 != nullptr || comb16 != nullptr);
@@ -284,7 +306,7 @@ __global__ void __maxnreg__(MAX_REG)
         const int job_start = per_pair * gs + kr * RT * gc;
         const int seg_end = min(u1, job_start + RT * gc);
         const int nkb = min(LUT_KB, KB - LUT_KB * kr);
-        const int nin = 128 * nkb;
+        const int nin = TILE_IN * nkb;
         const bool active = b < nkb;
         if (tid < gc) {
             if (SELF) {
@@ -369,7 +391,30 @@ __global__ void __maxnreg__(MAX_REG)
             if (comb16 == nullptr) pdl_launch_dependents();
             waited = true;
         }
-        if (!FC1) {
+        if (!FC1 && F4) {
+            // (FP4: one input per thread, 8 partials of g and of u in flight)
+            static_assert(!F4 || KRI <= THREADS, "one input per thread");
+            const float* pp = p1 + (size_t)gs * KR1 * 2 * I;
+            const int i = tid, gi = KRI * kr + i;
+            float g = 0.0f, up = 0.0f;
+            for (int j0 = 0; j0 < KR1; j0 += 8) {
+                float pg[8], pu[8];
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const bool in = i < nin && j0 + jj < KR1;
+                    pg[jj] = in ? pp[(size_t)(j0 + jj) * 2 * I + gi] : 0.0f;
+                    pu[jj] = in ? pp[(size_t)(j0 + jj) * 2 * I + I + gi] : 0.0f;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                    if (j0 + jj < KR1) {
+                        g += pg[jj];
+                        up += pu[jj];
+                    }
+            }
+            if (i < nin) S.xs[xs_at(i)] = silu_mul(g, up);
+            __syncthreads();
+        } else if (!FC1) {
             // silu(g) * u of the pair from FC1's K-range partial sums, added in
             // order: a thread's (up to 4) inputs with 4 partials each in flight
             const float* pp = p1 + (size_t)gs * KR1 * 2 * I;
@@ -379,7 +424,7 @@ __global__ void __maxnreg__(MAX_REG)
                     float pg[4][4], pu[4][4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int i = i0 + q * THREADS, gi = KR_IN * kr + i;
+                        const int i = i0 + q * THREADS, gi = KRI * kr + i;
 #pragma unroll
                         for (int jj = 0; jj < 4; ++jj) {
                             const bool in = i < nin && j0 + jj < KR1;
@@ -411,7 +456,7 @@ __global__ void __maxnreg__(MAX_REG)
         auto compute_store = [&](const UnitRegs& r, Cur cu) {
             const int pi = cu.pi, rt = cu.rt;
             float acc[1];
-            acc[0] = unit_rows(r, lb, active, lane) * tab_s;
+            acc[0] = unit_rows<F4>(r, lb, active, lane) * tab_s;
             const int h = rt * 16 + unit_row(lane);  // output row of this lane pair
             auto emit = [&](float y) {  // FC2: the finished y of row h
                 const int s = S.ys[pi];
@@ -533,6 +578,7 @@ __global__ void __maxnreg__(MAX_REG)
         pdl_wait();
         if (comb16 == nullptr) pdl_launch_dependents();
     }
+    if (F4) pdl_wait();  // (see the kernel's description)
     if (comb && n_lut == 0) {  // no pair computed: the combine is zero
         for (int h = blockIdx.x * THREADS + tid; h < H; h += C * THREADS) {
             if (comb32) comb32[h] = 0.0f;
@@ -546,15 +592,20 @@ __global__ void __maxnreg__(MAX_REG)
 moe_status launch_lut_fc(bool fc1, bool self, const SlotTableHost* t, const uint16_t* x, const int32_t* offsets,
                          const int32_t* sorted_pair, const float* weights, int k, int P, int mode, float* out,
                          uint8_t* status, char* ws, const WsLayout& L, cudaStream_t s,
-                         const int32_t* pair_to_sorted, float* comb32, uint16_t* comb16) {
+                         const int32_t* pair_to_sorted, float* comb32, uint16_t* comb16, bool f4) {
+    if (f4 && (self || comb32 || comb16)) {
+        set_error("moe_vq2_expert_ffn: FP4 table pairs come from the schedule");
+        return MOE_ERR_UNSUPPORTED;
+    }
     int* header = reinterpret_cast<int*>(ws);
-    const LutRec* recs = reinterpret_cast<const LutRec*>(ws + L.rec_off);
+    const LutRec* recs = reinterpret_cast<const LutRec*>(ws + (f4 ? L.rec4_off : L.rec_off));
     const int4* fc1_range = reinterpret_cast<const int4*>(ws + L.range_off);
-    const float* p1 = reinterpret_cast<const float*>(ws + L.p1_off);
-    float* pout = reinterpret_cast<float*>(ws + (fc1 ? L.p1_off : L.p2_off));
-    int* cnt = reinterpret_cast<int*>(ws + L.cnt_off);
-    auto kern = self ? (fc1 ? ffn_lut_kernel<true, true> : ffn_lut_kernel<false, true>)
-                     : (fc1 ? ffn_lut_kernel<true, false> : ffn_lut_kernel<false, false>);
+    const float* p1 = reinterpret_cast<const float*>(ws + (f4 ? L.p1_4_off : L.p1_off));
+    float* pout = reinterpret_cast<float*>(ws + (f4 ? (fc1 ? L.p1_4_off : L.p2_4_off) : (fc1 ? L.p1_off : L.p2_off)));
+    int* cnt = reinterpret_cast<int*>(ws + (f4 ? L.cnt4_off : L.cnt_off));
+    auto kern = f4 ? (fc1 ? ffn_lut_kernel<true, false, true> : ffn_lut_kernel<false, false, true>)
+                   : self ? (fc1 ? ffn_lut_kernel<true, true, false> : ffn_lut_kernel<false, true, false>)
+                          : (fc1 ? ffn_lut_kernel<true, false, false> : ffn_lut_kernel<false, false, false>);
     cudaError_t e = ensure_smem_attr(kern, (int)DYN_SMEM);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: table kernel shared memory");
     // One CTA per SM; the single-token FC1 leaves one SM free, so that all of

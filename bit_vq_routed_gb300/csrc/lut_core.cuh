@@ -21,6 +21,12 @@
 //
 // A unit is 16 rows x 1024 inputs (8 packed tiles: 4 KB of codes, 256 B of
 // scales), copied into a warp's slot by three bulk copies.
+//
+// FP4 (MXFP4) experts use the same table shape with the code byte's two e2m1
+// values in place of the codebook row: a byte of group G holds elements 2G
+// and 2G + 1, so a table covers 512 inputs, a packed e2m1 tile (16 rows x 64)
+// is 512 bytes with the lane ownership of a VQ2 tile, and each row sums its
+// two 32-element blocks separately for their ue8m0 scales.
 #pragma once
 
 #include "ffn_common.cuh"
@@ -101,17 +107,47 @@ __device__ __forceinline__ float row_sum(const UnitRegs& u, uint32_t lb) {
     return t * ((ROW & 1) ? __high2float(h) : __low2float(h));
 }
 
+// The same sum for packed e2m1 tiles (FP4 experts): a tile is 16 rows x 64
+// elements, and the lane's chunk i (16 bytes) holds rows i and i + 8 for its
+// 8 groups of 2 elements: byte 4s + 2h + u is row i + 8h, group slot 2s + u.
+// Slots 0-3 and 4-7 lie in the tile's two 32-element scale blocks: each part
+// is multiplied by its ue8m0 scale (sc[0], sc[1]: one byte per row).
+template <int RB>
+__device__ __forceinline__ float row_sum_f4(const UnitRegs& u, uint32_t lb) {
+    constexpr int ROW = (RB >> 1) + 8 * (RB & 1);
+    constexpr int I = ROW & 7, H = ROW >> 3;
+    const uint32_t* w = &u.cw[I].x;
+    float t0 = 0.0f, t1 = 0.0f;
+    t0 = tab_add<0>(prmt_i<0x7604u | ((2 * H) << 4)>(w[0], lb), t0);
+    t0 = tab_add<1>(prmt_i<0x7604u | ((2 * H + 1) << 4)>(w[0], lb), t0);
+    t0 = tab_add<2>(prmt_i<0x7604u | ((2 * H) << 4)>(w[1], lb), t0);
+    t0 = tab_add<3>(prmt_i<0x7604u | ((2 * H + 1) << 4)>(w[1], lb), t0);
+    t1 = tab_add<4>(prmt_i<0x7604u | ((2 * H) << 4)>(w[2], lb), t1);
+    t1 = tab_add<5>(prmt_i<0x7604u | ((2 * H + 1) << 4)>(w[2], lb), t1);
+    t1 = tab_add<6>(prmt_i<0x7604u | ((2 * H) << 4)>(w[3], lb), t1);
+    t1 = tab_add<7>(prmt_i<0x7604u | ((2 * H + 1) << 4)>(w[3], lb), t1);
+    // ue8m0 byte e -> 2^(e - 127): the byte moved to bits 16-23 (one byte
+    // permute), shifted to the exponent field; e = 0 gives 0x400000, the
+    // subnormal 2^-127
+    constexpr uint32_t SSEL = 0x4044u | (uint32_t)((ROW & 3) << 8);
+    const uint32_t b0 = prmt_i<SSEL>((&u.sc[0].x)[ROW >> 2], 0u) << 7;
+    const uint32_t b1 = prmt_i<SSEL>((&u.sc[1].x)[ROW >> 2], 0u) << 7;
+    const float s0 = __uint_as_float(max(b0, 0x400000u)), s1 = __uint_as_float(max(b1, 0x400000u));
+    return fmaf(t1, s1, t0 * s0);
+}
+
 // The 16 row sums of a unit, reduced over the warp by a reduce-scatter: lanes
 // 2p and 2p+1 end with the sum of row unit_row(lane).  Its first step (lanes
 // 16 apart) runs as each pair of row sums (i, i + 8) is ready, so only 8 sums
 // stay live.  Inactive lanes (scale block beyond the K-range) add zeros.
+template <bool F4 = false>
 __device__ __forceinline__ float unit_rows(const UnitRegs& r, uint32_t lb, bool active, int lane) {
     float acc[8];
     const bool up16 = lane & 16;
 #define MOE_LUT_PAIR(I)                                                                  \
     {                                                                                    \
-        const float lo = active ? row_sum<I>(r, lb) : 0.0f;                              \
-        const float hi = active ? row_sum<I + 8>(r, lb) : 0.0f;                          \
+        const float lo = active ? (F4 ? row_sum_f4<I>(r, lb) : row_sum<I>(r, lb)) : 0.0f;              \
+        const float hi = active ? (F4 ? row_sum_f4<I + 8>(r, lb) : row_sum<I + 8>(r, lb)) : 0.0f;      \
         acc[I] = (up16 ? hi : lo) + __shfl_xor_sync(0xffffffffu, up16 ? lo : hi, 16);   \
     }
     MOE_LUT_PAIR(0)
@@ -152,10 +188,13 @@ __device__ __forceinline__ int unit_row(int lane) {
 // unscaled entries bit for bit.  Block-wide (every thread calls it, after the
 // inputs are in xs); red: 2 * LW words of shared scratch, which the caller
 // must not pass to another call before a CTA barrier.  Returns e.
+// cb == nullptr: e2m1 byte tables, whose entries are at most 6 + 6 = 12 times
+// max |x|.
 __device__ __forceinline__ int table_exponent(const float* xs, int nin, const float* cb, unsigned* red, int tid) {
     float xm = 0.0f, c1 = 0.0f;
     for (int i = tid; i < nin; i += THREADS) xm = fmaxf(xm, fabsf(xs[xs_at(i)]));
-    if (tid < 128) c1 = fabsf(cb[4 * tid]) + fabsf(cb[4 * tid + 1]) + fabsf(cb[4 * tid + 2]) + fabsf(cb[4 * tid + 3]);
+    if (tid < 128)
+        c1 = cb ? fabsf(cb[4 * tid]) + fabsf(cb[4 * tid + 1]) + fabsf(cb[4 * tid + 2]) + fabsf(cb[4 * tid + 3]) : 12.0f;
     // non-negative floats order as their bit patterns
     const unsigned ux = __reduce_max_sync(0xffffffffu, __float_as_uint(xm));
     const unsigned uc = __reduce_max_sync(0xffffffffu, __float_as_uint(c1));
@@ -223,6 +262,61 @@ __device__ __forceinline__ void build_table(const float* xs, const float* cb, in
                      "r"(wv[3]));
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + 128u * 256u), "r"(wv[0] ^ 0x80008000u),
                      "r"(wv[1] ^ 0x80008000u), "r"(wv[2] ^ 0x80008000u), "r"(wv[3] ^ 0x80008000u));
+    }
+}
+
+// e2m1 value of a 4-bit code: sign bit 3, exponent bits 1-2 (bias 1), one
+// mantissa bit; exponent 0 is the subnormal 0 / 0.5.  (Plain arithmetic, so
+// that a constant code folds to a constant.)
+__host__ __device__ constexpr float e2m1_value(int n) {
+    return ((n & 8) ? -1.0f : 1.0f) *
+           (((n & 7) >> 1) ? (float)(2 + (n & 1)) * (float)(1 << ((n & 7) >> 1)) * 0.25f : 0.5f * (float)(n & 1));
+}
+
+// The e2m1 table of one K-range (FP4 experts): a code byte holds the two
+// elements 2G (low nibble) and 2G + 1 (high nibble) of group G, so entry
+// L[v][G] = e2m1(v & 15) x[2G] + e2m1(v >> 4) x[2G + 1], divided by 2^e
+// (table_exponent with cb == nullptr); no sign fold (all 256 bytes are
+// built).  The K-range holds 512 inputs, nkb tiles of 64; the quads, slots
+// and addresses are those of build_table, with 2-input groups.  Warp w
+// builds the bytes v = w + 16 i (LW == 16): its low nibble is w, its high
+// nibble the step i.
+__device__ __forceinline__ void build_table_f4(const float* xs, int nkb, int e, int tid) {
+    static_assert(LW == 16, "one low nibble per warp");
+    const int warp = tid >> 5;
+    const int q = tid & 31, lq = q & 7, jj = (q >> 3) & 1, p = q >> 4, bq = lane_block(4 * lq);
+    if (bq >= nkb) return;
+    const int i0 = 64 * bq + 32 * p + 16 * jj;  // inputs 2 g0 .. 2 g0 + 15, g0 = 32 bq + 4 (4p + 2jj)
+    const float inv = exp2_int(-e);
+    const float4 f0 = *reinterpret_cast<const float4*>(&xs[xs_at(i0)]);
+    const float4 f1 = *reinterpret_cast<const float4*>(&xs[xs_at(i0 + 4)]);
+    const float4 f2 = *reinterpret_cast<const float4*>(&xs[xs_at(i0 + 8)]);
+    const float4 f3 = *reinterpret_cast<const float4*>(&xs[xs_at(i0 + 12)]);
+    // word mm holds groups g0 + mm (low half) and g0 + 4 + mm (high half):
+    // x0[mm] / x1[mm] their first / second elements
+    const float2 x0[4] = {make_float2(f0.x * inv, f2.x * inv), make_float2(f0.z * inv, f2.z * inv),
+                          make_float2(f1.x * inv, f3.x * inv), make_float2(f1.z * inv, f3.z * inv)};
+    const float2 x1[4] = {make_float2(f0.y * inv, f2.y * inv), make_float2(f0.w * inv, f2.w * inv),
+                          make_float2(f1.y * inv, f3.y * inv), make_float2(f1.w * inv, f3.w * inv)};
+    const float lo = e2m1_value(warp);
+    float2 lx[4];  // the low nibble's part, the same for every byte of this warp
+#pragma unroll
+    for (int mm = 0; mm < 4; ++mm) lx[mm] = __fmul2_rn(make_float2(lo, lo), x0[mm]);
+    const uint32_t a0 = TAB + (uint32_t)p * PLANE + 128u * jj + 16u * lq + 256u * (uint32_t)warp;
+    // (unrolled by 8: the step's value is a constant up to its sign; a full
+    // unroll spills in FC2)
+#pragma unroll 8
+    for (int it = 0; it < 16; ++it) {
+        const float hi = e2m1_value(it);
+        uint32_t wv[4];
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+            const float2 v2 = __ffma2_rn(make_float2(hi, hi), x1[mm], lx[mm]);
+            const __half2 hv = __floats2half2_rn(v2.x, v2.y);
+            wv[mm] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + 256u * 16u * (uint32_t)it), "r"(wv[0]),
+                     "r"(wv[1]), "r"(wv[2]), "r"(wv[3]));
     }
 }
 

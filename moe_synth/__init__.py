@@ -198,6 +198,7 @@ WORKLOADS = {
     "decode_b1": dict(T=1, layers=4),
     "decode_b32_zipf": dict(T=32, layers=1, zipf_s=1.1),
     "mixed_fp4_b8": dict(T=8, layers=1, zipf_s=1.1, fp4_top=52, resident_subset=96),
+    "mixed_fp4_b1": dict(T=1, layers=4, zipf_s=1.1, fp4_top=52),
     "prefill_4096": dict(T=4096, layers=1, zipf_s=1.1),
 }
 

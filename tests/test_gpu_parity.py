@@ -59,6 +59,40 @@ def test_single_token_experts_table_path(torch, H, I, T, E, k):
     _check_layer(spec, T, seed=T)
 
 
+@pytest.mark.parametrize("H,I,E,k,fp4_top", [(512, 256, 16, 4, 16), (1280, 384, 64, 8, 64), (768, 640, 128, 3, 128),
+                                              (4096, 2048, 256, 8, 52), (1024, 384, 32, 4, 16), (256, 128, 4, 2, 4),
+                                              (512, 256, 8, 1, 8)])
+def test_fp4_experts_single_token_e2m1_table_path(torch, H, I, E, k, fp4_top):
+    # in single-token calls FP4 experts go through the e2m1 table kernels;
+    # K-ranges of 2 to 8 tiles of 64 inputs (H, I not multiples of 512)
+    # included
+    spec = ms.LayerSpec(H=H, I=I, E=E, k=k, seed=H + I + k, zipf_s=1.1, fp4_top=fp4_top)
+    _check_layer(spec, 1, seed=k)
+
+
+def test_fp4_experts_single_token_non_resident_reported(torch):
+    spec = ms.LayerSpec(H=512, I=256, E=16, k=8, seed=17, fp4_top=16)
+    res = np.zeros(16, bool)
+    res[::2] = True
+    _check_layer(spec, 1, seed=17, resident=res)
+
+
+def test_fp4_table_pairs_fused_scatter_matches_per_pair(torch):
+    import bit_vq_routed_gb300 as bv
+    spec = ms.LayerSpec(H=1280, I=640, E=64, k=8, seed=31, fp4_top=64)
+    layer = ms.Layer(spec)
+    x = ms.tokens(1, spec.H, seed=31)
+    dev, keep = device_layer(layer, 1)
+    g = run(dev, x)
+    xt = torch.from_numpy(x).view(torch.bfloat16).cuda()
+    out = torch.zeros(1, spec.H, dtype=torch.float32, device="cuda")
+    dev.route(xt)
+    dev.experts(xt, bv.MOE_FUSED_SCATTER, out)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert np.abs(o - g["out"]).max() <= 1e-5 * np.abs(g["out"]).max()
+
+
 def test_wider_hidden_mixed_formats(torch):
     spec = ms.LayerSpec(H=1024, I=384, E=12, k=4, seed=21, zipf_s=1.1, fp4_top=4)
     _check_layer(spec, 24, seed=3)

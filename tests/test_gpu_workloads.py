@@ -4,6 +4,7 @@
   - decode batch 32 with Zipf(1.1) routing bias;
   - mixed FP4 (52 most routed) / VQ2 decode batch 8, all resident and with
     only the 96 most routed resident (GPU partial + oracle remainder = whole);
+  - the same layers at decode batch 1 (FP4 experts on the e2m1 table path);
   - prefill chunk of 4096 tokens: routing bit-exact for every token, layer
     output on a sample of tokens the oracle computes one by one.
 """
@@ -79,6 +80,20 @@ def test_mixed_fp4_vq2_batch8_and_partial_residency(torch):
     assert (g2["status"] == 0).any()
     assert_close(g2["out"], r2["partial"], "resident partial")
     assert_close(g2["out"] + r2["remainder"], r2["out"], "partial + remainder")
+
+
+def test_mixed_fp4_vq2_batch1(torch):
+    layer = ms.Layer(ms.spec_decode(0, zipf_s=1.1, fp4_top=52))
+    dev, keep = device_layer(layer, 1)
+    n_fp4 = 0
+    for stream in range(3):
+        x = ms.tokens(1, 4096, seed=400, stream=stream)
+        g = run(dev, x)
+        r = O.moe_layer(layer, x)
+        assert_routing_exact(g, r)
+        n_fp4 += int((layer.formats[r["ids"]] == ms.FMT_FP4).sum())
+        assert_close(g["out"], r["out"], f"mixed batch 1, token {stream}")
+    assert n_fp4 > 0
 
 
 def test_prefill_4096_routing_exact_and_sampled_outputs(torch):
