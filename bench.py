@@ -45,15 +45,15 @@ FFN_FLOP_PER_PAIR = 2 * 3 * 4096 * 2048  # gate, up and down matvecs of one (tok
 L2_BYTES = 129 * 2 ** 20
 
 # DRAM bytes (read + write) of one expert-FFN call, from one ncu capture of its
-# kernels (the two single-token table kernels, ffn_lut_kernel<1,1> and
-# ffn_lut_kernel<0,1>, of `python bench.py --layers 1 --steps 3 --warmup 3
-# --no-cpu` under ncu: FC1 35,737,856 + 512, FC2 18,547,456 at decode batch 1).
+# kernels (the two single-token table kernels, ffn_lut_kernel<1,1,0> and
+# ffn_lut_kernel<0,1,0>, of `python bench.py --layers 1 --steps 3 --warmup 3
+# --no-cpu` under ncu: FC1 35,727,616 + 3,584, FC2 18,540,544 at decode batch 1).
 # Reported only while the kernel sources hash to the ones the counters were
 # taken on.
-TRAFFIC = {"decode_b1": {"bytes": 54_267_392,
-                         "profile": "ncu capture of ffn_lut_kernel<1,1> and ffn_lut_kernel<0,1>, decode batch 1",
+TRAFFIC = {"decode_b1": {"bytes": 54_271_744,
+                         "profile": "ncu capture of ffn_lut_kernel<1,1,0> and ffn_lut_kernel<0,1,0>, decode batch 1",
                          "sources": ["ffn_lut.cu", "lut_core.cuh", "ffn_common.cuh", "common.cuh"],
-                         "sha256": "a647cbed88054ba61af381c753247846f118872b62283f18c84e3156c1a99d26"}}
+                         "sha256": "96072346d4bdf9fc2afb2b3bef51625cb9e3204e4a517e2c2b8442a399f094e5"}}
 
 
 # Workloads whose bench figure averages many token batches (different expert
