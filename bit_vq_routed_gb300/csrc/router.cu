@@ -63,11 +63,14 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t
     };
     pdl_wait();
     pdl_launch_dependents();  // dependents may start their prologues now
-    float acc[4][16];
+    // acc2[a][bp] = (dot (a, 2 bp), dot (a, 2 bp + 1)): the packed fp32 pairs
+    // round each product and each sum exactly as the scalar operations do,
+    // two experts per instruction
+    float2 acc2[4][8];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 16; ++b) acc[a][b] = 0.0f;
+        for (int bp = 0; bp < 8; ++bp) acc2[a][bp] = make_float2(0.0f, 0.0f);
     issue(0);
     for (int sl = 0; sl < nslab; ++sl) {
         if (sl + 1 < nslab) {
@@ -78,20 +81,36 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t
         }
         __syncthreads();
         const int buf = sl & 1;
-        float xf[4][8];
+        float2 xd[4][8];  // each input twice
 #pragma unroll
-        for (int a = 0; a < 4; ++a) unpack_bf16x8(*reinterpret_cast<const uint4*>(&xs[buf][tg * 4 + a][8 * lane]), xf[a]);
+        for (int a = 0; a < 4; ++a) {
+            float xf[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(&xs[buf][tg * 4 + a][8 * lane]), xf);
 #pragma unroll
-        for (int b = 0; b < 16; ++b) {
-            float wf[8];
-            unpack_bf16x8(*reinterpret_cast<const uint4*>(&ws[buf][eg * 16 + b][8 * lane]), wf);
+            for (int i = 0; i < 8; ++i) xd[a][i] = make_float2(xf[i], xf[i]);
+        }
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
+        for (int bp = 0; bp < 8; ++bp) {
+            float w0[8], w1[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(&ws[buf][eg * 16 + 2 * bp][8 * lane]), w0);
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(&ws[buf][eg * 16 + 2 * bp + 1][8 * lane]), w1);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[a][b] = __fadd_rn(acc[a][b], __fmul_rn(xf[a][i], wf[i]));
+            for (int i = 0; i < 8; ++i) {
+                const float2 w2 = make_float2(w0[i], w1[i]);
+#pragma unroll
+                for (int a = 0; a < 4; ++a) acc2[a][bp] = __fadd2_rn(acc2[a][bp], __fmul2_rn(xd[a][i], w2));
+            }
         }
         __syncthreads();
     }
+    float acc[4][16];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int bp = 0; bp < 8; ++bp) {
+            acc[a][2 * bp] = acc2[a][bp].x;
+            acc[a][2 * bp + 1] = acc2[a][bp].y;
+        }
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
