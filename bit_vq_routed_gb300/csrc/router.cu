@@ -129,8 +129,60 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t
         }
 }
 
-__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
-    return v > bv || (v == bv && e < be);
+// Order-preserving 32-bit key of a logit: a larger logit has a larger key,
+// and equal logits have equal keys (-0 is keyed as +0); NaN and absent or
+// taken entries get key 0, below every other (-inf: 0x007fffff).
+__device__ __forceinline__ unsigned logit_key(float v) {
+    unsigned u = __float_as_uint(v);
+    if (u == 0x80000000u) u = 0u;
+    if ((u & 0x7fffffffu) > 0x7f800000u) return 0u;  // NaN
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(unsigned key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// The k best of a warp's logits in (logit descending, id ascending) order
+// -- equal logits go to the lower id: value i of lane l is expert l + 32 i
+// (absent ones marked in taken).  Each round takes the warp-wide largest key
+// (__reduce_max_sync) and, among the lanes that hold it, the lowest id
+// (__reduce_min_sync); only the lane that owned the winner rescans its
+// values.  Lane j < k ends with the j-th selected logit and id.
+template <int NPER>
+__device__ __forceinline__ void warp_select_topk(const float (&v)[NPER], uint32_t taken, int k, float& sel_v,
+                                                 int& sel_e) {
+    const int lane = threadIdx.x & 31;
+    unsigned key[NPER];
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) key[i] = logit_key(v[i]);
+    unsigned bk = 0;
+    int be = INT_MAX;
+    auto rescan = [&]() {
+        bk = 0;
+        be = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < NPER; ++i)
+            if (!((taken >> i) & 1) && key[i] > bk) {  // (i increasing: the first of equal keys has the lowest id)
+                bk = key[i];
+                be = lane + 32 * i;
+            }
+    };
+    rescan();
+    unsigned sel_k = 0;
+    sel_e = 0;
+    for (int j = 0; j < k; ++j) {
+        const unsigned mk = __reduce_max_sync(FULL, bk);
+        const int we = __reduce_min_sync(FULL, bk == mk ? be : INT_MAX);
+        if (lane == j) {
+            sel_k = mk;
+            sel_e = we;
+        }
+        if ((we & 31) == lane) {
+            taken |= 1u << (we >> 5);
+            rescan();
+        }
+    }
+    sel_v = key_logit(sel_k);
 }
 
 // Small-batch router: one CTA of 8 warps per (RS_TG tokens, 8 experts); the
@@ -228,44 +280,9 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
             taken |= 1u << i;
         }
     }
-    float bv = -INFINITY;
-    int be = INT_MAX;
-    auto rescan = [&]() {
-        bv = -INFINITY;
-        be = INT_MAX;
-#pragma unroll
-        for (int i = 0; i < NPER; ++i) {
-            const int e = lane + 32 * i;
-            if (!((taken >> i) & 1) && better(v[i], e, bv, be)) {
-                bv = v[i];
-                be = e;
-            }
-        }
-    };
-    rescan();
-    float sel_v = 0.0f;  // lane j keeps the j-th selected logit
-    int sel_e = 0;
-    for (int j = 0; j < k; ++j) {
-        float wv = bv;
-        int we = be;
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            const float ov = __shfl_xor_sync(FULL, wv, off);
-            const int oe = __shfl_xor_sync(FULL, we, off);
-            if (better(ov, oe, wv, we)) {
-                wv = ov;
-                we = oe;
-            }
-        }
-        if (lane == j) {
-            sel_v = wv;
-            sel_e = we;
-        }
-        if ((we & 31) == lane) {
-            taken |= 1u << (we >> 5);
-            rescan();
-        }
-    }
+    float sel_v;  // lane j keeps the j-th selected logit and its id
+    int sel_e;
+    warp_select_topk<NPER>(v, taken, k, sel_v, sel_e);
     const float top = __shfl_sync(FULL, sel_v, 0);
     const float num = lane < k ? expf(sel_v - top) : 0.0f;
     float den = 0.0f;
@@ -307,44 +324,9 @@ __device__ __forceinline__ void route_one_token(LogitOf logit_of, int E, int k, 
             taken |= 1u << i;
         }
     }
-    float bv = -INFINITY;
-    int be = INT_MAX;
-    auto rescan = [&]() {
-        bv = -INFINITY;
-        be = INT_MAX;
-#pragma unroll
-        for (int i = 0; i < NPER; ++i) {
-            const int ee = lane + 32 * i;
-            if (!((taken >> i) & 1) && better(v[i], ee, bv, be)) {
-                bv = v[i];
-                be = ee;
-            }
-        }
-    };
-    rescan();
-    float sel_v = 0.0f;
-    int sel_e = 0;
-    for (int j = 0; j < k; ++j) {
-        float wv2 = bv;
-        int we = be;
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            const float ov = __shfl_xor_sync(FULL, wv2, off);
-            const int oe = __shfl_xor_sync(FULL, we, off);
-            if (better(ov, oe, wv2, we)) {
-                wv2 = ov;
-                we = oe;
-            }
-        }
-        if (lane == j) {
-            sel_v = wv2;
-            sel_e = we;
-        }
-        if ((we & 31) == lane) {
-            taken |= 1u << (we >> 5);
-            rescan();
-        }
-    }
+    float sel_v;  // lane j keeps the j-th selected logit and its id
+    int sel_e;
+    warp_select_topk<NPER>(v, taken, k, sel_v, sel_e);
     const float top = __shfl_sync(FULL, sel_v, 0);
     const float num = lane < k ? expf(sel_v - top) : 0.0f;
     float den = 0.0f;
@@ -484,44 +466,9 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const uint16_t* __rest
                 taken |= 1u << i;
             }
         }
-        float bv = -INFINITY;
-        int be = INT_MAX;
-        auto rescan = [&]() {
-            bv = -INFINITY;
-            be = INT_MAX;
-#pragma unroll
-            for (int i = 0; i < NPER; ++i) {
-                const int ee = lane + 32 * i;
-                if (!((taken >> i) & 1) && better(v[i], ee, bv, be)) {
-                    bv = v[i];
-                    be = ee;
-                }
-            }
-        };
-        rescan();
-        float sel_v = 0.0f;
-        int sel_e = 0;
-        for (int j = 0; j < k; ++j) {
-            float wv2 = bv;
-            int we = be;
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                const float ov = __shfl_xor_sync(FULL, wv2, off);
-                const int oe = __shfl_xor_sync(FULL, we, off);
-                if (better(ov, oe, wv2, we)) {
-                    wv2 = ov;
-                    we = oe;
-                }
-            }
-            if (lane == j) {
-                sel_v = wv2;
-                sel_e = we;
-            }
-            if ((we & 31) == lane) {
-                taken |= 1u << (we >> 5);
-                rescan();
-            }
-        }
+        float sel_v;  // lane j keeps the j-th selected logit and its id
+        int sel_e;
+        warp_select_topk<NPER>(v, taken, k, sel_v, sel_e);
         const float top = __shfl_sync(FULL, sel_v, 0);
         const float num = lane < k ? expf(sel_v - top) : 0.0f;
         float den = 0.0f;
