@@ -178,17 +178,18 @@ __global__ void __maxnreg__(MAX_REG)
         }
     };
     int pre_kr = -1;
-    // SELF FC1: the slot descriptors do not depend on the kernel before this one
+    // SELF: the slot descriptors do not depend on the kernel before this one
     // (only the slot-table writer changes them, and it lets no dependent start
     // before it has finished), so they are staged in the code slots, after the
     // expert offsets, before the wait: the pair listing then needs one round
     // trip to global memory instead of two.
     // (The descriptor words are loaded into registers first, so that their
-    // round trip overlaps the activations'.)
+    // round trip overlaps the activations' (FC1) or the expert offsets' (FC2,
+    // whose offsets are two kernels back, so complete).)
     constexpr int DW = 4;  // descriptor words per thread at most
     const int n_dw = E * (int)(sizeof(SlotDesc) / 8);
     const size_t off_bytes = ((size_t)4 * (E + 1) + 15) & ~(size_t)15;
-    const bool desc_staged = SELF && FC1 && n_dw <= DW * THREADS &&
+    const bool desc_staged = SELF && n_dw <= DW * THREADS &&
                              off_bytes + sizeof(SlotDesc) * E <= (size_t)LOW_SLOTS * SLOT_BYTES;
     SlotDesc* s_desc = reinterpret_cast<SlotDesc*>(dyn + (low_base - base) + off_bytes);
     unsigned long long dv[DW];
@@ -197,6 +198,13 @@ __global__ void __maxnreg__(MAX_REG)
 #pragma unroll
         for (int r = 0; r < DW; ++r)
             if (tid + r * THREADS < n_dw) dv[r] = src[tid + r * THREADS];
+    }
+    constexpr int OW = 3;  // offsets per thread at most (E + 1 <= 1025)
+    int ov[OW];
+    if (SELF && !FC1) {
+#pragma unroll
+        for (int r = 0; r < OW; ++r)
+            if (tid + r * THREADS <= E) ov[r] = __ldcg(offsets + tid + r * THREADS);
     }
     if (SELF && FC1 && KR <= C) {
         pre_kr = (int)(((long long)(blockIdx.x + 1) * KR - 1) / C);
@@ -223,7 +231,13 @@ __global__ void __maxnreg__(MAX_REG)
         }
         // the offsets are staged in the (still unused) code slots below the table
         int* s_off = reinterpret_cast<int*>(dyn + (low_base - base));
-        for (int i = tid; i <= E; i += THREADS) s_off[i] = FC1 ? offsets[i] : __ldcg(offsets + i);
+        if (FC1) {
+            for (int i = tid; i <= E; i += THREADS) s_off[i] = offsets[i];
+        } else {
+#pragma unroll
+            for (int r = 0; r < OW; ++r)
+                if (tid + r * THREADS <= E) s_off[tid + r * THREADS] = ov[r];
+        }
         if (tid < MAX_GROUP) S.e_of_s[tid] = -1;
         __syncthreads();
         for (int e = tid; e < E; e += THREADS)  // the expert of each sorted position < P
