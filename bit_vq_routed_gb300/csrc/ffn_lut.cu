@@ -132,9 +132,11 @@ __global__ void __maxnreg__(MAX_REG)
         if (U == 0) {
             u0 = u1 = 0;
         } else if (J <= C) {
-            const int jb = (int)(((long long)(blockIdx.x + 1) * J - 1) / C);  // a0(jb) <= i < a0(jb + 1)
-            const int a0 = lut_cta_of((long long)jb * job_units, C, U);
-            const int a1 = lut_cta_of((long long)(jb + 1) * job_units, C, U);
+            // equal jobs: a0(j) = floor(C start(j) / U) = floor(C j / J), all
+            // in 32-bit arithmetic (J <= C <= 1024)
+            const int jb = ((int)(blockIdx.x + 1) * J - 1) / C;  // a0(jb) <= i < a0(jb + 1)
+            const int a0 = C * jb / J;
+            const int a1 = C * (jb + 1) / J;
             u0 = jb * job_units;
             u1 = u0 + job_units;
             s_off0 = blockIdx.x - a0;
