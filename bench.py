@@ -47,13 +47,13 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM bytes (read + write) of one expert-FFN call, from one ncu capture of its
 # kernels (the two single-token table kernels, ffn_lut_kernel<1,1,0> and
 # ffn_lut_kernel<0,1,0>, of `python bench.py --layers 1 --steps 3 --warmup 3
-# --no-cpu` under ncu: FC1 35,727,616 + 3,584, FC2 18,540,544 at decode batch 1).
+# --no-cpu` under ncu: FC1 35,726,848 + 2,304, FC2 18,552,320 at decode batch 1).
 # Reported only while the kernel sources hash to the ones the counters were
 # taken on.
-TRAFFIC = {"decode_b1": {"bytes": 54_271_744,
+TRAFFIC = {"decode_b1": {"bytes": 54_281_472,
                          "profile": "ncu capture of ffn_lut_kernel<1,1,0> and ffn_lut_kernel<0,1,0>, decode batch 1",
                          "sources": ["ffn_lut.cu", "lut_core.cuh", "ffn_common.cuh", "common.cuh"],
-                         "sha256": "96072346d4bdf9fc2afb2b3bef51625cb9e3204e4a517e2c2b8442a399f094e5"}}
+                         "sha256": "806278a28930a9fc01b8041ec15426dc993a12252029255c8096f12b522dd4a8"}}
 
 
 # Workloads whose bench figure averages many token batches (different expert
