@@ -53,7 +53,7 @@ L2_BYTES = 129 * 2 ** 20
 TRAFFIC = {"decode_b1": {"bytes": 54_281_472,
                          "profile": "ncu capture of ffn_lut_kernel<1,1,0> and ffn_lut_kernel<0,1,0>, decode batch 1",
                          "sources": ["ffn_lut.cu", "lut_core.cuh", "ffn_common.cuh", "common.cuh"],
-                         "sha256": "806278a28930a9fc01b8041ec15426dc993a12252029255c8096f12b522dd4a8"}}
+                         "sha256": "5e14b01205d93a9282c2c42ab352d0ea162bb8cc35829b4efc5cf24ea575303c"}}
 
 
 # Workloads whose bench figure averages many token batches (different expert

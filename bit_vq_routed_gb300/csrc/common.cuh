@@ -221,7 +221,9 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
 // calls pdl_wait() before it touches memory an earlier kernel may write or
 // read, and pdl_launch_dependents() right after it -- except a kernel that
 // writes a bf16 activation output (the combine's out_bf16), which lets its
-// dependents start only when it has finished.  So when a kernel starts, its
+// dependents start only when it has finished, and the e2m1 table kernels,
+// which touch only what is complete two launches back (or their own
+// results) and call pdl_wait() just before they exit.  So when a kernel starts, its
 // predecessor has at least passed its own wait, i.e. everything two launches
 // back is complete, and so are the bf16 activations the caller passes in (x):
 // no library kernel that may still be running writes them.  The slot-table
