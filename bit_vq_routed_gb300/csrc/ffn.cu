@@ -322,8 +322,10 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     if (T == 1 && t->n_fp4 == 0) {
         // one token, VQ2 experts only: every pair takes the table path and the
         // two table kernels list the pairs themselves (no schedule kernel)
-        if ((st = launch_lut_fc(true, true, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s)) !=
-            MOE_OK)
+        // (FC1 gets the combine outputs too: it zeroes FC2's counters only
+        // where FC2 will use them)
+        if ((st = launch_lut_fc(true, true, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s,
+                                pair_to_sorted, comb32, comb16)) != MOE_OK)
             return st;
         return launch_lut_fc(false, true, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w, L, s,
                              pair_to_sorted, comb32, comb16);

@@ -171,7 +171,8 @@ __global__ void __maxnreg__(MAX_REG)
     // sums straight into the zeroed output row (fp32 addition is commutative,
     // so 0 + p0 + p1 does not depend on the order) instead of a finishing
     // step; FC1 zeroes the rows of the table pairs.
-    const bool fc2_adds = !F4 && mode == MOE_PER_PAIR && lut_jobs(I) == 2;
+    const int KR2 = lut_jobs(I);  // FC2's K-ranges (VQ2)
+    const bool fc2_adds = !F4 && mode == MOE_PER_PAIR && KR2 == 2;
     auto zero_rows = [&](auto row_of) {
         const int n4 = H / 4;  // (n_lut <= E <= 1024 table pairs)
         for (int i = blockIdx.x * THREADS + tid; i < n_lut * n4; i += C * THREADS) {
@@ -271,9 +272,17 @@ __global__ void __maxnreg__(MAX_REG)
         n_lut = S.n_self;
         uniform_range(FC1 ? KR : n_lut * KR, FC1 ? n_lut * RT : RT);
         if (FC1) {
-            const int nc = n_lut * (H / 16);
-            for (int i = blockIdx.x * THREADS + tid; i < nc; i += C * THREADS) cnt[i] = 0;
-            for (int i = blockIdx.x * THREADS + tid; i < H / 16; i += C * THREADS) cnt2[i] = 0;
+            // FC2's arrival counters start at zero where FC2 uses them (it
+            // leaves them at zero): per row tile when it adds K-range
+            // partials through them, per output tile when it combines.  FC1
+            // gets FC2's combine outputs only to know that.
+            const bool fc2_combines = comb32 != nullptr || comb16 != nullptr;
+            if (fc2_combines || (KR2 > 1 && !fc2_adds)) {
+                const int nc = n_lut * (H / 16);
+                for (int i = blockIdx.x * THREADS + tid; i < nc; i += C * THREADS) cnt[i] = 0;
+            }
+            if (fc2_combines)
+                for (int i = blockIdx.x * THREADS + tid; i < H / 16; i += C * THREADS) cnt2[i] = 0;
             if (fc2_adds) zero_rows([&](int p) { return S.all_ys[p]; });
         }
     } else if (FC1) {
