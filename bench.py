@@ -47,13 +47,13 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM bytes (read + write) of one expert-FFN call, from one ncu capture of its
 # kernels (the two single-token table kernels, ffn_lut_kernel<1,1,0> and
 # ffn_lut_kernel<0,1,0>, of `python bench.py --layers 1 --steps 3 --warmup 3
-# --no-cpu` under ncu: FC1 35,726,848 + 2,304, FC2 18,552,320 at decode batch 1).
+# --no-cpu` under ncu: FC1 35,730,176 + 5,376, FC2 18,554,112 at decode batch 1).
 # Reported only while the kernel sources hash to the ones the counters were
 # taken on.
-TRAFFIC = {"decode_b1": {"bytes": 54_281_472,
+TRAFFIC = {"decode_b1": {"bytes": 54_289_664,
                          "profile": "ncu capture of ffn_lut_kernel<1,1,0> and ffn_lut_kernel<0,1,0>, decode batch 1",
                          "sources": ["ffn_lut.cu", "lut_core.cuh", "ffn_common.cuh", "common.cuh"],
-                         "sha256": "5e14b01205d93a9282c2c42ab352d0ea162bb8cc35829b4efc5cf24ea575303c"}}
+                         "sha256": "e43b3ce42a7b8caeb0b8918996863786ad50fc4d981f7a97e8914ee8bf2e9326"}}
 
 
 # Workloads whose bench figure averages many token batches (different expert
