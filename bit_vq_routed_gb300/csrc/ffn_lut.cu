@@ -62,7 +62,8 @@ static_assert(0x400 + ((sizeof(Smem) + 127) / 128 * 128) + LOW_SLOTS * SLOT_BYTE
 // SELF: a single-token call whose experts are all VQ2 (no schedule kernel):
 // the kernel lists the call's pairs itself from the expert offsets and the
 // slot table (one token group; pairs in sorted order, non-resident ones
-// reported and skipped).
+// reported and skipped).  comb32 / comb16 (SELF): FC2 also writes the combine
+// of the pairs; FC1 gets them only to know which of FC2's counters to zero.
 // F4: the FP4 experts of a single-token call (e2m1 tables over K-ranges of
 // 512 inputs; the schedule's second record list, one token group; never
 // SELF).  These kernels read only what the schedule and the kernels before
