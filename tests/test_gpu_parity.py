@@ -51,7 +51,8 @@ def test_ragged_and_degenerate_shapes(torch, T, E, k):
 
 
 @pytest.mark.parametrize("H,I,T,E,k", [(512, 256, 1, 16, 4), (1024, 640, 2, 64, 8), (1536, 384, 3, 32, 6),
-                                        (4096, 2048, 1, 16, 8), (768, 128, 5, 128, 3)])
+                                        (4096, 2048, 1, 16, 8), (768, 128, 5, 128, 3),
+                                        (256, 128, 1, 1024, 32), (512, 256, 2, 64, 32)])  # the largest E and k
 def test_single_token_experts_table_path(torch, H, I, T, E, k):
     # experts that get one token go through the activation-table kernels;
     # K-ranges of 1-4 scale blocks (H, I not multiples of 512) included
