@@ -62,7 +62,7 @@ def test_single_token_experts_table_path(torch, H, I, T, E, k):
 
 @pytest.mark.parametrize("H,I,E,k,fp4_top", [(512, 256, 16, 4, 16), (1280, 384, 64, 8, 64), (768, 640, 128, 3, 128),
                                               (4096, 2048, 256, 8, 52), (1024, 384, 32, 4, 16), (256, 128, 4, 2, 4),
-                                              (512, 256, 8, 1, 8)])
+                                              (512, 256, 8, 1, 8), (512, 256, 64, 32, 64)])  # (last: 32 pairs, one group)
 def test_fp4_experts_single_token_e2m1_table_path(torch, H, I, E, k, fp4_top):
     # in single-token calls FP4 experts go through the e2m1 table kernels;
     # K-ranges of 2 to 8 tiles of 64 inputs (H, I not multiples of 512)
