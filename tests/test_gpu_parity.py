@@ -78,6 +78,25 @@ def test_fp4_experts_single_token_non_resident_reported(torch):
     _check_layer(spec, 1, seed=17, resident=res)
 
 
+@pytest.mark.parametrize("fp4_top", [0, 16])
+def test_single_token_no_resident_expert(torch, fp4_top):
+    # a single-token call whose routed experts are all missing (VQ2-only
+    # table: the self-scheduling table kernels; with FP4 experts: the
+    # schedule and the e2m1 kernels): every pair reported, output zero
+    spec = ms.LayerSpec(H=512, I=256, E=16, k=4, seed=23, fp4_top=fp4_top)
+    layer = ms.Layer(spec)
+    x = ms.tokens(1, spec.H, seed=23)
+    routed = set(O.moe_layer(layer, x)["ids"].ravel().tolist())
+    # with FP4 experts, one FP4 expert the token does not route to is resident
+    # (the table then holds FP4 experts, which selects the schedule path)
+    keep_ids = [e for e in range(spec.E) if e not in routed][:1] if fp4_top else []
+    dev, keep = device_layer(layer, 1, np.array(keep_ids, np.int64))
+    g = run(dev, x)
+    assert (g["status"] == 0).all()
+    assert (g["out"] == 0).all()
+    assert device_error_word(dev) == 0
+
+
 def test_fp4_table_pairs_fused_scatter_matches_per_pair(torch):
     import bit_vq_routed_gb300 as bv
     spec = ms.LayerSpec(H=1280, I=640, E=64, k=8, seed=31, fp4_top=64)
