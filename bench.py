@@ -53,7 +53,7 @@ L2_BYTES = 129 * 2 ** 20
 TRAFFIC = {"decode_b1": {"bytes": 54_289_664,
                          "profile": "ncu capture of ffn_lut_kernel<1,1,0> and ffn_lut_kernel<0,1,0>, decode batch 1",
                          "sources": ["ffn_lut.cu", "lut_core.cuh", "ffn_common.cuh", "common.cuh"],
-                         "sha256": "e85f100fab77bc256d53658bb78f8ab136e27763c2f2564aa71f19ca240a39f9"}}
+                         "sha256": "0b338d3b4c66ace46e4d7280241e02552a11ca0eeeb7e2b8a06365b8af983b70"}}
 
 
 # Workloads whose bench figure averages many token batches (different expert

@@ -51,7 +51,8 @@ constexpr int MAX_TP = LUT_MAX_M * 1024;  // table pairs at most (E <= 1024)
 constexpr size_t SCHED_SMEM = sizeof(int) * (1025 + (MAX_TP + 1) + 4 * MAX_TP + SP_SMEM) + 1024;
 
 // One CTA of 1024 threads.  Expert e with m_e pairs, if resident:
-//   VQ2 with m_e <= LUT_MAX_M (and use_lut) -> m_e activation-table pairs
+//   VQ2 with m_e <= lut_max_m (LUT_MAX_M, or LUT_MAX_M_LARGE in large calls)
+//     -> m_e activation-table pairs
 //     (one per token: the expert's codes are streamed once per token, which
 //     costs less than the mma.sync decode at such counts);
 //   FP4 with m_e == 1 (and use_lut4, single-token calls) -> one e2m1 table
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
                                                         const int32_t* __restrict__ sorted_pair, int P, int k,
                                                         uint8_t* __restrict__ status, int* __restrict__ header,
                                                         Chunk* __restrict__ chunks, LutRec* __restrict__ recs,
-                                                        int32_t* __restrict__ grp_start, int use_lut,
+                                                        int32_t* __restrict__ grp_start, int lut_max_m,
                                                         Chunk* __restrict__ uchunks, int use_umma, int H, int I,
                                                         int C, int4* __restrict__ fc1_range, int split16,
                                                         LutRec* __restrict__ recs4, int use_lut4) {
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
 
     const int m = tid < E ? s_off[tid + 1] - s_off[tid] : 0;
     const bool res = tid < E && d.resident != 0 && m > 0;
-    const bool lut = res && use_lut && m <= LUT_MAX_M && d.format == MOE_FMT_VQ2;
+    const bool lut = res && m <= lut_max_m && d.format == MOE_FMT_VQ2;
     const int nl = lut ? m : 0;  // this expert's table pairs
     const bool um = res && use_umma && m >= UMMA_MIN && d.format == MOE_FMT_VQ2;
     const bool fp4 = d.format == MOE_FMT_FP4;
@@ -304,7 +305,9 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     LutRec* recs = reinterpret_cast<LutRec*>(w + L.rec_off);
     int32_t* grp_start = reinterpret_cast<int32_t*>(w + L.grp_start_off);
     Chunk* uchunks = reinterpret_cast<Chunk*>(w + L.uchunks_off);
-    const int use_lut = 1;
+    // VQ2 experts with at most lut_max_m tokens take the table kernels
+    const int lut_max_m = T >= MMA_SPLIT_T ? LUT_MAX_M_LARGE : LUT_MAX_M;
+    const bool use_lut = lut_max_m > 0;
     // An expert gets at most T of the pairs: at T == UMMA_MIN only an expert
     // routed by every token would qualify, and the 32-token mma.sync chunk
     // serves it as well, so the tcgen05 launches start above that (at
@@ -333,7 +336,7 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     cudaError_t e = ensure_smem_attr(schedule_kernel, (int)SCHED_SMEM);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule shared memory");
     e = launch_pdl(schedule_kernel, dim3(1), dim3(1024), SCHED_SMEM, s, (const SlotDesc*)t->d_desc, E, offsets,
-                               sorted_pair, P, k, status, header, chunks, recs, grp_start, use_lut,
+                               sorted_pair, P, k, status, header, chunks, recs, grp_start, lut_max_m,
                                uchunks, use_umma, H, I, num_sms(), reinterpret_cast<int4*>(w + L.range_off), split16,
                                reinterpret_cast<LutRec*>(w + L.rec4_off), use_lut4 ? 1 : 0);
     if (e != cudaSuccess) return cuda_status(e, "moe_vq2_expert_ffn: schedule launch");

@@ -21,6 +21,11 @@ constexpr int UMMA_MIN = 32;   // tokens from which an expert takes the tcgen05 
 constexpr int UMMA_NT = 256;   // tokens per tcgen05 chunk
 constexpr int MAX_LUT_CTAS = 1024;  // grid of the activation-table kernels (one CTA per SM) at most
 constexpr int LUT_MAX_M = 3;   // VQ2 experts with up to this many tokens take the activation-table path
+// The same in calls of at least MMA_SPLIT_T tokens, where the mma.sync
+// kernels run anyway (measured, prefill of 4096 tokens, ms per call: up to 3
+// tokens 2.319, 2 tokens 2.312, 1 token 2.291-2.300, none 2.379).
+constexpr int LUT_MAX_M_LARGE = 1;
+static_assert(LUT_MAX_M_LARGE <= LUT_MAX_M, "the schedule's table-pair arrays are sized by LUT_MAX_M");
 // In calls of at most LUT4_MAX_T tokens, FP4 experts with one token take the
 // e2m1 activation-table path.  Measured with 52 of 256 experts FP4
 // (expert-FFN call, us, e2m1 path / mma.sync path): 1 token 50.0 / 100.0;
