@@ -4,8 +4,8 @@
 // its token count m_e:
 //   - VQ2, m_e <= LUT_MAX_M: the activation-table kernels (ffn_lut.cu), one
 //     table pair per token;
-//   - FP4 in single-token calls (m_e == 1, calls of at most LUT4_MAX_T
-//     tokens): the e2m1 activation-table kernels (ffn_lut.cu);
+//   - FP4 in calls of at most LUT4_MAX_T tokens: the e2m1 activation-table
+//     kernels (ffn_lut.cu), one table pair per token;
 //   - VQ2, m_e >= 32: the tcgen05 kernels (ffn_umma.cu);
 //   - otherwise: the mma.sync kernels (ffn_mma.cu), chunks of <= 32 (VQ2) or
 //     <= 16 (FP4) tokens.
@@ -55,8 +55,8 @@ constexpr size_t SCHED_SMEM = sizeof(int) * (1025 + (MAX_TP + 1) + 4 * MAX_TP + 
 //     -> m_e activation-table pairs
 //     (one per token: the expert's codes are streamed once per token, which
 //     costs less than the mma.sync decode at such counts);
-//   FP4 with m_e == 1 (and use_lut4, single-token calls) -> one e2m1 table
-//     pair (listed in expert order, all in one token group);
+//   FP4 (and use_lut4: calls of at most LUT4_MAX_T tokens) -> m_e e2m1 table
+//     pairs, one per token (grouped by token, in expert order in a group);
 //   VQ2 with m_e >= UMMA_MIN (and use_umma) -> ceil(m_e / UMMA_NT) tcgen05 chunks;
 //   otherwise -> mma.sync chunks of MMA_NT_VQ2 (VQ2) or MMA_NT_FP4 (FP4,
 //     and with split16 VQ2 experts of at most MMA_NT_FP4 tokens) tokens; the
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
     const int nl = lut ? m : 0;  // this expert's table pairs
     const bool um = res && use_umma && m >= UMMA_MIN && d.format == MOE_FMT_VQ2;
     const bool fp4 = d.format == MOE_FMT_FP4;
-    const bool lut4 = res && use_lut4 && m == 1 && fp4;
+    const bool lut4 = res && use_lut4 && m <= LUT4_MAX_T && fp4;  // (m <= T <= LUT4_MAX_T)
     const bool part2 = fp4 || (split16 && m <= MMA_NT_FP4);  // the 16-token configuration
     const int nt_e = part2 ? MMA_NT_FP4 : MMA_NT_VQ2;  // tokens per mma.sync chunk of this expert
     const int n = (res && !lut && !um && !lut4) ? (m + nt_e - 1) / nt_e : 0;
@@ -116,27 +116,40 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
     const unsigned long long ex =
         block_scan64((unsigned long long)(part2 ? 0 : n) | ((unsigned long long)nu << 21) | ((unsigned long long)nl << 42),
                      warp_tot, &tot);
-    // the 16-token chunks, listed after the others, and the e2m1 table pairs
+    // the 16-token chunks, listed after the others
     unsigned long long tot4;
-    const unsigned long long ex4 = block_scan64((part2 ? (unsigned long long)n : 0ull) | ((unsigned long long)lut4 << 21),
-                                                warp_tot, &tot4);
+    const unsigned long long ex4 = block_scan64(part2 ? (unsigned long long)n : 0ull, warp_tot, &tot4);
+    // the e2m1 table pairs, grouped by token (tokens 0..T-1, T <= 3): field t
+    // (21 bits) counts the experts with a pair of token t
+    static_assert(LUT4_MAX_T <= 3, "three 21-bit token fields");
+    unsigned long long has4 = 0;
+    if (lut4)
+        for (int q = 0; q < m; ++q) has4 |= 1ull << (21 * (sp_at(s_off[tid] + q) / k));
+    unsigned long long tot_t;
+    const unsigned long long ex_t = block_scan64(has4, warp_tot, &tot_t);
     const int n_vq2 = (int)(tot & 0x1fffff);
     const int cbase = part2 ? n_vq2 + (int)(ex4 & 0x1fffff) : (int)(ex & 0x1fffff), ubase = (int)((ex >> 21) & 0x1fffff);
-    const int n_chunks = n_vq2 + (int)(tot4 & 0x1fffff), n_umma = (int)((tot >> 21) & 0x1fffff), n_lut = (int)(tot >> 42);
-    const int n_lut4 = (int)(tot4 >> 21);
+    const int n_chunks = n_vq2 + (int)tot4, n_umma = (int)((tot >> 21) & 0x1fffff), n_lut = (int)(tot >> 42);
+    const int g40 = (int)(tot_t & 0x1fffff), g41 = (int)((tot_t >> 21) & 0x1fffff), g42 = (int)(tot_t >> 42);
+    const int n_lut4 = g40 + g41 + g42;
+    const int n_groups4 = (g40 > 0) + (g41 > 0) + (g42 > 0);
     if (lut4) {
-        LutRec r;
-        for (int mtx = 0; mtx < 3; ++mtx) {
-            r.codes[mtx] = d.codes[mtx];
-            r.scales[mtx] = d.scales[mtx];
+        // the pair of token t: after the groups of tokens below t, in expert
+        // order; a token's pairs form one group (they share each FC1 table)
+        for (int q = 0; q < m; ++q) {
+            const int sp = s_off[tid] + q, t = sp_at(sp) / k;
+            const int gs = (t > 0 ? g40 : 0) + (t > 1 ? g41 : 0);
+            LutRec r;
+            for (int mtx = 0; mtx < 3; ++mtx) {
+                r.codes[mtx] = d.codes[mtx];
+                r.scales[mtx] = d.scales[mtx];
+            }
+            r.sorted = sp;
+            r.token = t;
+            r.gs = gs;
+            r.gc = t == 0 ? g40 : t == 1 ? g41 : g42;
+            recs4[gs + (int)((ex_t >> (21 * t)) & 0x1fffff)] = r;
         }
-        r.sorted = s_off[tid];
-        r.token = sp_at(s_off[tid]) / k;
-        // one token: its e2m1 pairs form one group (they share each FC1 table)
-        static_assert(LUT4_MAX_T == 1, "e2m1 pairs of one token");
-        r.gs = 0;
-        r.gc = n_lut4;
-        recs4[(int)(ex4 >> 21)] = r;
     }
     for (int c = 0; c < n; ++c) {
         Chunk ch;
@@ -257,6 +270,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const SlotDesc* __restri
         header[HDR_NUMMA] = n_umma;
         header[HDR_NVQ2] = n_vq2;
         header[HDR_NLUT4] = n_lut4;
+        header[HDR_NGROUPS4] = n_groups4;
     }
     // eight positions per thread at a time: their sorted_pair loads (beyond
     // the staged part) are in flight together
@@ -313,12 +327,13 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     // serves it as well, so the tcgen05 launches start above that (at
     // batch 32 they found work in one batch of eight and cost two launches).
     const int use_umma = T > UMMA_MIN ? 1 : 0;
-    // FP4 experts with one token take the e2m1 table kernels in single-token
-    // calls.
+    // FP4 experts take the e2m1 table kernels in calls of at most LUT4_MAX_T
+    // tokens.
     const bool use_lut4 = T <= LUT4_MAX_T && t->n_fp4 > 0;
-    // With one token no expert gets two pairs, so the mma.sync kernels only
-    // have work if FP4 experts do not take the table path.
-    const bool mma = T > 1 || (t->n_fp4 > 0 && !use_lut4) || !use_lut;
+    // In calls of at most lut_max_m tokens no expert gets more pairs than the
+    // table path takes, so the mma.sync kernels only have work if FP4
+    // experts do not take the e2m1 tables.
+    const bool mma = T > lut_max_m || (t->n_fp4 > 0 && !use_lut4);
     const int split16 = T >= MMA_SPLIT_T ? 1 : 0;
 
     moe_status st;

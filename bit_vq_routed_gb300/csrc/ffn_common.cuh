@@ -26,16 +26,14 @@ constexpr int LUT_MAX_M = 3;   // VQ2 experts with up to this many tokens take t
 // tokens 2.319, 2 tokens 2.312, 1 token 2.291-2.300, none 2.379).
 constexpr int LUT_MAX_M_LARGE = 1;
 static_assert(LUT_MAX_M_LARGE <= LUT_MAX_M, "the schedule's table-pair arrays are sized by LUT_MAX_M");
-// In calls of at most LUT4_MAX_T tokens, FP4 experts with one token take the
-// e2m1 activation-table path.  Measured with 52 of 256 experts FP4
-// (expert-FFN call, us, e2m1 path / mma.sync path): 1 token 50.0 / 100.0;
-// with a first build of the e2m1 kernels (one table per pair) 2 tokens
-// 136.3 / 112.9, 4 tokens 158.6 / 129.3, 8 tokens 176.8 / 174.2.  With one
-// token every FP4 expert takes it and the call needs no mma.sync, gather or
-// conversion kernel; with more, the mma.sync kernels still run for the FP4
-// experts with several tokens and take about as long for a few experts as
-// for all of them.
-constexpr int LUT4_MAX_T = 1;
+// In calls of at most LUT4_MAX_T tokens the FP4 experts take the e2m1
+// activation-table path, one table pair per token.  Measured with 52 of 256
+// experts FP4 (expert-FFN call, us, e2m1 path / mma.sync path): 1 token
+// 50.0 / 100.0, 2 tokens 87.7 / 112.9, 3 tokens 124.0 / 116.0.  Then no
+// mma.sync, gather or conversion kernel is launched (every expert takes a
+// table); from three tokens on, the FP4 experts with several tokens cost
+// less on mma.sync than streamed once per token.
+constexpr int LUT4_MAX_T = 2;
 
 // A run of sorted positions of one expert (tensor-core paths).
 struct Chunk {
@@ -55,8 +53,11 @@ static_assert(sizeof(LutRec) == 64 && offsetof(LutRec, codes) == 0 && offsetof(L
 // Header words at the start of the workspace.
 // HDR_NVQ2: the chunks list holds the 32-token chunks first (HDR_NVQ2 of
 // them), then the 16-token ones (FP4, and small VQ2 experts in large calls).
-// HDR_NLUT4: the e2m1 table pairs (rec4).
-enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NUMMA = 4, HDR_NVQ2 = 5, HDR_NLUT4 = 6 };
+// HDR_NLUT4, HDR_NGROUPS4: the e2m1 table pairs (rec4) and their token groups.
+enum : int {
+    HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NUMMA = 4, HDR_NVQ2 = 5, HDR_NLUT4 = 6,
+    HDR_NGROUPS4 = 7
+};
 
 // Activation-table pairs (VQ2 experts with at most LUT_MAX_M tokens, one pair
 // per token) are listed sorted by (token, expert) in lut_rec, grouped by
@@ -73,8 +74,8 @@ enum : int { HDR_NCHUNKS = 0, HDR_NLUT = 1, HDR_ERR = 2, HDR_NGROUPS = 3, HDR_NU
 // so neither overflows fp16 whatever the range of the activations; the FC1
 // epilogues write a in fp32 (a32) and flag the sorted positions they wrote
 // (amax), from which the conversion kernel makes a16.
-// The e2m1 table pairs (FP4 experts with one token, calls of at most
-// LUT4_MAX_T tokens) have their own records (rec4, one token group),
+// The e2m1 table pairs (FP4 experts in calls of at most LUT4_MAX_T tokens,
+// one pair per token) have their own records (rec4, grouped by token),
 // partial sums (p1_4, p2_4) and FC2 arrival counters (cnt4).
 struct WsLayout {
     size_t chunks_off, rec_off, grp_start_off, p1_off, p2_off, cnt_off, cnt2_off, range_off;
@@ -120,7 +121,7 @@ __host__ __device__ inline WsLayout ws_layout(int T, int k, int E, int H, int I)
     o = ws_align(o + sizeof(int32_t) * (size_t)(H / 16));
     L.range_off = o;
     o = ws_align(o + sizeof(int4) * (size_t)MAX_LUT_CTAS);
-    L.max_lut4 = T <= LUT4_MAX_T ? (int)(P < (long long)E ? P : (long long)E) : 0;
+    L.max_lut4 = T <= LUT4_MAX_T ? (int)P : 0;  // (one pair per (token, expert) at most)
     L.rec4_off = o;
     o = ws_align(o + sizeof(LutRec) * (size_t)L.max_lut4);
     L.p1_4_off = o;

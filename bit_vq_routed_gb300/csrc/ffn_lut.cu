@@ -64,9 +64,9 @@ static_assert(0x400 + ((sizeof(Smem) + 127) / 128 * 128) + LOW_SLOTS * SLOT_BYTE
 // slot table (one token group; pairs in sorted order, non-resident ones
 // reported and skipped).  comb32 / comb16 (SELF): FC2 also writes the combine
 // of the pairs; FC1 gets them only to know which of FC2's counters to zero.
-// F4: the FP4 experts of a single-token call (e2m1 tables over K-ranges of
-// 512 inputs; the schedule's second record list, one token group; never
-// SELF).  These kernels read only what the schedule and the kernels before
+// F4: the FP4 experts of calls of at most LUT4_MAX_T tokens (e2m1 tables
+// over K-ranges of 512 inputs; the schedule's second record list, grouped by
+// token; never SELF).  These kernels read only what the schedule and the kernels before
 // their predecessor wrote (FC2: the e2m1 FC1's partial sums), which is
 // complete when they start, because the predecessor lets its dependents
 // start only after its own wait.  So they run beside their predecessor's
@@ -292,7 +292,13 @@ __global__ void __maxnreg__(MAX_REG)
         pdl_launch_dependents();
         if (F4) {
             n_lut = __ldcg(header + HDR_NLUT4);
-            uniform_range(KR, n_lut * RT);  // one token group
+            if (__ldcg(header + HDR_NGROUPS4) <= 1) {
+                uniform_range(KR, n_lut * RT);  // one token group
+            } else {  // groups of unequal size: a contiguous share of the units
+                const int U = n_lut * KR * RT;
+                u0 = (int)((long long)U * blockIdx.x / C);
+                u1 = (int)((long long)U * (blockIdx.x + 1) / C);
+            }
         } else {
             n_lut = header[HDR_NLUT];
             const int4 rg = fc1_range[blockIdx.x];  // computed by the schedule

@@ -78,6 +78,18 @@ def test_fp4_experts_single_token_non_resident_reported(torch):
     _check_layer(spec, 1, seed=17, resident=res)
 
 
+@pytest.mark.parametrize("H,I,T,E,k,fp4_top", [(512, 256, 2, 16, 4, 16), (1280, 384, 3, 64, 8, 64),
+                                                (4096, 2048, 2, 256, 8, 52), (768, 640, 3, 32, 6, 16),
+                                                (256, 128, 3, 4, 2, 4), (512, 256, 3, 16, 8, 8)])
+def test_fp4_experts_two_and_three_token_calls(torch, H, I, T, E, k, fp4_top):
+    # two tokens: the FP4 experts take the e2m1 tables, one pair per token,
+    # the pairs grouped by token (experts with two tokens among them), and no
+    # mma.sync launch is needed; three tokens: mma.sync for the FP4 experts,
+    # tables for the VQ2 ones
+    spec = ms.LayerSpec(H=H, I=I, E=E, k=k, seed=H + I + T + k, zipf_s=1.1, fp4_top=fp4_top)
+    _check_layer(spec, T, seed=T + k)
+
+
 @pytest.mark.parametrize("fp4_top", [0, 16])
 def test_single_token_no_resident_expert(torch, fp4_top):
     # a single-token call whose routed experts are all missing (VQ2-only
@@ -101,11 +113,11 @@ def test_fp4_table_pairs_fused_scatter_matches_per_pair(torch):
     import bit_vq_routed_gb300 as bv
     spec = ms.LayerSpec(H=1280, I=640, E=64, k=8, seed=31, fp4_top=64)
     layer = ms.Layer(spec)
-    x = ms.tokens(1, spec.H, seed=31)
-    dev, keep = device_layer(layer, 1)
+    x = ms.tokens(2, spec.H, seed=31)  # (two token groups of e2m1 pairs)
+    dev, keep = device_layer(layer, 2)
     g = run(dev, x)
     xt = torch.from_numpy(x).view(torch.bfloat16).cuda()
-    out = torch.zeros(1, spec.H, dtype=torch.float32, device="cuda")
+    out = torch.zeros(2, spec.H, dtype=torch.float32, device="cuda")
     dev.route(xt)
     dev.experts(xt, bv.MOE_FUSED_SCATTER, out)
     torch.cuda.synchronize()
