@@ -105,10 +105,9 @@ __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t& r0, uint32
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
-// ue8m0 exponent byte -> 2^(E-127) as fp32 (E = 0 gives the subnormal 2^-127)
-__device__ __forceinline__ float e8m0_to_float(uint32_t e) {
-    return e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);
-}
+// ue8m0 exponent byte -> 2^(E-127) as fp32 (E = 0 gives the subnormal 2^-127,
+// whose bit pattern 0x400000 lies below every E << 23 with E >= 1)
+__device__ __forceinline__ float e8m0_to_float(uint32_t e) { return __uint_as_float(max(e << 23, 0x00400000u)); }
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {

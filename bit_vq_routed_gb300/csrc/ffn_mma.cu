@@ -26,6 +26,11 @@
 namespace moe {
 namespace {
 
+template <int N>
+struct IntTag {
+    static constexpr int value = N;
+};
+
 constexpr int WARPS = 8;
 constexpr int THREADS = 32 * WARPS;
 constexpr int CB_COPIES = 16;
@@ -220,52 +225,64 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_, WIDE_>::MIN_BLOCKS)
                     }
                 }
             } else if constexpr (NTOK == MMA_NT_FP4) {
-                for (int kt = 0; kt < kn / 64; ++kt) {
+                // NA: the n8 tiles that hold tokens of this chunk (a compile-time
+                // count, so that the block-scale products and the zeroed partial
+                // sums of the empty tiles are not computed); the 64-element tiles
+                // of a slab two per pass, so that one's loads and conversions
+                // overlap the other's MMAs
+                auto fp4_slab = [&](auto na_tag) {
+                    constexpr int NA = decltype(na_tag)::value;
+#pragma unroll 2
+                    for (int kt = 0; kt < kn / 64; ++kt) {
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {  // 32-element scale blocks
-                        float tmp[2][NNT][4];
+                        for (int half = 0; half < 2; ++half) {  // 32-element scale blocks
+                            float tmp[2][NA][4];
 #pragma unroll
-                        for (int t = 0; t < 2; ++t)
+                            for (int t = 0; t < 2; ++t)
 #pragma unroll
-                            for (int nt = 0; nt < NNT; ++nt)
+                                for (int nt = 0; nt < NA; ++nt)
 #pragma unroll
-                                for (int q = 0; q < 4; ++q) tmp[t][nt][q] = 0.0f;
+                                    for (int q = 0; q < 4; ++q) tmp[t][nt][q] = 0.0f;
 #pragma unroll
-                        for (int s2 = 0; s2 < 2; ++s2) {
-                            const int s = 2 * half + s2;
-                            const int e0 = kt * 64 + 16 * s + 2 * j;  // element of k-slot 2j
-                            uint32_t b0[NNT], b1[NNT];
+                            for (int s2 = 0; s2 < 2; ++s2) {
+                                const int s = 2 * half + s2;
+                                const int e0 = kt * 64 + 16 * s + 2 * j;  // element of k-slot 2j
+                                uint32_t b0[NA], b1[NA];
 #pragma unroll
-                            for (int nt = 0; nt < NNT; ++nt)
-                                if (nt < n_nt) {
+                                for (int nt = 0; nt < NA; ++nt) {
                                     b0[nt] = sh_u32(xs + (8 * nt + i) * XSTRIDE + 2 * e0);
                                     b1[nt] = sh_u32(xs + (8 * nt + i) * XSTRIDE + 2 * (e0 + 8));
                                 }
 #pragma unroll
-                            for (int t = 0; t < 2; ++t) {
-                                const uint32_t w = sh_u32(wb + t * TILE_CODES + kt * 512 + 16 * lane + 4 * s);
-                                uint32_t r0, r1, r2, r3;  // row i lo-k, row i hi-k, row i+8 lo-k, row i+8 hi-k
-                                e2m1x8_to_f16x8(w, r0, r1, r2, r3);
+                                for (int t = 0; t < 2; ++t) {
+                                    const uint32_t w = sh_u32(wb + t * TILE_CODES + kt * 512 + 16 * lane + 4 * s);
+                                    uint32_t r0, r1, r2, r3;  // row i lo-k, row i hi-k, row i+8 lo-k, row i+8 hi-k
+                                    e2m1x8_to_f16x8(w, r0, r1, r2, r3);
 #pragma unroll
-                                for (int nt = 0; nt < NNT; ++nt)
-                                    if (nt < n_nt) mma_16816(tmp[t][nt], r0, r2, r1, r3, b0[nt], b1[nt]);
+                                    for (int nt = 0; nt < NA; ++nt) mma_16816(tmp[t][nt], r0, r2, r1, r3, b0[nt], b1[nt]);
+                                }
                             }
-                        }
 #pragma unroll
-                        for (int t = 0; t < 2; ++t) {
-                            const uint8_t* sa = wb + 2 * TILE_CODES + t * TILE_SCALES + (2 * kt + half) * 16;
-                            const uint32_t e_lo = sa[i], e_hi = sa[i + 8];
-                            const float s_lo = e8m0_to_float(e_lo), s_hi = e8m0_to_float(e_hi);
+                            for (int t = 0; t < 2; ++t) {
+                                const uint8_t* sa = wb + 2 * TILE_CODES + t * TILE_SCALES + (2 * kt + half) * 16;
+                                const uint32_t e_lo = sa[i], e_hi = sa[i + 8];
+                                const float s_lo = e8m0_to_float(e_lo), s_hi = e8m0_to_float(e_hi);
 #pragma unroll
-                            for (int nt = 0; nt < NNT; ++nt) {
-                                acc[t][nt][0] = fmaf(s_lo, tmp[t][nt][0], acc[t][nt][0]);
-                                acc[t][nt][1] = fmaf(s_lo, tmp[t][nt][1], acc[t][nt][1]);
-                                acc[t][nt][2] = fmaf(s_hi, tmp[t][nt][2], acc[t][nt][2]);
-                                acc[t][nt][3] = fmaf(s_hi, tmp[t][nt][3], acc[t][nt][3]);
+                                for (int nt = 0; nt < NA; ++nt) {
+                                    acc[t][nt][0] = fmaf(s_lo, tmp[t][nt][0], acc[t][nt][0]);
+                                    acc[t][nt][1] = fmaf(s_lo, tmp[t][nt][1], acc[t][nt][1]);
+                                    acc[t][nt][2] = fmaf(s_hi, tmp[t][nt][2], acc[t][nt][2]);
+                                    acc[t][nt][3] = fmaf(s_hi, tmp[t][nt][3], acc[t][nt][3]);
+                                }
                             }
                         }
                     }
-                }
+                };
+                static_assert(NNT == 2, "FP4 chunks: one or two n8 tiles");
+                if (n_nt == 1)
+                    fp4_slab(IntTag<1>{});
+                else
+                    fp4_slab(IntTag<2>{});
             }
             __syncthreads();  // buffer buf is free for the copies of slab sl + 2
         }
