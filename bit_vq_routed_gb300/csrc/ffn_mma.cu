@@ -49,6 +49,9 @@ struct MmaCfg {
     static constexpr int NNT = NTOK / 8;                 // n8 MMA tiles per chunk
     static constexpr int SLAB = WIDE_ ? 512 : 256;       // inputs per slab (VQ2; FP4 slabs are half as many)
     static constexpr int XSTRIDE = 2 * SLAB + 32;        // bytes per token row of a slab (padding: B-fragment banks)
+    // FP4 slabs (SLAB / 2 inputs): rows 4 banks apart, so that the 8 rows x 4
+    // k-pairs of a warp's 32-bit B loads hit 32 distinct banks
+    static constexpr int XSTRIDE_F4 = SLAB + 16;
     static constexpr int TILE_CODES = 4 * SLAB;          // one 16-row tile x one slab
     static constexpr int TILE_SCALES = SLAB / 4;         // 16 rows x SLAB/128 fp16 (VQ2) or x SLAB/64 ue8m0 (FP4)
     static constexpr int WARP_BYTES = 2 * (TILE_CODES + TILE_SCALES);  // per warp per slab (two tiles)
@@ -93,6 +96,8 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_, WIDE_>::MIN_BLOCKS)
     using Cfg = MmaCfg<NTOK_, WIDE_>;
     using Smem = typename Cfg::Smem;
     constexpr int NTOK = Cfg::NTOK, NNT = Cfg::NNT, SLAB = Cfg::SLAB, XSTRIDE = Cfg::XSTRIDE;
+    constexpr int XSTRIDE_F4 = Cfg::XSTRIDE_F4;
+    static_assert(XSTRIDE_F4 % 16 == 0 && (XSTRIDE_F4 / 4) % 8 == 4, "FP4 row stride: 16-byte rows, 4 banks apart");
     constexpr int TILE_CODES = Cfg::TILE_CODES, TILE_SCALES = Cfg::TILE_SCALES;
     extern __shared__ __align__(16) uint8_t dyn[];
     Smem& S = *reinterpret_cast<Smem*>(dyn);
@@ -138,6 +143,7 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_, WIDE_>::MIN_BLOCKS)
         const int KT = vq2 ? K / 128 : K / 64;  // 512-byte code tiles per row tile
         const int slab_in = vq2 ? SLAB : SLAB / 2;
         const int nslab = (K + slab_in - 1) / slab_in;
+        const int xstride = vq2 ? XSTRIDE : XSTRIDE_F4;
 
         // issue the cp.async copies of slab sl into buffer sl & 1
         auto issue = [&](int sl) {
@@ -149,7 +155,7 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_, WIDE_>::MIN_BLOCKS)
                 const int n = idx / chunks_per_row, c = idx - n * chunks_per_row;
                 const bool valid = n < ch.count;
                 const uint16_t* src = bsrc + (size_t)(ch.start + (valid ? n : 0)) * K + k0 + 8 * c;
-                cp_async16(smem_u32(&S.xs[buf][n * XSTRIDE + 16 * c]), src, valid);
+                cp_async16(smem_u32(&S.xs[buf][n * xstride + 16 * c]), src, valid);
             }
             // this warp's code tiles and scales
             uint8_t* wb = &S.w[buf][warp][0];
@@ -234,6 +240,11 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_, WIDE_>::MIN_BLOCKS)
                     constexpr int NA = decltype(na_tag)::value;
 #pragma unroll 2
                     for (int kt = 0; kt < kn / 64; ++kt) {
+                        // this lane's 16 code bytes of each tile (4 words: s = 0..3)
+                        uint4 wv[2];
+#pragma unroll
+                        for (int t = 0; t < 2; ++t)
+                            wv[t] = *reinterpret_cast<const uint4*>(wb + t * TILE_CODES + kt * 512 + 16 * lane);
 #pragma unroll
                         for (int half = 0; half < 2; ++half) {  // 32-element scale blocks
                             float tmp[2][NA][4];
@@ -250,12 +261,12 @@ __global__ void __launch_bounds__(THREADS, MmaCfg<NTOK_, WIDE_>::MIN_BLOCKS)
                                 uint32_t b0[NA], b1[NA];
 #pragma unroll
                                 for (int nt = 0; nt < NA; ++nt) {
-                                    b0[nt] = sh_u32(xs + (8 * nt + i) * XSTRIDE + 2 * e0);
-                                    b1[nt] = sh_u32(xs + (8 * nt + i) * XSTRIDE + 2 * (e0 + 8));
+                                    b0[nt] = sh_u32(xs + (8 * nt + i) * XSTRIDE_F4 + 2 * e0);
+                                    b1[nt] = sh_u32(xs + (8 * nt + i) * XSTRIDE_F4 + 2 * (e0 + 8));
                                 }
 #pragma unroll
                                 for (int t = 0; t < 2; ++t) {
-                                    const uint32_t w = sh_u32(wb + t * TILE_CODES + kt * 512 + 16 * lane + 4 * s);
+                                    const uint32_t w = (&wv[t].x)[s];
                                     uint32_t r0, r1, r2, r3;  // row i lo-k, row i hi-k, row i+8 lo-k, row i+8 hi-k
                                     e2m1x8_to_f16x8(w, r0, r1, r2, r3);
 #pragma unroll
