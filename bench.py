@@ -47,13 +47,13 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM bytes (read + write) of one expert-FFN call, from one ncu capture of its
 # kernels (the two single-token table kernels, ffn_lut_kernel<1,1,0> and
 # ffn_lut_kernel<0,1,0>, of `python bench.py --layers 1 --steps 3 --warmup 3
-# --no-cpu` under ncu: FC1 35,730,176 + 5,376, FC2 18,554,112 at decode batch 1).
+# --no-cpu` under ncu: FC1 35,727,104 + 3,840, FC2 18,553,600 at decode batch 1).
 # Reported only while the kernel sources hash to the ones the counters were
 # taken on.
-TRAFFIC = {"decode_b1": {"bytes": 54_289_664,
+TRAFFIC = {"decode_b1": {"bytes": 54_284_544,
                          "profile": "ncu capture of ffn_lut_kernel<1,1,0> and ffn_lut_kernel<0,1,0>, decode batch 1",
                          "sources": ["ffn_lut.cu", "lut_core.cuh", "ffn_common.cuh", "common.cuh"],
-                         "sha256": "0b338d3b4c66ace46e4d7280241e02552a11ca0eeeb7e2b8a06365b8af983b70"}}
+                         "sha256": "f7c9da1c67fb7deff07fb7718e802801a570bf36bf8170b5b5b9861c42e8ae6e"}}
 
 
 # Workloads whose bench figure averages many token batches (different expert
