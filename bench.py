@@ -53,7 +53,7 @@ L2_BYTES = 129 * 2 ** 20
 TRAFFIC = {"decode_b1": {"bytes": 54_284_544,
                          "profile": "ncu capture of ffn_lut_kernel<1,1,0> and ffn_lut_kernel<0,1,0>, decode batch 1",
                          "sources": ["ffn_lut.cu", "lut_core.cuh", "ffn_common.cuh", "common.cuh"],
-                         "sha256": "f7c9da1c67fb7deff07fb7718e802801a570bf36bf8170b5b5b9861c42e8ae6e"}}
+                         "sha256": "2bc094d1ca2286e792616d0bb15966f43e4638ecabdddaf85b027c9169b2f2aa"}}
 
 
 # Workloads whose bench figure averages many token batches (different expert

@@ -1,8 +1,8 @@
 // Activation-table path of the expert FFN, for VQ2 experts that receive at
 // most LUT_MAX_M tokens in this call (every expert at decode batch 1, most of
 // them at small batches): one table pair per (token, expert), the expert's
-// codes streamed once per token.  In single-token calls the FP4 experts take
-// the same kernels with e2m1 tables (the F4 instances).
+// codes streamed once per token.  In calls of one or two tokens the FP4 experts
+// take the same kernels with e2m1 tables (the F4 instances).
 //
 // The table, the lane layout and the per-unit lookups are the shared core in
 // lut_core.cuh.
