@@ -44,6 +44,17 @@ def test_tiny_layer_fp4_experts(torch):
     _check_layer(spec, 4, seed=1)
 
 
+@pytest.mark.parametrize("T", [3, 8, 9, 16, 17, 31])
+def test_experts_at_chunk_and_tile_boundaries(torch, T):
+    """Every token routes to all three experts (E = k = 3), so each expert gets
+    exactly T tokens: the FP4 expert's 16-token chunks hold one n8 tile of
+    tokens up to 8 and two from 9, with a second chunk from 17; the two VQ2
+    experts take the table path at 3 tokens, then the 32-token mma.sync
+    chunks (one to four n8 tiles)."""
+    spec = ms.LayerSpec(H=512, I=256, E=3, k=3, seed=40 + T, fp4_top=1)
+    _check_layer(spec, T, seed=T)
+
+
 @pytest.mark.parametrize("T,E,k", [(1, 8, 2), (37, 4, 2), (5, 16, 3), (64, 8, 8), (3, 1, 1), (17, 32, 1)])
 def test_ragged_and_degenerate_shapes(torch, T, E, k):
     spec = ms.LayerSpec(H=256, I=128, E=E, k=k, seed=T + 10 * E + k)
