@@ -53,7 +53,7 @@ L2_BYTES = 129 * 2 ** 20
 TRAFFIC = {"decode_b1": {"bytes": 54_284_544,
                          "profile": "ncu capture of ffn_lut_kernel<1,1,0> and ffn_lut_kernel<0,1,0>, decode batch 1",
                          "sources": ["ffn_lut.cu", "lut_core.cuh", "ffn_common.cuh", "common.cuh"],
-                         "sha256": "2bc094d1ca2286e792616d0bb15966f43e4638ecabdddaf85b027c9169b2f2aa"}}
+                         "sha256": "2b0d38e17623b08719a47955646d2b6e7ffa9c2e9bc753a007b5f37e221598d8"}}
 
 
 # Workloads whose bench figure averages many token batches (different expert

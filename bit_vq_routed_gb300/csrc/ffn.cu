@@ -334,6 +334,8 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     // table path takes, so the mma.sync kernels only have work if FP4
     // experts do not take the e2m1 tables.
     const bool mma = T > lut_max_m || (t->n_fp4 > 0 && !use_lut4);
+    // (and VQ2 experts only reach them, in 32-token chunks, above lut_max_m)
+    const bool mma_vq2 = T > lut_max_m;
     const int split16 = T >= MMA_SPLIT_T ? 1 : 0;
 
     moe_status st;
@@ -363,7 +365,7 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     if (use_lut4 && (st = launch_lut_fc(true, false, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w,
                                         L, s, nullptr, nullptr, nullptr, true)) != MOE_OK)
         return st;
-    if (mma && (st = launch_mma_fc(true, t, sorted_pair, weights, k, mode, out, w, L, s, split16)) != MOE_OK) return st;
+    if (mma && (st = launch_mma_fc(true, t, sorted_pair, weights, k, mode, out, w, L, s, split16, mma_vq2)) != MOE_OK) return st;
     if (use_umma && (st = launch_umma(true, t, sorted_pair, weights, k, P, mode, out, w, L, s)) != MOE_OK) return st;
     if ((mma || use_umma) && (st = launch_a_to_f16(P, I, w, L, s)) != MOE_OK) return st;
     if (use_lut &&
@@ -373,7 +375,7 @@ moe_status launch_expert_ffn(const SlotTableHost* t, const uint16_t* x, const in
     if (use_lut4 && (st = launch_lut_fc(false, false, t, x, offsets, sorted_pair, weights, k, P, mode, out, status, w,
                                         L, s, nullptr, nullptr, nullptr, true)) != MOE_OK)
         return st;
-    if (mma && (st = launch_mma_fc(false, t, sorted_pair, weights, k, mode, out, w, L, s, split16)) != MOE_OK) return st;
+    if (mma && (st = launch_mma_fc(false, t, sorted_pair, weights, k, mode, out, w, L, s, split16, mma_vq2)) != MOE_OK) return st;
     if (use_umma && (st = launch_umma(false, t, sorted_pair, weights, k, P, mode, out, w, L, s)) != MOE_OK) return st;
     if (comb) return launch_combine(out, pair_to_sorted, weights, status, T, k, H, comb32, comb16, s);
     return MOE_OK;

@@ -183,5 +183,5 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(
 moe_status launch_umma(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
                        int P, int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s);
 moe_status launch_mma_fc(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
-                         int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s, bool split16);
+                         int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s, bool split16, bool vq2);
 }  // namespace moe

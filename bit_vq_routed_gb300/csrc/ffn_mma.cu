@@ -362,10 +362,13 @@ static moe_status launch_mma_cfg(bool fc1, const SlotTableHost* t, const int32_t
 }
 
 moe_status launch_mma_fc(bool fc1, const SlotTableHost* t, const int32_t* sorted_pair, const float* weights, int k,
-                         int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s, bool split16) {
-    // (split16 is set exactly for the calls of at least MMA_SPLIT_T tokens)
-    moe_status st = split16 ? launch_mma_cfg<MMA_NT_VQ2, true>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s)
-                            : launch_mma_cfg<MMA_NT_VQ2, false>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s);
+                         int mode, float* out, char* ws, const WsLayout& L, cudaStream_t s, bool split16, bool vq2) {
+    // (split16 is set exactly for the calls of at least MMA_SPLIT_T tokens;
+    // vq2: the call can have VQ2 experts in 32-token chunks)
+    moe_status st = MOE_OK;
+    if (vq2)
+        st = split16 ? launch_mma_cfg<MMA_NT_VQ2, true>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s)
+                     : launch_mma_cfg<MMA_NT_VQ2, false>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s);
     if (st == MOE_OK && (t->n_fp4 > 0 || split16))
         st = launch_mma_cfg<MMA_NT_FP4, false>(fc1, t, sorted_pair, weights, k, mode, out, ws, L, s);
     return st;
