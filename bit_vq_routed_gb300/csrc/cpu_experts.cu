@@ -11,13 +11,18 @@
 // the 4 inputs of the group (one 4-wide multiply-add per code, in portable
 // vector C++ that the compiler maps to NEON on aarch64 and SSE on x86-64);
 // each row's sum over a 128-input block is scaled by the row's fp16 scale.
-// FC1 (gate, up), silu(g) * u and FC2 run in fp32 over a pool of host threads
-// (items: a 16-row tile of one matrix for every token of one expert), then
-// the remainder of the combine is summed per token in pair order.
+// FC1 (gate, up) with silu(g) * u, then FC2 with the remainder of the
+// combine, run in fp32 as two parallel steps over a pool of host threads
+// (items: 16 rows of gate and up of one expert for all its tokens; 16 rows
+// of every listed expert's down matrix for all tokens, then those rows of
+// each token's remainder summed in pair order).  The pool's threads poll for
+// work for a while before they sleep, so that a call's steps do not pay a
+// wake-up each.
 #include <cmath>
 #include <cstring>
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <condition_variable>
 #include <functional>
 #include <mutex>
@@ -72,9 +77,14 @@ void vq2_tile_rows(const uint8_t* codes, const uint16_t* scales, int K, int rt, 
         f4 acc[16];
         for (int b = 0; b < 16; ++b) acc[b] = f4{0.f, 0.f, 0.f, 0.f};
         for (int g = 0; g < 32; ++g) {
-            const uint8_t* cw = tile + 16 * g;  // byte 2i + h: row i + 8h
+            // byte 2i + h of the chunk: row i + 8h (two 8-byte loads; the
+            // bytes taken out with shifts, little-endian on both hosts)
+            uint64_t w0, w1;
+            std::memcpy(&w0, tile + 16 * g, 8);
+            std::memcpy(&w1, tile + 16 * g + 8, 8);
             const f4 x = xv[g];
-            for (int b = 0; b < 16; ++b) acc[b] += cbs[cw[b]] * x;
+            for (int b = 0; b < 8; ++b) acc[b] += cbs[(w0 >> (8 * b)) & 0xffu] * x;
+            for (int b = 0; b < 8; ++b) acc[8 + b] += cbs[(w1 >> (8 * b)) & 0xffu] * x;
         }
         for (int b = 0; b < 16; ++b) {
             const int row = (b >> 1) + 8 * (b & 1);
@@ -82,6 +92,15 @@ void vq2_tile_rows(const uint8_t* codes, const uint16_t* scales, int K, int rt, 
         }
     }
     for (int r = 0; r < 16; ++r) y16[r] = tot[r];
+}
+
+// ue8m0 byte e -> 2^(e - 127), exactly (e = 0: the subnormal 2^-127, bits
+// 0x400000; e = 255: infinity).
+inline float e8m0_value(uint8_t e) {
+    const uint32_t u = e ? (uint32_t)e << 23 : 0x00400000u;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return f;
 }
 
 // The same for one FP4 matrix (packed: 64-element tiles, ue8m0 scale per 32).
@@ -101,7 +120,7 @@ void fp4_tile_rows(const uint8_t* codes, const uint8_t* scales, int K, int rt, c
             }
             for (int h = 0; h < 2; ++h) {
                 const uint8_t e = scales[((size_t)rt * KB + 2 * kt + h) * 16 + r16];
-                tot[r16] += part[h] * std::ldexp(1.0f, (int)e - 127);
+                tot[r16] += part[h] * e8m0_value(e);
             }
         }
     }
@@ -116,46 +135,76 @@ struct moe_cpu_pool {
     std::vector<std::thread> workers;
     std::mutex mu;
     std::condition_variable go, done;
-    std::function<void(int)> fn;
+    const std::function<void(int)>* fn = nullptr;
     int n_items = 0;
     std::atomic<int> next{0};
-    int busy = 0;           // workers still on the current job
-    unsigned long gen = 0;  // job generation
-    bool stop = false;
+    std::atomic<int> remaining{0};      // workers still on the current job
+    std::atomic<unsigned long> gen{0};  // job generation
+    std::atomic<bool> stop{false};
+    int sleepers = 0;              // workers blocked on `go` (under mu)
+    bool caller_sleeping = false;  // the caller blocked on `done` (under mu)
+    // how long a worker polls for the next job (and the caller for the end
+    // of one) before it blocks: longer than the steps of a call and the GPU
+    // work between two calls of a decode loop, so that a call pays no wake-up
+    static constexpr long long SPIN_NS = 2000000;
+    template <class Pred>
+    static bool poll(Pred ready) {
+        const auto end = std::chrono::steady_clock::now() + std::chrono::nanoseconds(SPIN_NS);
+        for (unsigned i = 1;; ++i) {
+            if (ready()) return true;
+            if ((i & 255u) == 0 && std::chrono::steady_clock::now() > end) return ready();
+        }
+    }
 
     void work() {
         unsigned long seen = 0;
         for (;;) {
-            std::function<void(int)> f;
-            int n;
-            {
+            poll([&] { return gen.load(std::memory_order_acquire) != seen || stop.load(std::memory_order_relaxed); });
+            unsigned long g = gen.load(std::memory_order_acquire);
+            if (g == seen && !stop.load()) {
                 std::unique_lock<std::mutex> lk(mu);
-                go.wait(lk, [&] { return stop || gen != seen; });
-                if (stop) return;
-                seen = gen;
-                f = fn;
-                n = n_items;
+                ++sleepers;
+                go.wait(lk, [&] { return stop.load() || gen.load(std::memory_order_acquire) != seen; });
+                --sleepers;
+                g = gen.load(std::memory_order_acquire);
             }
+            if (stop.load()) return;
+            seen = g;
+            // (fn and n_items were written before the generation was published)
+            const std::function<void(int)>& f = *fn;
+            const int n = n_items;
             for (int i = next.fetch_add(1); i < n; i = next.fetch_add(1)) f(i);
-            std::lock_guard<std::mutex> lk(mu);
-            if (--busy == 0) done.notify_all();
+            if (remaining.fetch_sub(1, std::memory_order_acq_rel) == 1) {
+                std::lock_guard<std::mutex> lk(mu);
+                if (caller_sleeping) done.notify_all();
+            }
         }
     }
     // Runs f(0..n-1) over the workers and the calling thread; returns when all are done.
     void parallel_for(int n, const std::function<void(int)>& f) {
         if (n <= 0) return;
+        if (workers.empty() || n == 1) {
+            for (int i = 0; i < n; ++i) f(i);
+            return;
+        }
+        // every worker has left the previous job (remaining reached 0 after
+        // its last claim of an item)
+        fn = &f;
+        n_items = n;
+        next.store(0, std::memory_order_relaxed);
+        remaining.store((int)workers.size(), std::memory_order_relaxed);
+        gen.fetch_add(1, std::memory_order_release);
         {
             std::lock_guard<std::mutex> lk(mu);
-            fn = f;
-            n_items = n;
-            next.store(0);
-            busy = (int)workers.size();
-            ++gen;
+            if (sleepers) go.notify_all();
         }
-        go.notify_all();
         for (int i = next.fetch_add(1); i < n; i = next.fetch_add(1)) f(i);
-        std::unique_lock<std::mutex> lk(mu);
-        done.wait(lk, [&] { return busy == 0; });
+        if (!poll([&] { return remaining.load(std::memory_order_acquire) == 0; })) {
+            std::unique_lock<std::mutex> lk(mu);
+            caller_sleeping = true;
+            done.wait(lk, [&] { return remaining.load(std::memory_order_acquire) == 0; });
+            caller_sleeping = false;
+        }
     }
 };
 
@@ -179,7 +228,7 @@ moe_status moe_cpu_pool_create(int threads, moe_cpu_pool** out) {
     } catch (...) {
         {
             std::lock_guard<std::mutex> lk(p->mu);
-            p->stop = true;
+            p->stop.store(true);
         }
         p->go.notify_all();
         for (auto& w : p->workers) w.join();
@@ -197,7 +246,7 @@ moe_status moe_cpu_pool_destroy(moe_cpu_pool* pool) {
     if (!pool) return MOE_OK;
     {
         std::lock_guard<std::mutex> lk(pool->mu);
-        pool->stop = true;
+        pool->stop.store(true);
     }
     pool->go.notify_all();
     for (auto& w : pool->workers) w.join();
@@ -247,67 +296,62 @@ moe_status moe_cpu_expert_ffn(moe_cpu_pool* pool, int H, int I, const uint16_t* 
             for (int q = 0; q < 4; ++q) cbsv[4 * c + q] = sg * fp16_to_f32(codebook[4 * (c & 127) + q]);
         }
         const f4* cbs = reinterpret_cast<const f4*>(cbsv.data());
-        // inputs of the listed pairs in fp32 (pair order of `order`)
-        std::vector<float> xin((size_t)n_pairs * H), a((size_t)n_pairs * I);
-        std::vector<float> g((size_t)n_pairs * 2 * I), y((size_t)n_pairs * H);
-        pool->parallel_for(n_pairs, [&](int q) {
+        // inputs of the listed pairs in fp32 (pair order of `order`); a few
+        // pairs on this thread
+        std::vector<float> xin((size_t)n_pairs * H), a((size_t)n_pairs * I), y((size_t)n_pairs * H);
+        auto to_f32 = [&](int q) {
             const uint16_t* xr = x + (size_t)(order[q] / k) * H;
             float* dst = &xin[(size_t)q * H];
             for (int i = 0; i < H; ++i) dst[i] = bf16_to_f32(xr[i]);
-        });
-        // FC1: items (expert, 16-row tile of gate and up rows)
-        const int rt1 = 2 * I / 16;
-        const int n1 = (int)experts_used.size() * rt1;
-        pool->parallel_for(n1, [&](int it) {
+        };
+        if ((size_t)n_pairs * H <= ((size_t)1 << 16)) {
+            for (int q = 0; q < n_pairs; ++q) to_f32(q);
+        } else {
+            pool->parallel_for(n_pairs, to_f32);
+        }
+        auto tile_rows = [&](const moe_expert_desc& d, int mtx, int K, int rt, const float* v, float* y16) {
+            if (d.format == MOE_FMT_VQ2)
+                vq2_tile_rows(static_cast<const uint8_t*>(d.codes[mtx]), static_cast<const uint16_t*>(d.scales[mtx]), K,
+                              rt, cbs, reinterpret_cast<const f4*>(v), y16);
+            else
+                fp4_tile_rows(static_cast<const uint8_t*>(d.codes[mtx]), static_cast<const uint8_t*>(d.scales[mtx]), K,
+                              rt, v, y16);
+        };
+        // FC1 and a = silu(g) * u: items (expert, 16 rows of gate and up)
+        const int rt1 = I / 16;
+        pool->parallel_for((int)experts_used.size() * rt1, [&](int it) {
             const int e = experts_used[it / rt1], rt = it % rt1;
             const moe_expert_desc& d = experts[e];
-            const int mtx = rt < I / 16 ? 0 : 1, rtm = rt - mtx * (I / 16);
-            float y16[16];
+            float g16[16], u16[16];
             for (int q = cnt[e]; q < cnt[e + 1]; ++q) {
-                const f4* v4 = reinterpret_cast<const f4*>(&xin[(size_t)q * H]);
-                if (d.format == MOE_FMT_VQ2)
-                    vq2_tile_rows(static_cast<const uint8_t*>(d.codes[mtx]), static_cast<const uint16_t*>(d.scales[mtx]),
-                                  H, rtm, cbs, v4, y16);
-                else
-                    fp4_tile_rows(static_cast<const uint8_t*>(d.codes[mtx]), static_cast<const uint8_t*>(d.scales[mtx]),
-                                  H, rtm, reinterpret_cast<const float*>(v4), y16);
-                std::memcpy(&g[(size_t)q * 2 * I + mtx * I + 16 * rtm], y16, sizeof y16);
+                const float* xq = &xin[(size_t)q * H];
+                tile_rows(d, 0, H, rt, xq, g16);
+                tile_rows(d, 1, H, rt, xq, u16);
+                float* aq = &a[(size_t)q * I + 16 * rt];
+                for (int r = 0; r < 16; ++r) aq[r] = g16[r] / (1.0f + std::exp(-g16[r])) * u16[r];
             }
         });
-        // a = silu(g) * u
-        pool->parallel_for(n_pairs, [&](int q) {
-            const float* gq = &g[(size_t)q * 2 * I];
-            float* aq = &a[(size_t)q * I];
-            for (int i = 0; i < I; ++i) aq[i] = gq[i] / (1.0f + std::exp(-gq[i])) * gq[I + i];
-        });
-        // FC2: items (expert, 16-row tile of down rows)
-        const int rt2 = H / 16;
-        pool->parallel_for((int)experts_used.size() * rt2, [&](int it) {
-            const int e = experts_used[it / rt2], rt = it % rt2;
-            const moe_expert_desc& d = experts[e];
-            for (int q = cnt[e]; q < cnt[e + 1]; ++q) {
-                const f4* a4 = reinterpret_cast<const f4*>(&a[(size_t)q * I]);
-                float* yq = &y[(size_t)q * H + 16 * rt];
-                if (d.format == MOE_FMT_VQ2)
-                    vq2_tile_rows(static_cast<const uint8_t*>(d.codes[2]), static_cast<const uint16_t*>(d.scales[2]), I,
-                                  rt, cbs, a4, yq);
-                else
-                    fp4_tile_rows(static_cast<const uint8_t*>(d.codes[2]), static_cast<const uint8_t*>(d.scales[2]), I,
-                                  rt, reinterpret_cast<const float*>(a4), yq);
-            }
-        });
-        // the remainder of the combine, per token in pair order
+        // FC2 and the remainder of the combine: items (16 rows of H) over
+        // every listed expert and pair, then those rows of each token's
+        // remainder, summed in pair order
         std::vector<int> q_of(P, -1);
         for (int q = 0; q < n_pairs; ++q) q_of[order[q]] = q;
-        pool->parallel_for(T, [&](int t) {
-            float* o = out + (size_t)t * H;
-            std::fill(o, o + H, 0.0f);
-            for (int j = 0; j < k; ++j) {
-                const int q = q_of[t * k + j];
-                if (q < 0) continue;
-                const float w = weights[t * k + j];
-                const float* yq = &y[(size_t)q * H];
-                for (int h = 0; h < H; ++h) o[h] += w * yq[h];
+        pool->parallel_for(H / 16, [&](int rt) {
+            for (int e : experts_used) {
+                const moe_expert_desc& d = experts[e];
+                for (int q = cnt[e]; q < cnt[e + 1]; ++q)
+                    tile_rows(d, 2, I, rt, &a[(size_t)q * I], &y[(size_t)q * H + 16 * rt]);
+            }
+            for (int t = 0; t < T; ++t) {
+                float* o = out + (size_t)t * H + 16 * rt;
+                for (int r = 0; r < 16; ++r) o[r] = 0.0f;
+                for (int j = 0; j < k; ++j) {
+                    const int q = q_of[t * k + j];
+                    if (q < 0) continue;
+                    const float w = weights[t * k + j];
+                    const float* yq = &y[(size_t)q * H + 16 * rt];
+                    for (int r = 0; r < 16; ++r) o[r] += w * yq[r];
+                }
             }
         });
     } catch (const std::bad_alloc&) {
